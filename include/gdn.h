@@ -1,0 +1,144 @@
+/*
+ * gdn.h -- C ABI of libgdn.so, a GB300 (sm_103a) implementation of the Gated DeltaNet (GDN)
+ * linear-attention recurrence.
+ *
+ * WHAT IS COMPUTED
+ *   logicaffeine_compile::codegen_cuda::gdn (module description): every value head keeps a
+ *   Dv x Dk f32 memory S and, per token,
+ *       u = S k^                              (prediction from the OLD memory)
+ *       S = alpha S + beta (v - alpha u) k^T  (decay, then correct by the prediction error)
+ *       o = S q^                              (read of the UPDATED memory)
+ *       y = rmsnorm(o * silu(z)) * GN         (gate first, then normalise over the head)
+ *   The kernels evaluate o with the single-pass identity of that page's "The fusion"
+ *   section, o[a] = alpha (S_old q^)[a] + coef[a] (k^ . q^), coef[a] = beta (v[a] - alpha u[a]),
+ *   so each state row is read once and written once per token.
+ *
+ *   torch_to_nnef.op.gated_delta, native_gdn_reject_reason: q and k are l2-normalised and the
+ *   1/sqrt(head_dim) scale is folded in:
+ *       k^ = k / sqrt(sum k^2 + qk_eps),   q^ = q / sqrt(sum q^2 + qk_eps) / sqrt(Dk).
+ *   alpha = exp(log_decay); beta is used as given.  rmsnorm: x / sqrt(mean x^2 + norm_eps).
+ *   Value head hv reads key head hv / (Hv / Hk) (modelopt.torch.puzzletron.pruning.
+ *   gated_delta_net, GDNShape.value_heads_per_group).
+ *
+ * LAYOUTS  (torch_to_nnef.op.gated_delta, emit_native_gdn_recurrent; all dense row-major)
+ *   head_major = 0:  q,k [B,S,Hk,Dk]   v,z,y [B,S,Hv,Dv]   log_decay,beta [B,S,Hv]
+ *   head_major = 1:  q,k [B,Hk,S,Dk]   v,z,y [B,Hv,S,Dv]   log_decay,beta [B,Hv,S]
+ *   state, s0:       [B,Hv,Dv,Dk] f32, row = value index, column = key index.
+ *   gn:              [Dv] f32.
+ *   y is always f32: the promoted type of gated_delta_fake on the same page (the memory is
+ *   f32 even for a 16-bit model).
+ *
+ * OWNERSHIP
+ *   The caller owns every buffer and every pointer is a DEVICE pointer (the stream's device).
+ *   The library allocates nothing, keeps no state between calls and never copies to the
+ *   host.  Work is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *   default stream) and is asynchronous: results are ready when the stream is.
+ *
+ * ERRORS
+ *   Every entry point validates its arguments on the host BEFORE enqueuing anything and
+ *   returns a negative gdn_status on failure, with nothing enqueued and no buffer touched.
+ *   A launch failure returns GDN_ERR_CUDA (text from gdn_last_error()).  Faults during
+ *   kernel execution surface at the caller's next synchronisation, as usual for CUDA.
+ *   There is no fallback path of any kind.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_VERSION 1
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+typedef enum {
+    GDN_F32 = 0,
+    GDN_BF16 = 1,
+    GDN_F16 = 2
+} gdn_dtype;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL_PTR = -1,        /* a required pointer is NULL, or z/gn only one given     */
+    GDN_ERR_BAD_SHAPE = -2,       /* dims < 0 or heads < 1, Hv % Hk != 0, S != 1 on decode   */
+    GDN_ERR_UNSUPPORTED_DIM = -3, /* Dk, Dv not in {16,32,64,128} or Dk != Dv               */
+    GDN_ERR_BAD_DTYPE = -4,       /* unknown dtype, or gate dtype neither F32 nor act dtype  */
+    GDN_ERR_MISALIGNED = -5,      /* a pointer is not aligned (16 B; gates: element size)    */
+    GDN_ERR_ALIASING = -6,        /* y overlaps an operand, or state partially overlaps s0   */
+    GDN_ERR_BAD_ARG = -7,         /* eps negative or not finite; bad flag; size overflow     */
+    GDN_ERR_CUDA = -8             /* the CUDA runtime reported an error at launch            */
+} gdn_status;
+
+/* Operands of one call.  Shape fields follow GDNShape (num_key_heads = Hk, num_value_heads
+ * = Hv, key_head_dim = Dk, value_head_dim = Dv) plus batch B and sequence length S. */
+typedef struct gdn_params {
+    int32_t B, S, Hk, Hv, Dk, Dv;
+    int32_t head_major;       /* 0: [B,S,H,W] / [B,S,H] operands; 1: [B,H,S,W] / [B,H,S]     */
+    int32_t act_dtype;        /* gdn_dtype of q, k, v, z                                      */
+    int32_t gate_dtype;       /* gdn_dtype of log_decay and beta: GDN_F32 or act_dtype        */
+    int32_t reserved;         /* must be 0                                                    */
+    const void *q, *k;        /* [B,S,Hk,Dk] / [B,Hk,S,Dk]                                    */
+    const void *v;            /* [B,S,Hv,Dv] / [B,Hv,S,Dv]                                    */
+    const void *log_decay;    /* [B,S,Hv] / [B,Hv,S]                                          */
+    const void *beta;         /* [B,S,Hv] / [B,Hv,S]                                          */
+    const void *z;            /* like v; NULL together with gn: y = raw o (no gated norm)     */
+    const float *gn;          /* [Dv] f32 gated-norm weight; NULL together with z             */
+    const float *s0;          /* scan: initial memory [B,Hv,Dv,Dk]; NULL = zeros.
+                                 decode: ignored (the memory is `state`, updated in place)    */
+    float *state;             /* decode: memory, read and written in place.
+                                 scan: final memory out; may be the same pointer as s0        */
+    float *y;                 /* output, like v but f32; must not overlap any operand         */
+    float qk_eps;             /* l2-norm eps of q and k (1e-6 in the reference workloads)     */
+    float norm_eps;           /* rmsnorm eps (1e-6 in the reference workloads)                */
+} gdn_params;
+
+/*
+ * gdn_decode_step -- one token (S must be 1) for every (b, hv) head; `state` is read and
+ * written in place (one HBM read and one write of each state row).  At S == 1 the two
+ * layouts coincide, so head_major only has to be a valid flag.  B == 0 is a no-op.
+ * Source: logicaffeine codegen_cuda::gdn, "The fusion" and GDN_KERNELS; torch_to_nnef
+ * gated_delta, native_gdn_reject_reason (the fused operator is a single decode step).
+ */
+GDN_API int gdn_decode_step(const gdn_params *p, void *stream);
+
+/*
+ * gdn_scan -- the recurrence over the time axis, t = 0 .. S-1, from s0 (or zeros) to the
+ * final memory written to `state`; y receives every token's output.  Each head's memory
+ * stays on chip for the whole sequence.  S == 0 copies s0 (or zeros) into `state` and
+ * leaves y untouched; B == 0 is a no-op.  `state` may equal `s0` (in-place resume); any
+ * other overlap of the two is rejected.
+ * Source: torch_to_nnef gated_delta, gated_delta_reference (recurrence over the time axis)
+ * and emit_native_gdn_recurrent (operands and outputs); logicaffeine codegen_cuda::gdn.
+ */
+GDN_API int gdn_scan(const gdn_params *p, void *stream);
+
+/*
+ * gdn_reject_reason -- NULL when gdn_decode_step (is_decode != 0) or gdn_scan (is_decode
+ * == 0) would accept `p`, else a short static string naming the first failed check.
+ * Host-only; touches no device memory.
+ * Source: torch_to_nnef gated_delta, native_gdn_reject_reason (a reason string for logging;
+ * this library has no fallback to log it before).
+ */
+GDN_API const char *gdn_reject_reason(const gdn_params *p, int is_decode);
+
+/* gdn_status_string -- static text for a gdn_status value (unknown codes included). */
+GDN_API const char *gdn_status_string(int status);
+
+/* gdn_last_error -- text of the last GDN_ERR_CUDA seen by the calling thread ("" if none). */
+GDN_API const char *gdn_last_error(void);
+
+/* gdn_version -- GDN_VERSION of the loaded library. */
+GDN_API int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,1 +1,230 @@
-"""GB300-native Gated DeltaNet recurrence (placeholder; binding added with the C-ABI)."""
+"""GB300-native Gated DeltaNet (GDN) recurrence: Python binding of ``libgdn.so``.
+
+The functions here carry the names of the C entry points declared in ``include/gdn.h`` and
+only marshal arguments: tensors become device pointers and sizes, the current torch stream
+becomes the ``cudaStream_t``, and every step of the computation runs in the library's CUDA
+kernels.  There is no fallback: if ``libgdn.so`` is missing, or the call is rejected, the
+function raises.
+
+Computed (logicaffeine ``codegen_cuda::gdn``, module description and "The fusion"): per
+value head and token, ``u = S k^``, ``S = alpha S + beta (v - alpha u) k^T``, ``o = S q^``,
+``y = rmsnorm(o * silu(z)) * GN``, with ``k^``, ``q^`` l2-normalised and ``q^`` scaled by
+``1/sqrt(Dk)`` (torch_to_nnef ``gated_delta``, native_gdn_reject_reason) and
+``alpha = exp(log_decay)``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+LIBRARY = _build.LIBRARY
+
+GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
+_DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
+
+GDN_OK = 0
+GDN_ERR_NULL_PTR = -1
+GDN_ERR_BAD_SHAPE = -2
+GDN_ERR_UNSUPPORTED_DIM = -3
+GDN_ERR_BAD_DTYPE = -4
+GDN_ERR_MISALIGNED = -5
+GDN_ERR_ALIASING = -6
+GDN_ERR_BAD_ARG = -7
+GDN_ERR_CUDA = -8
+
+# Symbols declared in include/gdn.h (checked by the tests against the header).
+EXPORTED = ("gdn_decode_step", "gdn_scan", "gdn_reject_reason", "gdn_status_string",
+            "gdn_last_error", "gdn_version")
+
+
+class GdnParams(ctypes.Structure):
+    """ctypes mirror of ``gdn_params`` in include/gdn.h."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("S", ctypes.c_int32), ("Hk", ctypes.c_int32),
+        ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32), ("Dv", ctypes.c_int32),
+        ("head_major", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
+        ("gate_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("log_decay", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("gn", ctypes.c_void_p), ("s0", ctypes.c_void_p),
+        ("state", ctypes.c_void_p), ("y", ctypes.c_void_p),
+        ("qk_eps", ctypes.c_float), ("norm_eps", ctypes.c_float),
+    ]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+_lib = None
+
+
+def library(path: str | None = None) -> ctypes.CDLL:
+    """Load ``libgdn.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIBRARY
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it first (python -c 'import "
+                           "__graft_entry__ as g; g.build()'); there is no fallback path")
+    lib = ctypes.CDLL(p)
+    P = ctypes.POINTER(GdnParams)
+    lib.gdn_decode_step.argtypes = [P, ctypes.c_void_p]
+    lib.gdn_decode_step.restype = ctypes.c_int
+    lib.gdn_scan.argtypes = [P, ctypes.c_void_p]
+    lib.gdn_scan.restype = ctypes.c_int
+    lib.gdn_reject_reason.argtypes = [P, ctypes.c_int]
+    lib.gdn_reject_reason.restype = ctypes.c_char_p
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_last_error.argtypes = []
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_version.argtypes = []
+    lib.gdn_version.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def make_params(q, k, v, log_decay, beta, state, y, *, z=None, gn=None, s0=None,
+                head_major=False, qk_eps=1e-6, norm_eps=1e-6) -> GdnParams:
+    """Fill a :class:`GdnParams` from tensors (shapes read per ``head_major``).
+
+    Tensors must be contiguous; nothing is copied or converted here.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("log_decay", log_decay), ("beta", beta),
+                    ("state", state), ("y", y), ("z", z), ("gn", gn), ("s0", s0)):
+        if t is not None and not t.is_contiguous():
+            raise GdnError(GDN_ERR_BAD_ARG, f"{name} must be contiguous (no implicit copies)")
+    if q.dim() != 4 or v.dim() != 4 or state.dim() != 4:
+        raise GdnError(GDN_ERR_BAD_SHAPE, "q, k, v must be 4-D and state [B,Hv,Dv,Dk]")
+    if head_major:
+        B, Hk, S, Dk = q.shape
+        Hv, Dv = v.shape[1], v.shape[3]
+        expect_v = (B, Hv, S, Dv)
+        expect_g = (B, Hv, S)
+    else:
+        B, S, Hk, Dk = q.shape
+        Hv, Dv = v.shape[2], v.shape[3]
+        expect_v = (B, S, Hv, Dv)
+        expect_g = (B, S, Hv)
+    checks = [("k", k, tuple(q.shape)), ("v", v, expect_v), ("y", y, expect_v),
+              ("log_decay", log_decay, expect_g), ("beta", beta, expect_g),
+              ("state", state, (B, Hv, Dv, Dk))]
+    if z is not None:
+        checks.append(("z", z, expect_v))
+    if gn is not None:
+        checks.append(("gn", gn, (Dv,)))
+    if s0 is not None:
+        checks.append(("s0", s0, (B, Hv, Dv, Dk)))
+    for name, t, shape in checks:
+        if tuple(t.shape) != tuple(shape):
+            raise GdnError(GDN_ERR_BAD_SHAPE, f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    act = _DTYPE_CODE.get(q.dtype)
+    gate = _DTYPE_CODE.get(log_decay.dtype)
+    if act is None or gate is None:
+        raise GdnError(GDN_ERR_BAD_DTYPE, "q and log_decay must be float32, bfloat16 or float16")
+    for name, t in (("k", k), ("v", v), ("z", z)):
+        if t is not None and t.dtype != q.dtype:
+            raise GdnError(GDN_ERR_BAD_DTYPE, f"{name} must have q's dtype")
+    if beta.dtype != log_decay.dtype:
+        raise GdnError(GDN_ERR_BAD_DTYPE, "beta must have log_decay's dtype")
+    for name, t in (("state", state), ("y", y), ("gn", gn), ("s0", s0)):
+        if t is not None and t.dtype != torch.float32:
+            raise GdnError(GDN_ERR_BAD_DTYPE, f"{name} must be float32")
+    return GdnParams(B=B, S=S, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, head_major=int(bool(head_major)),
+                     act_dtype=act, gate_dtype=gate, reserved=0,
+                     q=_ptr(q), k=_ptr(k), v=_ptr(v), log_decay=_ptr(log_decay),
+                     beta=_ptr(beta), z=_ptr(z), gn=_ptr(gn), s0=_ptr(s0),
+                     state=_ptr(state), y=_ptr(y), qk_eps=qk_eps, norm_eps=norm_eps)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _raise(lib, status: int, params: GdnParams, is_decode: int):
+    if status == GDN_OK:
+        return
+    text = lib.gdn_status_string(status).decode()
+    reason = lib.gdn_reject_reason(ctypes.byref(params), is_decode)
+    detail = reason.decode() if reason else lib.gdn_last_error().decode()
+    raise GdnError(status, f"{text}: {detail}")
+
+
+def _require_cuda(*tensors):
+    for t in tensors:
+        if t is not None and not t.is_cuda:
+            raise GdnError(GDN_ERR_BAD_ARG, "all tensors must be CUDA tensors (no CPU path)")
+
+
+def gdn_decode_step(q, k, v, log_decay, beta, state, y=None, *, z=None, gn=None,
+                    head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None):
+    """One decode token (S == 1); ``state`` [B,Hv,Dv,Dk] f32 is updated in place.
+
+    Returns ``y`` (allocated with v's shape in f32 if not given).
+    """
+    _require_cuda(q, k, v, log_decay, beta, state, y, z, gn)
+    if y is None:
+        y = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+    prm = make_params(q, k, v, log_decay, beta, state, y, z=z, gn=gn, head_major=head_major,
+                      qk_eps=qk_eps, norm_eps=norm_eps)
+    lib = library()
+    st = lib.gdn_decode_step(ctypes.byref(prm), _stream_handle(stream, v.device))
+    _raise(lib, st, prm, 1)
+    return y
+
+
+def gdn_scan(q, k, v, log_decay, beta, state=None, y=None, *, s0=None, z=None, gn=None,
+             head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None):
+    """The recurrence over the time axis from ``s0`` (None = zeros).
+
+    Returns ``(y, state)``; ``state`` may be ``s0`` itself (in-place resume).
+    """
+    _require_cuda(q, k, v, log_decay, beta, state, y, z, gn, s0)
+    if head_major:
+        B, Hk, S, Dk = q.shape
+        Hv, Dv = v.shape[1], v.shape[3]
+    else:
+        B, S, Hk, Dk = q.shape
+        Hv, Dv = v.shape[2], v.shape[3]
+    if y is None:
+        y = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+    if state is None:
+        state = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=v.device)
+    prm = make_params(q, k, v, log_decay, beta, state, y, z=z, gn=gn, s0=s0,
+                      head_major=head_major, qk_eps=qk_eps, norm_eps=norm_eps)
+    lib = library()
+    st = lib.gdn_scan(ctypes.byref(prm), _stream_handle(stream, v.device))
+    _raise(lib, st, prm, 0)
+    return y, state
+
+
+def gdn_reject_reason(params: GdnParams, is_decode: bool) -> str | None:
+    r = library().gdn_reject_reason(ctypes.byref(params), int(bool(is_decode)))
+    return None if r is None else r.decode()
+
+
+def gdn_status_string(status: int) -> str:
+    return library().gdn_status_string(status).decode()
+
+
+def gdn_last_error() -> str:
+    return library().gdn_last_error().decode()
+
+
+def gdn_version() -> int:
+    return library().gdn_version()

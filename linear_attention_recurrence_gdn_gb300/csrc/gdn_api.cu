@@ -1,0 +1,189 @@
+// gdn_api.cu -- the C ABI of libgdn.so: host-side validation, then the kernel launchers.
+//
+// Validation mirrors the role of torch_to_nnef.op.gated_delta, native_gdn_reject_reason
+// (hard constraints checked before anything runs, a short reason string); unlike the page's
+// exporter there is no fallback: a rejected call returns its status and enqueues nothing.
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+struct Range {
+    uintptr_t lo, hi;   // [lo, hi) in bytes; empty when lo == hi
+};
+
+bool overlaps(Range a, Range b) {
+    return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+Range span(const void *ptr, int64_t elems, int64_t elem_bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+    return Range{lo, ptr ? lo + static_cast<uintptr_t>(elems * elem_bytes) : lo};
+}
+
+int64_t dtype_bytes(int dt) {
+    switch (dt) {
+        case GDN_F32: return 4;
+        case GDN_BF16:
+        case GDN_F16: return 2;
+        default: return 0;
+    }
+}
+
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+bool supported_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// Returns GDN_OK or a status, and sets *why to a static reason.
+int check(const gdn_params *p, int is_decode, const char **why) {
+    *why = nullptr;
+    if (p == nullptr) { *why = "params pointer is NULL"; return GDN_ERR_NULL_PTR; }
+    if (p->reserved != 0) { *why = "reserved field must be 0"; return GDN_ERR_BAD_ARG; }
+    if (p->B < 0 || p->S < 0) { *why = "B and S must be >= 0"; return GDN_ERR_BAD_SHAPE; }
+    if (p->Hk < 1 || p->Hv < 1) { *why = "Hk and Hv must be >= 1"; return GDN_ERR_BAD_SHAPE; }
+    if (p->Hv % p->Hk != 0) {
+        *why = "Hv must be a multiple of Hk (value_heads_per_group)";
+        return GDN_ERR_BAD_SHAPE;
+    }
+    if (is_decode && p->S != 1) { *why = "decode step requires S == 1"; return GDN_ERR_BAD_SHAPE; }
+    if (p->head_major != 0 && p->head_major != 1) {
+        *why = "head_major must be 0 or 1";
+        return GDN_ERR_BAD_ARG;
+    }
+    if (p->Dk < 1 || p->Dv < 1) { *why = "Dk and Dv must be >= 1"; return GDN_ERR_BAD_SHAPE; }
+    if (!supported_dim(p->Dk) || !supported_dim(p->Dv)) {
+        *why = "Dk and Dv must be 16, 32, 64 or 128";
+        return GDN_ERR_UNSUPPORTED_DIM;
+    }
+    if (p->Dk != p->Dv) { *why = "Dk != Dv is not supported"; return GDN_ERR_UNSUPPORTED_DIM; }
+    const int64_t eact = dtype_bytes(p->act_dtype);
+    if (eact == 0) { *why = "act_dtype must be GDN_F32, GDN_BF16 or GDN_F16"; return GDN_ERR_BAD_DTYPE; }
+    if (p->gate_dtype != GDN_F32 && p->gate_dtype != p->act_dtype) {
+        *why = "gate_dtype must be GDN_F32 or equal to act_dtype";
+        return GDN_ERR_BAD_DTYPE;
+    }
+    const int64_t egate = dtype_bytes(p->gate_dtype);
+    if (!(p->qk_eps >= 0.f) || !isfinite(p->qk_eps) || !(p->norm_eps >= 0.f) ||
+        !isfinite(p->norm_eps)) {
+        *why = "qk_eps and norm_eps must be finite and >= 0";
+        return GDN_ERR_BAD_ARG;
+    }
+
+    const int64_t B = p->B, S = p->S, Hk = p->Hk, Hv = p->Hv, Dk = p->Dk, Dv = p->Dv;
+    // sizes: every element count must stay below 2^40 and the grid below 2^31 CTAs
+    const int64_t lim = int64_t(1) << 40;
+    if (B * Hv > (int64_t(1) << 30) || B * S > lim / (Hv * Dv) || B * S > lim / (Hk * Dk) ||
+        B * Hv > lim / (Dv * Dk)) {
+        *why = "tensor too large";
+        return GDN_ERR_BAD_ARG;
+    }
+    if (B == 0) return GDN_OK;   // nothing to do, nothing dereferenced
+    if (p->state == nullptr || p->y == nullptr) { *why = "state and y are required"; return GDN_ERR_NULL_PTR; }
+    if ((p->z == nullptr) != (p->gn == nullptr)) {
+        *why = "z and gn must both be given or both be NULL";
+        return GDN_ERR_NULL_PTR;
+    }
+    if (S > 0 && (p->q == nullptr || p->k == nullptr || p->v == nullptr ||
+                  p->log_decay == nullptr || p->beta == nullptr)) {
+        *why = "q, k, v, log_decay and beta are required";
+        return GDN_ERR_NULL_PTR;
+    }
+    // alignment: vector loads of 16 bytes on every activation / state operand
+    const void *vec[] = {p->q, p->k, p->v, p->z, p->gn, p->s0, p->state, p->y};
+    for (const void *ptr : vec)
+        if (ptr && !aligned(ptr, 16)) { *why = "operands must be 16-byte aligned"; return GDN_ERR_MISALIGNED; }
+    if ((p->log_decay && !aligned(p->log_decay, egate)) || (p->beta && !aligned(p->beta, egate))) {
+        *why = "log_decay and beta must be aligned to their element size";
+        return GDN_ERR_MISALIGNED;
+    }
+    // aliasing: y is written while every operand is read
+    const int64_t n_qk = B * S * Hk * Dk, n_v = B * S * Hv * Dv, n_g = B * S * Hv;
+    const int64_t n_state = B * Hv * Dv * Dk;
+    const Range ry = span(p->y, n_v, 4);
+    const Range token_reads[] = {span(p->q, n_qk, eact),         span(p->k, n_qk, eact),
+                                 span(p->v, n_v, eact),          span(p->z, n_v, eact),
+                                 span(p->log_decay, n_g, egate), span(p->beta, n_g, egate),
+                                 span(p->gn, Dv, 4)};
+    const Range rs = span(p->state, n_state, 4);
+    for (const Range &r : token_reads)
+        if (overlaps(ry, r)) { *why = "y overlaps an operand"; return GDN_ERR_ALIASING; }
+    if (overlaps(ry, rs) || (!is_decode && overlaps(ry, span(p->s0, n_state, 4)))) {
+        *why = "y overlaps an operand";
+        return GDN_ERR_ALIASING;
+    }
+    for (const Range &r : token_reads)
+        if (overlaps(rs, r)) { *why = "state overlaps an operand"; return GDN_ERR_ALIASING; }
+    if (!is_decode && p->s0 && p->s0 != p->state && overlaps(rs, span(p->s0, n_state, 4))) {
+        *why = "state partially overlaps s0 (only s0 == state is allowed)";
+        return GDN_ERR_ALIASING;
+    }
+    return GDN_OK;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_decode_step(const gdn_params *p, void *stream) {
+    const char *why;
+    const int st = check(p, 1, &why);
+    if (st != GDN_OK) return st;
+    if (p->B == 0) return GDN_OK;
+    return cuda_status(gdn::launch_decode(*p, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_scan(const gdn_params *p, void *stream) {
+    const char *why;
+    const int st = check(p, 0, &why);
+    if (st != GDN_OK) return st;
+    if (p->B == 0) return GDN_OK;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->S == 0) {
+        const size_t bytes = sizeof(float) * static_cast<size_t>(p->B) * p->Hv * p->Dv * p->Dk;
+        if (p->s0 == p->state) return GDN_OK;
+        if (p->s0) return cuda_status(cudaMemcpyAsync(p->state, p->s0, bytes, cudaMemcpyDeviceToDevice, s));
+        return cuda_status(cudaMemsetAsync(p->state, 0, bytes, s));
+    }
+    return cuda_status(gdn::launch_scan(*p, s));
+}
+
+const char *gdn_reject_reason(const gdn_params *p, int is_decode) {
+    const char *why;
+    return check(p, is_decode, &why) == GDN_OK ? nullptr : why;
+}
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_NULL_PTR: return "a required pointer is NULL (or only one of z, gn given)";
+        case GDN_ERR_BAD_SHAPE: return "bad shape (dims, Hv % Hk, or S != 1 on decode)";
+        case GDN_ERR_UNSUPPORTED_DIM: return "unsupported head dim (Dk = Dv in {16, 32, 64, 128})";
+        case GDN_ERR_BAD_DTYPE: return "bad dtype";
+        case GDN_ERR_MISALIGNED: return "misaligned pointer";
+        case GDN_ERR_ALIASING: return "output overlaps an operand";
+        case GDN_ERR_BAD_ARG: return "bad argument (eps, flag, reserved field or size)";
+        case GDN_ERR_CUDA: return "CUDA error (see gdn_last_error)";
+        default: return "unknown status";
+    }
+}
+
+const char *gdn_last_error(void) { return g_last_error; }
+
+int gdn_version(void) { return GDN_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,16 @@
+// gdn_internal.h -- launchers behind the C ABI (arguments already validated by gdn_api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// One decode step: one CTA per (b, hv) head, gated norm fused in the CTA tail.
+cudaError_t launch_decode(const gdn_params &p, cudaStream_t stream);
+
+// Multi-token scan (S >= 1): state resident on chip across the time axis.
+cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,483 @@
+#!/usr/bin/env python
+"""Benchmark of the GDN recurrence on GB300: decode-step state HBM GB/s and gdn_scan tokens/s.
+
+One bench step is one ``gdn_decode_step`` (one token for every sequence of the batch) on the
+Qwen-style decode workload B=64, Hk=16, Hv=32, Dk=Dv=128, bf16 activations, f32 state
+(134 MB, updated in place).  The JSON line's value is the algorithmic HBM traffic of a step
+(one read and one write of the state plus the step's inputs and output) over the device
+time of the step.  Supplementary: the prefill and long-context scans (tokens/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (there is no other implementation of this
+method to run) on a bounded sample of the same workload.  Under torchrun each rank runs its
+own copy of the per-GPU workload (independent batches, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import ctypes
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from linear_attention_recurrence_gdn_gb300.workloads import (  # noqa: E402
+    DECODE_B64, LONG_B2, PREFILL_B4, Workload, make_inputs)
+
+METRIC = "GDN decode step: state HBM GB/s (% of peak); gdn_scan tokens/sec"
+FALLBACK_HBM_GBS = 6800.0
+FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM
+MAX_SM_MHZ_FALLBACK = 2070.0
+
+
+# ------------------------------------------------------------------------ roofline model
+
+def decode_bytes(w: Workload) -> int:
+    """Algorithmic HBM bytes of one decode step: read + write of the f32 state, q and k per
+    key head, v and z per value head, the f32 output, two f32 gates and the f32 norm weight."""
+    e = w.elem_bytes
+    return (8 * w.B * w.Hv * w.Dv * w.Dk + 2 * w.B * w.Hk * w.Dk * e
+            + w.B * w.Hv * (2 * w.Dv * e + 4 * w.Dv + 8) + 4 * w.Dv)
+
+
+def scan_flops(w: Workload) -> int:
+    """6 Dk Dv FLOP per (token, value head): S.k, S.q and the rank-1 update."""
+    return 6 * w.Dk * w.Dv * w.B * w.S * w.Hv
+
+
+def scan_bytes(w: Workload) -> int:
+    e = w.elem_bytes
+    s0 = 4 * w.B * w.Hv * w.Dv * w.Dk if w.s0_std is not None else 0
+    return (2 * w.B * w.S * w.Hk * w.Dk * e + w.B * w.S * w.Hv * (2 * w.Dv * e + 4 * w.Dv + 8)
+            + s0 + 4 * w.B * w.Hv * w.Dv * w.Dk + 4 * w.Dv)
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured",
+                "sm_max_mhz": float(d.get("sm_max_mhz", MAX_SM_MHZ_FALLBACK))}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback",
+                "sm_max_mhz": MAX_SM_MHZ_FALLBACK}
+
+
+def profiled_traffic(kernel_file: str, summary: str):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel source is unchanged.
+
+    ``summary`` (under profiles/) holds lines ``source_sha256: <hex>`` and
+    ``dram_bytes_per_launch: <int>``; a hash mismatch means the counters are stale -> None.
+    """
+    try:
+        text = open(os.path.join(ROOT, "profiles", summary)).read()
+        src = open(os.path.join(ROOT, "linear_attention_recurrence_gdn_gb300", "csrc",
+                                kernel_file), "rb").read()
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines() if ":" in line)
+    if fields.get("source_sha256", "").strip() != hashlib.sha256(src).hexdigest():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def allreduce_max(x: float, world: int, device=None) -> float:
+    """Max of a scalar over ranks (the slowest rank sets the job time)."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, kept with host timestamps."""
+
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None, period_ms: int = 50):
+        self.uuid = uuid
+        self.file = tempfile.NamedTemporaryFile(prefix="gdn_clocks_", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms)], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.close()
+
+    def samples(self):
+        out = []
+        try:
+            rows = list(csv.reader(open(self.file.name)))
+        except OSError:
+            return out
+        for r in rows:
+            if len(r) < 10:
+                continue
+            r = [c.strip() for c in r]
+            if self.uuid and self.uuid not in r[1]:
+                continue
+            try:
+                ts = _dt.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                out.append({"t": ts, "sm": float(r[2]), "max": float(r[3]),
+                            "reasons": {"hw_slowdown": r[6], "hw_thermal_slowdown": r[7],
+                                        "sw_thermal_slowdown": r[8], "sw_power_cap": r[9]}})
+            except ValueError:
+                continue
+        return out
+
+    def summary(self, t0: float, t1: float) -> dict:
+        s = self.samples()
+        inside = [x for x in s if t0 <= x["t"] <= t1]
+        window = "timed region"
+        if not inside:   # region shorter than the sampling period: nearest samples
+            inside = sorted(s, key=lambda x: min(abs(x["t"] - t0), abs(x["t"] - t1)))[:3]
+            window = "nearest samples to a timed region shorter than the sampling period"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        reasons = sorted({k for x in inside for k, v in x["reasons"].items()
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(x["sm"] for x in inside),
+                "sm_max_mhz": max(x["max"] for x in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+def device_uuid(dev) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------- decode
+
+def decode_params(gdn, w: Workload, dev, sets: int):
+    """Device buffers and C-ABI parameter blocks for `sets` independent decode problems."""
+    bufs, params = [], []
+    base = make_inputs(w)
+    for i in range(sets):
+        inp = base if i == 0 else make_inputs(w, seed=w.seed + 7919 * i)
+        d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        state = d["s0"].clone()
+        y = torch.empty(d["v"].shape, dtype=torch.float32, device=dev)
+        prm = gdn.make_params(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], state, y,
+                              z=d["z"], gn=d["gn"], head_major=w.head_major)
+        bufs.append((d, state, y))
+        params.append(prm)
+    return bufs, params
+
+
+def run_decode_steps(lib, params, stream_handle, n: int, start: int = 0):
+    for i in range(start, start + n):
+        st = lib.gdn_decode_step(ctypes.byref(params[i % len(params)]), stream_handle)
+        if st != 0:
+            raise RuntimeError(f"gdn_decode_step failed with status {st}")
+
+
+def bench_decode(gdn, w: Workload, dev, steps: int, warmup: int, world: int, sampler):
+    lib = gdn.library()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    state_bytes = 4 * w.B * w.Hv * w.Dv * w.Dk
+    sets = max(2, -(-4 * l2 // state_bytes))          # >= 4x L2 of distinct state
+    bufs, params = decode_params(gdn, w, dev, sets)
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+    run_decode_steps(lib, params, handle, warmup)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev0.record(stream)
+    run_decode_steps(lib, params, handle, steps, start=warmup)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier(world)
+    ms = allreduce_max(ev0.elapsed_time(ev1), world, dev)
+    clocks = sampler.summary(t0, t1) if sampler else None
+    return {"ms_total": ms, "ms_per_step": ms / steps, "sets": sets, "clocks": clocks,
+            "bufs": bufs, "params": params}
+
+
+def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
+    """Same metric end to end: every step copies its inputs from pinned host memory, runs the
+    C-ABI decode step on the resident state, and reads y back to the host."""
+    lib = gdn.library()
+    inp = make_inputs(w)
+    names = ["q", "k", "v", "z", "log_decay", "beta"]
+    host = {k: inp[k].pin_memory() for k in names}
+    d = {k: torch.empty_like(host[k], device=dev) for k in names}
+    gn = inp["gn"].to(dev)
+    state = inp["s0"].to(dev)
+    y = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
+    y_host = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+    prm = gdn.make_params(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], state, y,
+                          z=d["z"], gn=gn, head_major=w.head_major)
+    stream = torch.cuda.current_stream(dev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = y_host.numel() * 4
+
+    def step():
+        for k in names:
+            d[k].copy_(host[k], non_blocking=True)
+        st = lib.gdn_decode_step(ctypes.byref(prm), stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"gdn_decode_step failed with status {st}")
+        y_host.copy_(y, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(5):
+        step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    sec = allreduce_max(time.perf_counter() - t0, world, dev)
+    return {"value": aggregate_rate(decode_bytes(w), world, sec / steps) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": 1e3 * sec / steps,
+            "note": "state resident in HBM; per-step inputs from pinned host, y read back"}
+
+
+# ------------------------------------------------------------------------------ scan
+
+def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float):
+    inp = make_inputs(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    y = torch.empty(d["v"].shape, dtype=torch.float32, device=dev)
+    st = torch.empty((w.B, w.Hv, w.Dv, w.Dk), dtype=torch.float32, device=dev)
+
+    def run():
+        gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, y, s0=d["s0"],
+                     z=d["z"], gn=d["gn"], head_major=w.head_major)
+
+    run()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    achieved = scan_flops(w) / (ms * 1e-3) / 1e12
+    return {"config": w.as_config(), "value": w.B * w.S / (ms * 1e-3), "unit": "tokens/s",
+            "ms": ms, "reps": reps,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_note": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x "
+                                      f"{sm_mhz:.0f} MHz (max SM clock)"},
+            "hbm_bytes": scan_bytes(w)}
+
+
+# ------------------------------------------------------------------- oracle baselines
+
+def oracle_decode_sample(w: Workload, batch: int, threads: int, min_seconds: float,
+                         max_calls: int | None = None):
+    """Time the fp64 oracle on decode steps of the first `batch` sequences of `w`."""
+    import oracle   # the CPU-baseline leg is the one place bench.py runs the oracle
+    ws = w.replace(B=batch)
+    inp = make_inputs(ws)
+    oracle.run(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"], z=inp["z"],
+               gn=inp["gn"], s0=inp["s0"], threads=threads)          # warm-up / load
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"], z=inp["z"],
+                   gn=inp["gn"], s0=inp["s0"], threads=threads)
+        calls += 1
+        el = time.perf_counter() - t0
+        if (max_calls and calls >= max_calls) or (not max_calls and el >= min_seconds):
+            break
+    sec = el / calls
+    return {"value": decode_bytes(ws) / sec / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds_per_call": sec,
+            "sample": f"{calls} oracle decode step(s) of {batch} of {w.B} sequences "
+                      f"(all {w.Hv} value heads) of {w.name}, fp64, {threads} threads"}
+
+
+def reference_arm(args, w: Workload):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    threads = os.cpu_count() or 1
+    # size the per-step sample so that warmup + steps finish in about a minute
+    probe = oracle_decode_sample(w, 1, threads, 0.0, max_calls=1)
+    per_seq = probe["seconds_per_call"]
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    batch = max(1, min(w.B, int(budget / max(per_seq, 1e-6))))
+    ws = w.replace(B=batch)
+    inp = make_inputs(ws)
+
+    def step():
+        oracle.run(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"], z=inp["z"],
+                   gn=inp["gn"], s0=inp["s0"], threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = (time.perf_counter() - t0) / args.steps
+    value = decode_bytes(ws) / sec / 1e9
+    sample = (f"each step: one fp64 oracle decode step of {batch} of {w.B} sequences (all "
+              f"{w.Hv} value heads) of {w.name} on {threads} host threads")
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": dict(w.as_config(), sample_batch=batch),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--scan-reps", type=int, default=5)
+    ap.add_argument("--no-scan", action="store_true", help="skip the supplementary scans")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = DECODE_B64
+
+    if args.impl == "reference":
+        return reference_arm(args, w)
+
+    import linear_attention_recurrence_gdn_gb300 as gdn
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    gdn.library()
+    props = torch.cuda.get_device_properties(dev)
+    peaks = load_peaks()
+
+    sampler = ClockSampler(device_uuid(dev)) if rank == 0 else None
+    time.sleep(0.5 if sampler else 0.0)
+    dec = bench_decode(gdn, w, dev, args.steps, args.warmup, world, sampler)
+    del dec["bufs"], dec["params"]
+    torch.cuda.empty_cache()
+    ms_step = dec["ms_per_step"]
+    value = aggregate_rate(decode_bytes(w), world, ms_step * 1e-3) / 1e9
+    per_launch = decode_bytes(w) / (ms_step * 1e-3) / 1e9
+
+    e2e = e2e_decode(gdn, w, dev, args.e2e_steps, world)
+    scan = None
+    if not args.no_scan:
+        sm_mhz = peaks["sm_max_mhz"]
+        scan = {"metric": "gdn_scan tokens/sec", "note": "supplementary, not the headline",
+                "workloads": [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
+                                         sm_mhz) for x in (PREFILL_B4, LONG_B2)]}
+    if sampler:
+        sampler.stop()
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = oracle_decode_sample(w, w.B, os.cpu_count() or 1, args.cpu_seconds)
+        cpu.pop("seconds_per_call", None)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": dict(w.as_config(), l2=f"rotating {dec['sets']} independent state/input sets "
+                       f"({dec['sets']} x {4 * w.B * w.Hv * w.Dv * w.Dk / 1e6:.0f} MB state > "
+                       f"4 x L2 {props.L2_cache_size / 1e6:.0f} MB)",
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                       bytes_per_step=decode_bytes(w)),
+        "roofline": {"bound": "hbm", "achieved": per_launch, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": per_launch / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic("gdn_decode.cu", "decode_b64_dram_traffic.txt"),
+                     "peak_source": peaks["source"], "kernel": "gdn_decode_kernel",
+                     "frac_of_nominal_8tbs": per_launch / 8000.0},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": dec["clocks"],
+        "scan": scan,
+        "device": props.name,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

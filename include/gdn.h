@@ -94,7 +94,8 @@ typedef struct gdn_params {
                                  decode: ignored (the memory is `state`, updated in place)    */
     float *state;             /* decode: memory, read and written in place.
                                  scan: final memory out; may be the same pointer as s0        */
-    float *y;                 /* output, like v but f32; must not overlap any operand         */
+    float *y;                 /* output, like v but f32; must not overlap any operand;
+                                 may be NULL only when S == 0 (nothing is written)            */
     float qk_eps;             /* l2-norm eps of q and k (1e-6 in the reference workloads)     */
     float norm_eps;           /* rmsnorm eps (1e-6 in the reference workloads)                */
 } gdn_params;

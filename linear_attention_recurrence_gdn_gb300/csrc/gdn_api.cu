@@ -87,7 +87,11 @@ int check(const gdn_params *p, int is_decode, const char **why) {
         return GDN_ERR_BAD_ARG;
     }
     if (B == 0) return GDN_OK;   // nothing to do, nothing dereferenced
-    if (p->state == nullptr || p->y == nullptr) { *why = "state and y are required"; return GDN_ERR_NULL_PTR; }
+    // y is untouched (and may be NULL) when S == 0
+    if (p->state == nullptr || (p->y == nullptr && S > 0)) {
+        *why = "state and y are required";
+        return GDN_ERR_NULL_PTR;
+    }
     if ((p->z == nullptr) != (p->gn == nullptr)) {
         *why = "z and gn must both be given or both be NULL";
         return GDN_ERR_NULL_PTR;

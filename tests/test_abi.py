@@ -105,6 +105,7 @@ def test_valid_params_have_no_reject_reason(lib):
     st = BASE + 8 * GAP
     assert reject(lib, fake_params(s0=st, state=st), 0) is None         # in-place resume
     assert reject(lib, fake_params(gate_dtype=gdn.GDN_BF16), 0) is None
+    assert reject(lib, fake_params(S=0, y=None, q=None, k=None), 0) is None  # empty sequence
     for d in (16, 32, 128):
         assert reject(lib, fake_params(Dk=d, Dv=d), 0) is None
 

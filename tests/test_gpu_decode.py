@@ -1,0 +1,153 @@
+"""GPU parity of gdn_decode_step against the fp64 oracle (through the C ABI).
+
+Tolerance: max |gpu - oracle| / (1 + |oracle|) <= 1e-4 on y and on the updated state, for
+the f32-accumulated decode step.  Every case compares both outputs: a kernel that ignored
+the memory would otherwise pass (logicaffeine codegen_cuda::gdn, emit_gated_delta_forward
+prints O and the mutated S for that reason).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_recurrence_gdn_gb300 as gdn
+from linear_attention_recurrence_gdn_gb300 import build as gbuild
+from linear_attention_recurrence_gdn_gb300.workloads import (DECODE_B64, DECODE_B256_HM, TINY,
+                                                             make_inputs)
+from gdn_testutil import (DECODE_TOL, guard_intact, guarded, oracle_ref, rel_err,
+                          small_workload, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gbuild.build_library()
+    gdn.library()
+
+
+def run_decode(inp, *, gated=True, head_major=False, state=None):
+    d = to_dev(inp)
+    st = d["s0"].clone() if state is None else state
+    y = gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st,
+                            z=d["z"] if gated else None, gn=d["gn"] if gated else None,
+                            head_major=head_major)
+    torch.cuda.synchronize()
+    return y, st
+
+
+@pytest.mark.parametrize("w", [DECODE_B64, DECODE_B256_HM], ids=lambda w: w.name)
+def test_full_size_decode_matches_oracle(w):
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    state, whole = guarded(tuple(d["s0"].shape))
+    state.copy_(d["s0"])
+    y, ywhole = guarded(tuple(d["v"].shape))
+    gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], state, y,
+                        z=d["z"], gn=d["gn"], head_major=w.head_major)
+    torch.cuda.synchronize()
+    yr, sr = oracle_ref(inp, head_major=w.head_major)
+    assert rel_err(y, yr) <= DECODE_TOL
+    assert rel_err(state, sr) <= DECODE_TOL
+    assert guard_intact(whole, state.numel()) and guard_intact(ywhole, y.numel())
+
+
+def test_full_size_decode_raw_output_shows_query_scale():
+    # rmsnorm hides a missing 1/sqrt(Dk) or alpha on o; the raw output does not
+    inp = make_inputs(DECODE_B64)
+    y, st = run_decode(inp, gated=False)
+    yr, sr = oracle_ref(inp, gated=False)
+    assert rel_err(y, yr) <= DECODE_TOL
+    assert rel_err(st, sr) <= DECODE_TOL
+
+
+def test_tiny_workload_as_eight_decode_steps():
+    inp = make_inputs(TINY)
+    d = to_dev(inp)
+    state = d["s0"].clone()
+    ys = []
+    for t in range(TINY.S):
+        sl = {k: d[k][:, t:t + 1].contiguous() for k in ("q", "k", "v", "z", "log_decay", "beta")}
+        ys.append(gdn.gdn_decode_step(sl["q"], sl["k"], sl["v"], sl["log_decay"], sl["beta"],
+                                      state, z=sl["z"], gn=d["gn"]))
+    torch.cuda.synchronize()
+    yr, sr = oracle_ref(inp)
+    assert rel_err(torch.cat(ys, 1), yr) <= DECODE_TOL
+    assert rel_err(state, sr) <= DECODE_TOL
+
+
+SHAPES = [(D, Hk, Hv) for D in (16, 32, 64, 128) for (Hk, Hv) in ((2, 2), (2, 4), (1, 4))]
+
+
+@pytest.mark.parametrize("act", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"D{s[0]}_Hk{s[1]}_Hv{s[2]}")
+@pytest.mark.parametrize("gated", [True, False])
+def test_decode_shapes_and_dtypes(act, shape, gated):
+    D, Hk, Hv = shape
+    w = small_workload(B=3, S=1, Hk=Hk, Hv=Hv, D=D, act=act, seed=100 + D + Hv, s0_std=0.3)
+    inp = make_inputs(w)
+    y, st = run_decode(inp, gated=gated)
+    yr, sr = oracle_ref(inp, gated=gated)
+    assert rel_err(y, yr) <= DECODE_TOL
+    assert rel_err(st, sr) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_decode_gates_in_activation_dtype(act):
+    w = small_workload(B=4, S=1, Hk=2, Hv=4, D=128, act=act, seed=7)
+    inp = make_inputs(w, gate_dtype=w.act_dtype)
+    y, st = run_decode(inp)
+    yr, sr = oracle_ref(inp)
+    assert rel_err(y, yr) <= DECODE_TOL and rel_err(st, sr) <= DECODE_TOL
+
+
+def test_decode_head_major_flag_is_a_shape_change_at_one_token():
+    w = small_workload(B=5, S=1, Hk=2, Hv=4, D=64, act="bf16", seed=8)
+    inp = make_inputs(w)
+    y0, s0 = run_decode(inp, head_major=False)
+    hm = dict(inp)
+    for name in ("q", "k", "v", "z"):
+        hm[name] = inp[name].transpose(1, 2).contiguous()
+    for name in ("log_decay", "beta"):
+        hm[name] = inp[name].transpose(1, 2).contiguous()
+    y1, s1 = run_decode(hm, head_major=True)
+    assert torch.equal(y1.transpose(1, 2), y0) and torch.equal(s1, s0)
+
+
+def test_decode_fixed_point_alpha_one_beta_zero_is_exact():
+    w = small_workload(B=2, S=1, Hk=1, Hv=2, D=128, seed=9)
+    inp = make_inputs(w)
+    inp["log_decay"] = torch.zeros_like(inp["log_decay"])
+    inp["beta"] = torch.zeros_like(inp["beta"])
+    _, st = run_decode(inp)
+    assert torch.equal(st.cpu(), inp["s0"])
+
+
+def test_decode_zero_key_and_query_stay_finite():
+    w = small_workload(B=1, S=1, Hk=1, Hv=2, D=64, seed=10)
+    inp = make_inputs(w)
+    inp["k"] = torch.zeros_like(inp["k"])
+    inp["q"] = torch.zeros_like(inp["q"])
+    y, st = run_decode(inp)
+    yr, sr = oracle_ref(inp)
+    assert rel_err(y, yr) <= DECODE_TOL and rel_err(st, sr) <= DECODE_TOL
+
+
+def test_decode_empty_batch_is_a_noop():
+    w = small_workload(B=0, S=1, Hk=1, Hv=2, D=16)
+    inp = make_inputs(w)
+    y, st = run_decode(inp)
+    assert y.numel() == 0 and st.numel() == 0
+
+
+def test_decode_rejects_on_device_without_touching_buffers():
+    w = small_workload(B=2, S=1, Hk=1, Hv=2, D=32)
+    d = to_dev(make_inputs(w))
+    st = d["s0"].clone()
+    with pytest.raises(gdn.GdnError, match="z and gn"):
+        gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, z=d["z"])
+    torch.cuda.synchronize()
+    assert torch.equal(st, d["s0"])

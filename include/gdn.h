@@ -88,7 +88,8 @@ typedef struct gdn_params {
     const void *v;            /* [B,S,Hv,Dv] / [B,Hv,S,Dv]                                    */
     const void *log_decay;    /* [B,S,Hv] / [B,Hv,S]                                          */
     const void *beta;         /* [B,S,Hv] / [B,Hv,S]                                          */
-    const void *z;            /* like v; NULL together with gn: y = raw o (no gated norm)     */
+    const void *z;            /* like v; NULL together with gn: y = raw o (no gated norm).
+                                 With S == 0 every per-token pointer may be NULL              */
     const float *gn;          /* [Dv] f32 gated-norm weight; NULL together with z             */
     const float *s0;          /* scan: initial memory [B,Hv,Dv,Dk]; NULL = zeros.
                                  decode: ignored (the memory is `state`, updated in place)    */

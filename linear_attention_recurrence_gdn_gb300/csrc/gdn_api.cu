@@ -92,7 +92,7 @@ int check(const gdn_params *p, int is_decode, const char **why) {
         *why = "state and y are required";
         return GDN_ERR_NULL_PTR;
     }
-    if ((p->z == nullptr) != (p->gn == nullptr)) {
+    if (S > 0 && (p->z == nullptr) != (p->gn == nullptr)) {
         *why = "z and gn must both be given or both be NULL";
         return GDN_ERR_NULL_PTR;
     }

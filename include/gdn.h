@@ -73,7 +73,8 @@ typedef enum {
     GDN_ERR_MISALIGNED = -5,      /* a pointer is not aligned (16 B; gates: element size)    */
     GDN_ERR_ALIASING = -6,        /* y overlaps an operand, or state partially overlaps s0   */
     GDN_ERR_BAD_ARG = -7,         /* eps negative or not finite; bad flag; size overflow     */
-    GDN_ERR_CUDA = -8             /* the CUDA runtime reported an error at launch            */
+    GDN_ERR_CUDA = -8,            /* the CUDA runtime reported an error                      */
+    GDN_ERR_TIMEOUT = -9          /* a kernel gave up waiting for its own async copies       */
 } gdn_status;
 
 /* Operands of one call.  Shape fields follow GDNShape (num_key_heads = Hk, num_value_heads
@@ -135,6 +136,16 @@ GDN_API const char *gdn_status_string(int status);
 
 /* gdn_last_error -- text of the last GDN_ERR_CUDA seen by the calling thread ("" if none). */
 GDN_API const char *gdn_last_error(void);
+
+/*
+ * gdn_device_status -- waits for `stream`, then reports whether a kernel of this library,
+ * since the last call on this device, abandoned its work because a wait for its own bulk
+ * copies into shared memory exceeded its time limit (about 2 s; never expected on a healthy
+ * GPU).  Returns GDN_ERR_TIMEOUT then (the outputs of that call are incomplete) and clears
+ * the condition; GDN_OK otherwise; GDN_ERR_CUDA if the runtime reports an error.
+ * Source: none on the pages -- failure detection for the asynchronous-copy waits.
+ */
+GDN_API int gdn_device_status(void *stream);
 
 /* gdn_version -- GDN_VERSION of the loaded library. */
 GDN_API int gdn_version(void);

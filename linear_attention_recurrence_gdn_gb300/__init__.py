@@ -35,10 +35,11 @@ GDN_ERR_MISALIGNED = -5
 GDN_ERR_ALIASING = -6
 GDN_ERR_BAD_ARG = -7
 GDN_ERR_CUDA = -8
+GDN_ERR_TIMEOUT = -9
 
 # Symbols declared in include/gdn.h (checked by the tests against the header).
 EXPORTED = ("gdn_decode_step", "gdn_scan", "gdn_reject_reason", "gdn_status_string",
-            "gdn_last_error", "gdn_version")
+            "gdn_last_error", "gdn_device_status", "gdn_version")
 
 
 class GdnParams(ctypes.Structure):
@@ -86,6 +87,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_device_status.argtypes = [ctypes.c_void_p]
+    lib.gdn_device_status.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = ctypes.c_int
     if path is None:
@@ -224,6 +227,11 @@ def gdn_status_string(status: int) -> str:
 
 def gdn_last_error() -> str:
     return library().gdn_last_error().decode()
+
+
+def gdn_device_status(stream=None, device=None) -> int:
+    """GDN_OK, or GDN_ERR_TIMEOUT if a kernel abandoned work since the last check."""
+    return library().gdn_device_status(_stream_handle(stream, device))
 
 
 def gdn_version() -> int:

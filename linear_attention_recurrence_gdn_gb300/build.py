@@ -48,8 +48,8 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps() + [__file__])
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+def _compile(src: str, extra: list[str], build_dir: str) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src).replace(".cu", ".o"))
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -58,24 +58,28 @@ def _compile(src: str, extra: list[str]) -> str:
 
 
 def build_library(force: bool = False, extra_flags: list[str] | None = None,
-                  verbose: bool = False) -> str:
-    """Compile and link libgdn.so; returns its path.  Skips work when up to date."""
-    if not force and not extra_flags and up_to_date():
+                  verbose: bool = False, output: str | None = None) -> str:
+    """Compile and link libgdn.so (or `output`); returns its path.  Skips work when the
+    default library is up to date.  `extra_flags` go to every nvcc compile (e.g. -D tuning
+    macros); such builds should name their own `output`."""
+    out = output or LIBRARY
+    if not force and not extra_flags and output is None and up_to_date():
         return LIBRARY
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if output is None else out + ".build"
+    os.makedirs(build_dir, exist_ok=True)
     extra = list(extra_flags or [])
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIBRARY + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
+    tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIBRARY)
+    os.replace(tmp, out)
     if verbose:
-        print("built", LIBRARY)
-    return LIBRARY
+        print("built", out)
+    return out
 
 
 if __name__ == "__main__":

@@ -182,11 +182,19 @@ const char *gdn_status_string(int status) {
         case GDN_ERR_ALIASING: return "output overlaps an operand";
         case GDN_ERR_BAD_ARG: return "bad argument (eps, flag, reserved field or size)";
         case GDN_ERR_CUDA: return "CUDA error (see gdn_last_error)";
+        case GDN_ERR_TIMEOUT: return "a kernel timed out waiting for its own copies";
         default: return "unknown status";
     }
 }
 
 const char *gdn_last_error(void) { return g_last_error; }
+
+int gdn_device_status(void *stream) {
+    unsigned flag = 0;
+    const int st = cuda_status(gdn::decode_watchdog(&flag, static_cast<cudaStream_t>(stream)));
+    if (st != GDN_OK) return st;
+    return flag ? GDN_ERR_TIMEOUT : GDN_OK;
+}
 
 int gdn_version(void) { return GDN_VERSION; }
 

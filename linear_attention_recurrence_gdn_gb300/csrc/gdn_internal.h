@@ -10,6 +10,9 @@ namespace gdn {
 // One decode step: one CTA per (b, hv) head, gated norm fused in the CTA tail.
 cudaError_t launch_decode(const gdn_params &p, cudaStream_t stream);
 
+// Reads and clears the decode kernels' watchdog word (synchronises `stream`).
+cudaError_t decode_watchdog(unsigned *flag, cudaStream_t stream);
+
 // Multi-token scan (S >= 1): state resident on chip across the time axis.
 cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
 

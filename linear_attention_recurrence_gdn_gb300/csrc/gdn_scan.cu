@@ -26,6 +26,7 @@
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_tma.cuh"
 
 namespace gdn {
 namespace {
@@ -68,17 +69,6 @@ template <typename TA, int DK, int DV, int NW> struct ScanSmem {
     float al[C::T];
     float be[C::T];
 };
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 template <typename TA, int DK, int DV, int NW>
 __global__ void __launch_bounds__(ScanCfg<TA, DK, DV, NW>::NT)

@@ -62,7 +62,7 @@ def test_struct_layout_matches_header(tmp_path):
 
 def test_version_and_status_strings(lib):
     assert gdn.gdn_version() == 1
-    codes = [0, -1, -2, -3, -4, -5, -6, -7, -8]
+    codes = [0, -1, -2, -3, -4, -5, -6, -7, -8, -9]
     texts = [gdn.gdn_status_string(c) for c in codes]
     assert len(set(texts)) == len(codes)
     assert gdn.gdn_status_string(12345) == "unknown status"

@@ -409,6 +409,10 @@ def main(argv=None):
     ap.add_argument("--no-scan", action="store_true", help="skip the supplementary scans")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["all", "decode", "scan"], default="all",
+                    help="decode: skip the scans; scan: time only the scans (profiling runs)")
+    ap.add_argument("--scan-S", type=int, default=0,
+                    help="override the scan workloads' sequence length (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -428,6 +432,17 @@ def main(argv=None):
     props = torch.cuda.get_device_properties(dev)
     peaks = load_peaks()
 
+    scan_workloads = [PREFILL_B4, LONG_B2]
+    if args.scan_S > 0:
+        scan_workloads = [x.replace(S=args.scan_S, name=f"{x.name}_S{args.scan_S}")
+                          for x in scan_workloads]
+    if args.only == "scan":
+        out = [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
+                          peaks["sm_max_mhz"]) for x in scan_workloads]
+        if rank == 0:
+            print(json.dumps({"scan": out}), flush=True)
+        return 0
+
     sampler = ClockSampler(device_uuid(dev)) if rank == 0 else None
     time.sleep(0.5 if sampler else 0.0)
     dec = bench_decode(gdn, w, dev, args.steps, args.warmup, world, sampler)
@@ -439,11 +454,11 @@ def main(argv=None):
 
     e2e = e2e_decode(gdn, w, dev, args.e2e_steps, world)
     scan = None
-    if not args.no_scan:
+    if not args.no_scan and args.only == "all":
         sm_mhz = peaks["sm_max_mhz"]
         scan = {"metric": "gdn_scan tokens/sec", "note": "supplementary, not the headline",
                 "workloads": [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
-                                         sm_mhz) for x in (PREFILL_B4, LONG_B2)]}
+                                         sm_mhz) for x in scan_workloads]}
     if sampler:
         sampler.stop()
 

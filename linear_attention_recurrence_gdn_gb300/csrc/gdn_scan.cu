@@ -53,6 +53,7 @@ template <typename TA, int DK, int DV, int NW> struct ScanCfg {
     static constexpr int VPIECES = RB * (int)sizeof(TA) / 16;   // 16-byte pieces per v slice
     static_assert(DV % RB == 0, "row blocks must tile Dv");
     static_assert(KPIECES >= 1 && VPIECES >= 1, "16-byte copy granularity");
+    static_assert(2 * R == L, "one reduced value (u or w of a row slot) per lane");
 };
 
 // Shared-memory layout of one CTA (dynamic shared memory, 16-byte aligned members).
@@ -61,14 +62,32 @@ template <typename TA, int DK, int DV, int NW> struct ScanSmem {
     TA rawk[2][C::T][DK];
     TA rawq[2][C::T][DK];
     TA rawv[2][C::T][C::RB];
+    TA rawz[2][C::T][C::RB];   // only filled when the CTA owns a whole head and z is given
     float kh[C::T][DK];
     float qh[C::T][DK];
     float vf[C::T][C::RB];
     float ob[C::T][C::RB];
-    float kq[C::T];
-    float al[C::T];
-    float be[C::T];
+    float sz[C::T][C::RB];     // silu(z) of the chunk (whole-head CTAs with z)
+    float4 tok[C::T];          // per token: alpha, beta, k^.q^, 1 / alpha
 };
+
+// Reduce-scatter over the L lanes of an aligned group: every lane holds L partial values;
+// afterwards lane `part` holds the group-wide sum of value number `part`.  L - 1 shuffles
+// (L/2 + L/4 + ... + 1) instead of L log2(L) for separate all-reductions.
+template <int L>
+__device__ __forceinline__ float reduce_scatter(float (&v)[L], int part) {
+#pragma unroll
+    for (int h = L / 2; h >= 1; h >>= 1) {
+        const bool upper = (part & h) != 0;
+#pragma unroll
+        for (int j = 0; j < h; j++) {
+            const float send = upper ? v[j] : v[j + h];
+            const float keep = upper ? v[j + h] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, h);
+        }
+    }
+    return v[0];
+}
 
 template <typename TA, int DK, int DV, int NW>
 __global__ void __launch_bounds__(ScanCfg<TA, DK, DV, NW>::NT)
@@ -107,6 +126,8 @@ gdn_scan_kernel(const gdn_params p) {
     const TA *kg = static_cast<const TA *>(p.k) + k_base;
     const TA *qg = static_cast<const TA *>(p.q) + k_base;
     const TA *vg = static_cast<const TA *>(p.v) + v_base + r0;
+    const bool fused_norm = C::WHOLE_HEAD && p.z != nullptr;
+    const TA *zg = fused_norm ? static_cast<const TA *>(p.z) + v_base : nullptr;
 
     auto issue_chunk = [&](int t0, int buf) {
         const int nt = min(T, S - t0);
@@ -122,6 +143,9 @@ gdn_scan_kernel(const gdn_params p) {
             const int tt = i / C::VPIECES, pc = i % C::VPIECES;
             cp_async16(reinterpret_cast<char *>(&sm.rawv[buf][tt][0]) + 16 * pc,
                        reinterpret_cast<const char *>(vg + (t0 + tt) * v_ts) + 16 * pc);
+            if (fused_norm)
+                cp_async16(reinterpret_cast<char *>(&sm.rawz[buf][tt][0]) + 16 * pc,
+                           reinterpret_cast<const char *>(zg + (t0 + tt) * v_ts) + 16 * pc);
         }
         cp_async_commit();
     };
@@ -149,6 +173,8 @@ gdn_scan_kernel(const gdn_params p) {
 
     const float inv_sqrt_dk = rsqrtf(static_cast<float>(DK));
     const int nchunks = (S + T - 1) / T;
+    float lam = 1.0f;                                      // S = lam * (registers)
+    float rinv = 1.0f;                                     // running product of 1/alpha
     for (int ch = 0; ch < nchunks; ch++) {
         const int t0 = ch * T;
         const int nt = min(T, S - t0);
@@ -188,15 +214,18 @@ gdn_scan_kernel(const gdn_params p) {
                     sm.qh[tt][j] = qx[i] * rq;
                 }
             }
-            if (lane == 0) sm.kq[tt] = skq * rk * rq;
+            if (lane == 0) sm.tok[tt].z = skq * rk * rq;
         }
         for (int i = tid; i < nt * RB; i += C::NT) {
             const int tt = i / RB, j = i % RB;
             sm.vf[tt][j] = A::one(&sm.rawv[buf][tt][j]);
+            if (fused_norm) sm.sz[tt][j] = silu(A::one(&sm.rawz[buf][tt][j]));
         }
         if (tid < nt) {
-            sm.al[tid] = expf(gl);
-            sm.be[tid] = gb;
+            const float a = expf(gl);
+            sm.tok[tid].x = a;
+            sm.tok[tid].y = gb;
+            sm.tok[tid].w = 1.0f / a;                 // inf for a == 0: that token folds
         }
         // prefetch the next chunk's gates (latency hidden by the token loop)
         if (tid < T && t0 + T + tid < S) {
@@ -207,41 +236,104 @@ gdn_scan_kernel(const gdn_params p) {
         __syncthreads();
 
         // ---- the recurrence over the chunk's tokens (each warp on its own rows)
-        for (int tt = 0; tt < nt; tt++) {
-            float4 k4[NV], q4[NV];
+        //
+        // Deferred decay: the registers hold S' = S / lam, lam the product of the alphas
+        // since the last renormalisation, so the per-token update is one FMA per element:
+        //   u = lam_old (S' k^),  w = lam_old (S' q^),  lam_new = alpha lam_old,
+        //   coef = beta (v - lam_new (S' k^)),  o = lam_new (S' q^) + coef (k^.q^),
+        //   S' += (coef / lam_new) k^,           (S = lam_new S' + coef k^ afterwards)
+        // which is the page's update with alpha S folded into lam.  When lam_new would fall
+        // below 2^-40 (or alpha is 0) the decay is folded into the registers instead:
+        //   S' = lam_new S' + coef k^, lam = 1.
+        // 1 / lam_new is kept as a running product of 1 / alpha (computed per token while the
+        // chunk is staged), so the per-token path has no division.
+        float4 k4[NV], q4[NV];
 #pragma unroll
-            for (int c = 0; c < NV; c++) {
-                k4[c] = *reinterpret_cast<const float4 *>(&sm.kh[tt][4 * (c * L + part)]);
-                q4[c] = *reinterpret_cast<const float4 *>(&sm.qh[tt][4 * (c * L + part)]);
-            }
-            const float alpha = sm.al[tt], beta = sm.be[tt], kq = sm.kq[tt];
+        for (int c = 0; c < NV; c++) {
+            k4[c] = *reinterpret_cast<const float4 *>(&sm.kh[0][4 * (c * L + part)]);
+            q4[c] = *reinterpret_cast<const float4 *>(&sm.qh[0][4 * (c * L + part)]);
+        }
+        for (int tt = 0; tt < nt; tt++) {
+            const float4 tk = sm.tok[tt];                 // alpha, beta, k^.q^
+            // this lane's value of v (lanes part < R own the u of row slot `part`)
+            const float vrow = sm.vf[tt][lrow0 + (part % R) * RPS];
+            // partial dots over this lane's columns, two-wide accumulators
+            float red[2 * R];
 #pragma unroll
             for (int r = 0; r < R; r++) {
-                float pu = 0.f, pw = 0.f;
+                float2 au = make_float2(0.f, 0.f), aw = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < NV; c++) {
-                    pu = dot4(s[r][c], k4[c], pu);
-                    pw = dot4(s[r][c], q4[c], pw);
+                    au = __ffma2_rn(make_float2(s[r][c].x, s[r][c].y), make_float2(k4[c].x, k4[c].y), au);
+                    au = __ffma2_rn(make_float2(s[r][c].z, s[r][c].w), make_float2(k4[c].z, k4[c].w), au);
+                    aw = __ffma2_rn(make_float2(s[r][c].x, s[r][c].y), make_float2(q4[c].x, q4[c].y), aw);
+                    aw = __ffma2_rn(make_float2(s[r][c].z, s[r][c].w), make_float2(q4[c].z, q4[c].w), aw);
                 }
-                pu = group_sum<L>(pu);
-                pw = group_sum<L>(pw);
-                const int lr = lrow0 + r * RPS;
-                const float coef = beta * (sm.vf[tt][lr] - alpha * pu);
+                red[r] = au.x + au.y;
+                red[R + r] = aw.x + aw.y;
+            }
+            // prefetch the next token's k^, q^ (independent of the state)
+            float4 kn[NV], qn[NV];
+            const int tn = (tt + 1 < nt) ? tt + 1 : tt;
 #pragma unroll
-                for (int c = 0; c < NV; c++) {
-                    s[r][c].x = fmaf(alpha, s[r][c].x, coef * k4[c].x);
-                    s[r][c].y = fmaf(alpha, s[r][c].y, coef * k4[c].y);
-                    s[r][c].z = fmaf(alpha, s[r][c].z, coef * k4[c].z);
-                    s[r][c].w = fmaf(alpha, s[r][c].w, coef * k4[c].w);
+            for (int c = 0; c < NV; c++) {
+                kn[c] = *reinterpret_cast<const float4 *>(&sm.kh[tn][4 * (c * L + part)]);
+                qn[c] = *reinterpret_cast<const float4 *>(&sm.qh[tn][4 * (c * L + part)]);
+            }
+            // after the reduce-scatter, lane `part` holds value `part`: u' of row slot part
+            // (part < R) or w' of row slot part - R
+            const float mine = reduce_scatter<L>(red, part);
+            const float lam_new = lam * tk.x;
+            const float rinv_new = rinv * tk.w;                           // ~ 1 / lam_new
+            const bool fold = !(lam_new >= 0x1p-40f);
+            const float coef = tk.y * (vrow - lam_new * mine);          // valid in lanes < R
+            const float cp = fold ? coef : coef * rinv_new;               // coef / lam_new
+            float cr[R];
+#pragma unroll
+            for (int r = 0; r < R; r++) cr[r] = __shfl_sync(0xffffffffu, cp, (lane & ~(L - 1)) | r);
+            const float cw = __shfl_sync(0xffffffffu, cp, (lane & ~(L - 1)) | (part & (R - 1)));
+            if (part >= R) {                                              // o of row slot part - R
+                const float coef_w = fold ? cw : cw * lam_new;             // coef of that row
+                sm.ob[tt][lrow0 + (part - R) * RPS] = fmaf(lam_new, mine, coef_w * tk.z);
+            }
+            if (fold) {                                                   // rare, CTA-uniform
+#pragma unroll
+                for (int r = 0; r < R; r++)
+#pragma unroll
+                    for (int c = 0; c < NV; c++) {
+                        s[r][c].x = fmaf(lam_new, s[r][c].x, cr[r] * k4[c].x);
+                        s[r][c].y = fmaf(lam_new, s[r][c].y, cr[r] * k4[c].y);
+                        s[r][c].z = fmaf(lam_new, s[r][c].z, cr[r] * k4[c].z);
+                        s[r][c].w = fmaf(lam_new, s[r][c].w, cr[r] * k4[c].w);
+                    }
+                lam = 1.0f;
+                rinv = 1.0f;
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; r++) {
+                    const float2 c2 = make_float2(cr[r], cr[r]);
+#pragma unroll
+                    for (int c = 0; c < NV; c++) {
+                        const float2 lo = __ffma2_rn(c2, make_float2(k4[c].x, k4[c].y),
+                                                     make_float2(s[r][c].x, s[r][c].y));
+                        const float2 hi = __ffma2_rn(c2, make_float2(k4[c].z, k4[c].w),
+                                                     make_float2(s[r][c].z, s[r][c].w));
+                        s[r][c] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    }
                 }
-                if (part == 0) sm.ob[tt][lr] = fmaf(alpha, pw, coef * kq);
+                lam = lam_new;
+                rinv = rinv_new;
+            }
+#pragma unroll
+            for (int c = 0; c < NV; c++) {
+                k4[c] = kn[c];
+                q4[c] = qn[c];
             }
         }
         __syncthreads();
 
         // ---- outputs of the chunk
-        if (C::WHOLE_HEAD && p.z != nullptr) {
-            const TA *zg = static_cast<const TA *>(p.z) + v_base;
+        if (fused_norm) {
             float *yg = p.y + v_base;
             for (int tt = warp; tt < nt; tt += NW) {
                 constexpr int EPL = (DV + 31) / 32;
@@ -251,7 +343,7 @@ gdn_scan_kernel(const gdn_params p) {
 #pragma unroll
                 for (int i = 0; i < EPL; i++) {
                     const int j = lane + 32 * i;
-                    x[i] = (j < DV) ? sm.ob[tt][j] * silu(A::one(zg + off + j)) : 0.f;
+                    x[i] = (j < DV) ? sm.ob[tt][j] * sm.sz[tt][j] : 0.f;
                     ss = fmaf(x[i], x[i], ss);
                 }
                 ss = group_sum<32>(ss);
@@ -271,13 +363,16 @@ gdn_scan_kernel(const gdn_params p) {
         }
     }
 
-    // final memory rows
+    // final memory rows (undo the deferred decay)
     float *so = p.state + head * (DV * DK) + static_cast<int64_t>(r0) * DK;
 #pragma unroll
     for (int r = 0; r < R; r++)
 #pragma unroll
-        for (int c = 0; c < NV; c++)
-            *reinterpret_cast<float4 *>(so + (lrow0 + r * RPS) * DK + 4 * (c * L + part)) = s[r][c];
+        for (int c = 0; c < NV; c++) {
+            const float4 v = s[r][c];
+            *reinterpret_cast<float4 *>(so + (lrow0 + r * RPS) * DK + 4 * (c * L + part)) =
+                make_float4(lam * v.x, lam * v.y, lam * v.z, lam * v.w);
+        }
 }
 
 // Gated RMSNorm in place on y (raw o -> rmsnorm(o * silu(z)) * gn), one warp per (b, t, hv)

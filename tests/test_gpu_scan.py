@@ -129,8 +129,11 @@ def test_scan_in_place_resume_and_split_equal_single_scan():
                              s0=state, z=sl["z"], gn=d["gn"])
         parts.append(yp)
     torch.cuda.synchronize()
-    assert torch.equal(torch.cat(parts, 1), y)
-    assert torch.equal(state, st)
+    # the same recurrence, but the kernel's deferred decay restarts at each call, so the two
+    # evaluations agree to f32 rounding rather than bit for bit
+    ys = torch.cat(parts, 1)
+    assert float(((ys - y).abs() / (1 + y.abs())).max()) <= DECODE_TOL
+    assert float(((state - st).abs() / (1 + st.abs())).max()) <= DECODE_TOL
 
 
 def test_decode_steps_equal_scan():

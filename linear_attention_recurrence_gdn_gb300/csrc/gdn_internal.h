@@ -16,4 +16,10 @@ cudaError_t decode_watchdog(unsigned *flag, cudaStream_t stream);
 // Multi-token scan (S >= 1): state resident on chip across the time axis.
 cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
 
+// The scan on tensor cores (gdn_scan_tc.cu).
+cudaError_t launch_scan_tc(const gdn_params &p, cudaStream_t stream);
+
+// In-place gated RMSNorm of raw o in y (for scans whose heads are split over CTAs).
+cudaError_t launch_gated_norm(const gdn_params &p, cudaStream_t stream);
+
 }  // namespace gdn

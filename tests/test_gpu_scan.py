@@ -43,7 +43,9 @@ def test_tiny_workload():
     yr, sr = oracle_ref(inp)
     assert y.shape == (1, 8, 2, 16) and st.shape == (1, 2, 16, 16)
     assert rel_err(y, yr) <= SCAN_TOL and rel_err(st, sr) <= SCAN_TOL
-    assert rel_err(y, yr) <= 1e-5          # far inside the bar at this size
+    # far inside the bar: the tensor-core products split every f32 operand into bf16 hi + lo
+    # parts (about 2^-16 relative error per product), so a few 1e-5 at this size
+    assert rel_err(y, yr) <= 1e-4
 
 
 @pytest.mark.parametrize("w", [PREFILL_B4, LONG_B2], ids=lambda w: w.name)

@@ -22,8 +22,13 @@
 //   * accuracy: every operand is split into bf16 hi + lo parts and a product is formed as
 //     hi.hi + hi.lo + lo.hi (relative error about 2^-16 per product, f32 accumulation), so the
 //     result tracks the f32 recurrence far inside the tolerance;
-//   * the per-row scalar recurrence over the block's 16 tokens runs on the CUDA cores from a
-//     per-warp shared-memory transpose of X; the KK, QX tables are one small MMA per block;
+//   * the block's coefficients solve a unit-triangular system that is the same for every row:
+//     with r_t = beta_t (v_t - alpha_t lam D_t x_t) and N[s][t] = beta_t alpha_t KK[s][t]
+//     (s < t), the recurrence d_t + sum_{s<t} N[s][t] d_s = r_t gives d = r (I + N)^-1, and
+//     O = lam alpha D Y + d QX' with QX'[s][t] = alpha_t QX[s][t] (s < t), QX'[t][t] =
+//     k^_t . q^_t.  Per chunk, one small MMA per block forms KK and QX and one warp per block
+//     inverts I + N; every warp then gets d and O of its 16 rows as two more MMAs whose A
+//     operands are accumulator fragments (no per-row serial loop, no transposes);
 //   * chunks of 32 tokens of q, k, v, z are staged global -> shared with cp.async (double
 //     buffer) and normalised once per chunk into the bf16 hi/lo operand arrays;
 //   * when a CTA owns a whole head the gated RMSNorm runs in the CTA; otherwise raw o goes to y
@@ -71,11 +76,11 @@ template <typename TA, int D, int NW> struct TcSmem {
     float sz[kT][C::RB];
     float4 tok[kT];                  // alpha, beta, k^.q^ (f32), log_decay (clamped)
     float4 dec[kT];                  // D_t, W_t, Gam of the block, block-inclusive log sum
-    float kk[C::NBLK][kB][kB];       // [s][t], s < t (0 elsewhere)
-    float qx[C::NBLK][kB][kB];
-    float xg[NW][kB][kB + 4];        // per warp: x of 16 rows x 16 tokens (row-major, padded)
-    float yg[NW][kB][kB + 4];        // per warp: y of 16 rows x 16 tokens
-    float dg[NW][kB][kB + 4];        // per warp: d of 16 rows x 16 tokens
+    float nm[C::NBLK][kB][kB];       // N[s][t] = beta_t alpha_t KK[s][t] for s < t, else 0
+    // B operands [s][t] (k = s, n = t), bf16 hi/lo, rows padded to 24 (conflict-free ldmatrix):
+    __nv_bfloat16 thi[C::NBLK][kB][kB + 8], tlo[C::NBLK][kB][kB + 8];   // T = (I + N)^-1
+    __nv_bfloat16 phi[C::NBLK][kB][kB + 8], plo[C::NBLK][kB][kB + 8];   // QX'
+
 };
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -270,7 +275,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
         }
         __syncthreads();
 
-        // ---- stage 2: decay products per token; KK and QX tables by MMA
+        // ---- stage 2: decay products per token; KK, QX by MMA; N and QX' tables
         if (tid < kT) {
             const int blk0 = (tid / kB) * kB, end = min(blk0 + kB, max(nt, blk0 + 1)) - 1;
             float before = 0.f, upto = 0.f, total = 0.f;
@@ -317,16 +322,36 @@ gdn_scan_tc_kernel(const gdn_params p) {
             for (int nt8 = 0; nt8 < 2; nt8++)
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
-                    const int s = g + ((e & 2) ? 8 : 0);
+                    const int s2 = g + ((e & 2) ? 8 : 0);
                     const int t = 8 * nt8 + 2 * tq + (e & 1);
-                    float val = 0.f;
-                    if (s < t) {                           // weight prod_{s<r<t} alpha_r
-                        const float between = sm.dec[tb + t - 1].w - sm.dec[tb + s].w;
-                        val = expf(between) * acc[nt8][e];
+                    const float4 tk = sm.tok[tb + t];      // alpha, beta, k^.q^
+                    float wgt = 0.f;                       // prod_{s<r<t} alpha_r
+                    if (s2 < t) wgt = expf(sm.dec[tb + t - 1].w - sm.dec[tb + s2].w);
+                    if (isq) {
+                        const float val = (s2 < t) ? tk.x * wgt * acc[nt8][e] : (s2 == t ? tk.z : 0.f);
+                        split1(val, sm.phi[blk][s2][t], sm.plo[blk][s2][t]);
+                    } else {
+                        sm.nm[blk][s2][t] = (s2 < t) ? tk.y * tk.x * wgt * acc[nt8][e] : 0.f;
                     }
-                    if (isq) sm.qx[blk][s][t] = val;
-                    else sm.kk[blk][s][t] = val;
                 }
+        }
+        __syncthreads();
+        // T = (I + N)^-1 (unit upper triangular): lane s of warp blk builds row s by forward
+        // accumulation, T[s][t] = -sum_{s<=r<t} T[s][r] N[r][t].
+        if (warp < C::NBLK && lane < kB) {
+            const int blk = warp, srow = lane;
+            float tr[kB], acc[kB];
+#pragma unroll
+            for (int t = 0; t < kB; t++) { tr[t] = (t == srow) ? 1.f : 0.f; acc[t] = 0.f; }
+#pragma unroll
+            for (int r = 0; r < kB - 1; r++) {
+                if (r > srow) tr[r] = -acc[r];
+#pragma unroll
+                for (int t = r + 1; t < kB; t++) acc[t] = fmaf(tr[r], sm.nm[blk][r][t], acc[t]);
+            }
+            if (kB - 1 > srow) tr[kB - 1] = -acc[kB - 1];
+#pragma unroll
+            for (int t = 0; t < kB; t++) split1(tr[t], sm.thi[blk][srow][t], sm.tlo[blk][srow][t]);
         }
         __syncthreads();
 
@@ -356,68 +381,76 @@ gdn_scan_tc_kernel(const gdn_params p) {
                     mma3(ya[nt8], ah, al, qb[0], qb[1], qb[2], qb[3]);
                 }
             }
-            // X and Y to row-major shared memory: xg[row][token], yg[row][token]
-            float (*xg)[kB + 4] = sm.xg[warp];
-            float (*yg)[kB + 4] = sm.yg[warp];
-            float (*dg)[kB + 4] = sm.dg[warp];
-#pragma unroll
-            for (int nt8 = 0; nt8 < 2; nt8++) {
-                const int t = 8 * nt8 + 2 * tq;
-                *reinterpret_cast<float2 *>(&xg[g][t]) = make_float2(xa[nt8][0], xa[nt8][1]);
-                *reinterpret_cast<float2 *>(&xg[g + 8][t]) = make_float2(xa[nt8][2], xa[nt8][3]);
-                *reinterpret_cast<float2 *>(&yg[g][t]) = make_float2(ya[nt8][0], ya[nt8][1]);
-                *reinterpret_cast<float2 *>(&yg[g + 8][t]) = make_float2(ya[nt8][2], ya[nt8][3]);
-            }
-            __syncwarp();
-            // the block's scalar recurrence for one row (lanes tq 0,1: row g; 2,3: row g + 8;
-            // the pairs compute the same values), by forward accumulation: as soon as d_t is
-            // known its contribution is added to every later token's running sums, so each
-            // step's dependency path is a few FMAs.
-            {
-                const int rr = (tq < 2) ? g : g + 8;
-                const int lrow = wrow + rr;
-                float pu[kB], pq[kB];                      // lam D_t x_t (+ ...), lam D_t y_t (+ ...)
-#pragma unroll
-                for (int t4 = 0; t4 < kB; t4 += 4) {
-                    const float4 x4 = *reinterpret_cast<const float4 *>(&xg[rr][t4]);
-                    const float4 y4 = *reinterpret_cast<const float4 *>(&yg[rr][t4]);
-                    const float xs[4] = {x4.x, x4.y, x4.z, x4.w}, ys[4] = {y4.x, y4.y, y4.z, y4.w};
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const float ld = lam * sm.dec[tb + t4 + i].x;
-                        pu[t4 + i] = ld * xs[i];
-                        pq[t4 + i] = ld * ys[i];
-                    }
-                }
-                const bool writer = (tq & 1) == 0;
-#pragma unroll
-                for (int t = 0; t < kB; t++) {
-                    const float4 tk = sm.tok[tb + t];     // alpha, beta, k^.q^
-                    const float dt = (t < nb) ? tk.y * (sm.vf[tb + t][lrow] - tk.x * pu[t]) : 0.f;
-                    if (writer) {
-                        dg[rr][t] = dt;
-                        if (t < nb) sm.ob[tb + t][lrow] = fmaf(tk.x, pq[t], dt * tk.z);
-                    }
-#pragma unroll
-                    for (int t2 = t + 1; t2 < kB; t2++) {
-                        pu[t2] = fmaf(dt, sm.kk[blk][t][t2], pu[t2]);
-                        pq[t2] = fmaf(dt, sm.qx[blk][t][t2], pq[t2]);
-                    }
-                }
-            }
-            __syncwarp();
-            const float gam = sm.dec[tb].z;
-            const float lam_new = lam * gam;
-            const bool fold = !(lam_new >= 0x1p-40f);      // CTA-uniform
-            const float scale = fold ? 1.0f : 1.0f / lam_new;
-            float cf[2][4];                                // d_t W_t scale at the fragment positions
+            // r = beta (v - alpha lam D x), and lam alpha D Y, at this lane's fragment positions
+            float ra[2][4], oa[2][4];
 #pragma unroll
             for (int nt8 = 0; nt8 < 2; nt8++)
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     const int rr = g + ((e & 2) ? 8 : 0);
                     const int t = 8 * nt8 + 2 * tq + (e & 1);
-                    cf[nt8][e] = dg[rr][t] * sm.dec[tb + t].y * scale;
+                    const float4 tk = sm.tok[tb + t];     // alpha, beta
+                    const float lad = lam * tk.x * sm.dec[tb + t].x;
+                    // exact zeros past the sequence end: those columns meet every other
+                    // token's terms in the d, O and update MMAs
+                    ra[nt8][e] = (t < nb) ? tk.y * (sm.vf[tb + t][wrow + rr] - lad * xa[nt8][e]) : 0.f;
+                    oa[nt8][e] = lad * ya[nt8][e];
+                }
+            // d = r T  (A = r, rows x tokens s; B = T[s][t])
+            float da[2][4] = {};
+            {
+                uint32_t rh[4], rl[4];
+                split2(ra[0][0], ra[0][1], rh[0], rl[0]);
+                split2(ra[0][2], ra[0][3], rh[1], rl[1]);
+                split2(ra[1][0], ra[1][1], rh[2], rl[2]);
+                split2(ra[1][2], ra[1][3], rh[3], rl[3]);
+#pragma unroll
+                for (int nt8 = 0; nt8 < 2; nt8++) {
+                    uint32_t tbf[4];
+                    const int m = lane >> 3, r = lane & 7;
+                    const int srow = r + ((m & 1) ? 8 : 0);
+                    ldsm_x4_t(tbf, (m & 2) ? &sm.tlo[blk][srow][8 * nt8] : &sm.thi[blk][srow][8 * nt8]);
+                    mma3(da[nt8], rh, rl, tbf[0], tbf[1], tbf[2], tbf[3]);
+                }
+            }
+            // O = lam alpha D Y + d QX'
+            uint32_t dh[4], dl[4];
+            split2(da[0][0], da[0][1], dh[0], dl[0]);
+            split2(da[0][2], da[0][3], dh[1], dl[1]);
+            split2(da[1][0], da[1][1], dh[2], dl[2]);
+            split2(da[1][2], da[1][3], dh[3], dl[3]);
+#pragma unroll
+            for (int nt8 = 0; nt8 < 2; nt8++) {
+                uint32_t pbf[4];
+                const int m = lane >> 3, r = lane & 7;
+                const int srow = r + ((m & 1) ? 8 : 0);
+                ldsm_x4_t(pbf, (m & 2) ? &sm.plo[blk][srow][8 * nt8] : &sm.phi[blk][srow][8 * nt8]);
+                mma3(oa[nt8], dh, dl, pbf[0], pbf[1], pbf[2], pbf[3]);
+            }
+#pragma unroll
+            for (int nt8 = 0; nt8 < 2; nt8++) {
+                const int t = 8 * nt8 + 2 * tq;
+                if (t < nb) {
+                    sm.ob[tb + t][wrow + g] = oa[nt8][0];
+                    sm.ob[tb + t][wrow + g + 8] = oa[nt8][2];
+                }
+                if (t + 1 < nb) {
+                    sm.ob[tb + t + 1][wrow + g] = oa[nt8][1];
+                    sm.ob[tb + t + 1][wrow + g + 8] = oa[nt8][3];
+                }
+            }
+            // the rank-16 update: C = d W / lam' (A fragment), S' += C K^
+            const float gam = sm.dec[tb].z;
+            const float lam_new = lam * gam;
+            const bool fold = !(lam_new >= 0x1p-40f);      // CTA-uniform
+            const float scale = fold ? 1.0f : 1.0f / lam_new;
+            float cf[2][4];
+#pragma unroll
+            for (int nt8 = 0; nt8 < 2; nt8++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int t = 8 * nt8 + 2 * tq + (e & 1);
+                    cf[nt8][e] = da[nt8][e] * sm.dec[tb + t].y * scale;
                 }
             // A fragment of the coefficients (rows x tokens, k = token)
             uint32_t ch_[4], cl_[4];
@@ -441,7 +474,6 @@ gdn_scan_tc_kernel(const gdn_params p) {
                 mma3(sacc[j], ch_, cl_, kb[0], kb[1], kb[2], kb[3]);
             }
             lam = fold ? 1.0f : lam_new;
-            __syncwarp();
         }
         __syncthreads();
 

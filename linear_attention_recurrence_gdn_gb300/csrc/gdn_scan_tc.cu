@@ -46,6 +46,7 @@ namespace {
 
 constexpr int kT = 32;                     // tokens per staged chunk
 constexpr int kB = 16;                     // tokens per MMA block
+static_assert(kT == 32 && kT % kB == 0, "one lane per chunk token in the decay prefix scan");
 constexpr float kMinLogDecay = -80.0f;     // exp(-80) ~ 1.8e-35: a full reset for f32 purposes
 
 template <typename TA, int D, int NW> struct TcCfg {
@@ -211,6 +212,13 @@ gdn_scan_tc_kernel(const gdn_params p) {
 
     const float inv_sqrt_dk = rsqrtf(static_cast<float>(D));
     const int nchunks = (S + kT - 1) / kT;
+    constexpr int EPL_OUT = (D + 31) / 32;
+    float gnr[EPL_OUT];                                    // the norm weight, read once
+#pragma unroll
+    for (int i = 0; i < EPL_OUT; i++) {
+        const int j = lane + 32 * i;
+        gnr[i] = (fused_norm && j < D) ? p.gn[j] : 0.f;
+    }
     float lam = 1.0f;                                      // true memory = lam * registers
     for (int ch = 0; ch < nchunks; ch++) {
         const int t0 = ch * kT;
@@ -226,7 +234,9 @@ gdn_scan_tc_kernel(const gdn_params p) {
 
         // ---- stage 1: q^, k^ as bf16 hi/lo operand arrays (rows past the sequence end are
         //      zero so that the block MMAs see exact zeros there); gates; v, silu(z)
-        for (int tt = warp; tt < kT; tt += NW) {
+#pragma unroll
+        for (int it = 0; it < kT / NW; it++) {             // fixed trip count: tokens overlap
+            const int tt = warp + it * NW;
             constexpr int EPL = (D + 31) / 32;
             float kx[EPL], qx[EPL];
             float ssk = 0.f, ssq = 0.f, skq = 0.f;
@@ -238,29 +248,39 @@ gdn_scan_tc_kernel(const gdn_params p) {
                 qx[i] = (valid && j < D) ? A::one(&sm.rawq[buf][tt][j]) : 0.f;
                 ssk = fmaf(kx[i], kx[i], ssk);
                 ssq = fmaf(qx[i], qx[i], ssq);
+                skq = fmaf(kx[i], qx[i], skq);
             }
-            ssk = group_sum<32>(ssk);
-            ssq = group_sum<32>(ssq);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {       // the three sums reduce together
+                ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
+                ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
+                skq += __shfl_xor_sync(0xffffffffu, skq, off);
+            }
             const float rk = rsqrtf(ssk + p.qk_eps);
             const float rq = rsqrtf(ssq + p.qk_eps) * inv_sqrt_dk;
 #pragma unroll
             for (int i = 0; i < EPL; i++) {
                 const int j = lane + 32 * i;
-                kx[i] *= rk;
-                qx[i] *= rq;
-                skq = fmaf(kx[i], qx[i], skq);
                 if (j < D) {
-                    split1(kx[i], sm.khi[tt][j], sm.klo[tt][j]);
-                    split1(qx[i], sm.qhi[tt][j], sm.qlo[tt][j]);
+                    split1(kx[i] * rk, sm.khi[tt][j], sm.klo[tt][j]);
+                    split1(qx[i] * rq, sm.qhi[tt][j], sm.qlo[tt][j]);
                 }
             }
-            skq = group_sum<32>(skq);
-            if (lane == 0) sm.tok[tt].z = skq;
+            if (lane == 0) sm.tok[tt].z = skq * rk * rq;
         }
-        for (int i = tid; i < nt * RB; i += C::NT) {
+        static_assert((kT * RB / 4) % C::NT == 0, "4-element groups tile the chunk's v slice");
+#pragma unroll
+        for (int it = 0; it < kT * RB / 4 / C::NT; it++) {   // 4 consecutive values per thread
+            const int i = 4 * (tid + it * C::NT);
             const int tt = i / RB, j = i % RB;
-            sm.vf[tt][j] = A::one(&sm.rawv[buf][tt][j]);
-            if (fused_norm) sm.sz[tt][j] = silu(A::one(&sm.rawz[buf][tt][j]));
+            if (tt < nt) {
+                *reinterpret_cast<float4 *>(&sm.vf[tt][j]) = A::four(&sm.rawv[buf][tt][j]);
+                if (fused_norm) {
+                    const float4 z4 = A::four(&sm.rawz[buf][tt][j]);
+                    *reinterpret_cast<float4 *>(&sm.sz[tt][j]) =
+                        make_float4(silu(z4.x), silu(z4.y), silu(z4.z), silu(z4.w));
+                }
+            }
         }
         if (tid < kT) {
             const float gc = (tid < nt) ? fmaxf(gl, kMinLogDecay) : 0.f;
@@ -276,64 +296,61 @@ gdn_scan_tc_kernel(const gdn_params p) {
         __syncthreads();
 
         // ---- stage 2: decay products per token; KK, QX by MMA; N and QX' tables
-        if (tid < kT) {
-            const int blk0 = (tid / kB) * kB, end = min(blk0 + kB, max(nt, blk0 + 1)) - 1;
-            float before = 0.f, upto = 0.f, total = 0.f;
-            for (int j = blk0; j <= end; j++) {
-                const float gj = sm.tok[j].w;
-                if (j < tid) before += gj;
-                if (j <= tid) upto += gj;
-                total += gj;
+        if (warp == 0) {                                   // kT == 32: one lane per token
+            // block-relative inclusive prefix sum of log_decay (invalid tokens hold 0)
+            const float gj = sm.tok[lane].w;
+            float upto = gj;
+#pragma unroll
+            for (int off = 1; off < kB; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, upto, off, kB);
+                if ((lane & (kB - 1)) >= off) upto += o;
             }
-            sm.dec[tid] = make_float4(expf(before), expf(total - upto), expf(total), upto);
+            const float total = __shfl_sync(0xffffffffu, upto, kB - 1, kB);
+            sm.dec[lane] = make_float4(expf(upto - gj), expf(total - upto), expf(total), upto);
         }
         __syncthreads();
-        for (int task = warp; task < 2 * C::NBLK; task += NW) {
-            const int blk = task >> 1;
-            const bool isq = task & 1;
+        for (int task = warp; task < 4 * C::NBLK; task += NW) {
+            const int blk = task >> 2;
+            const bool isq = (task >> 1) & 1;
+            const int nt8 = task & 1;                      // which 8 tokens t
             const int tb = blk * kB;
-            float acc[2][4] = {};
+            float acc2[2][4] = {};                          // even / odd k-steps (shorter chains)
 #pragma unroll
             for (int kk = 0; kk < KST; kk++) {
                 // A = K^[s = tb..tb+15][cols 16kk..16kk+15]  (hi and lo)
                 uint32_t ah[4], al[4];
+                const int m = lane >> 3, r = lane & 7;       // matrix, row of ldmatrix
                 {
-                    const int m = lane >> 3, r = lane & 7;       // matrix, row of ldmatrix
                     const int srow = tb + r + ((m & 1) ? 8 : 0);
                     const int col = 16 * kk + ((m & 2) ? 8 : 0);
                     ldsm_x4(ah, &sm.khi[srow][col]);
                     ldsm_x4(al, &sm.klo[srow][col]);
                 }
-#pragma unroll
-                for (int nt8 = 0; nt8 < 2; nt8++) {
-                    // B = (K^ or Q^)^T: rows of the ldmatrix are tokens t, 8 columns each
-                    uint32_t bb[4];
-                    const int m = lane >> 3, r = lane & 7;
-                    const int trow = tb + 8 * nt8 + r;
-                    const int col = 16 * kk + ((m & 1) ? 8 : 0);
-                    const __nv_bfloat16 *src = (m & 2) ? (isq ? &sm.qlo[trow][col] : &sm.klo[trow][col])
-                                                       : (isq ? &sm.qhi[trow][col] : &sm.khi[trow][col]);
-                    ldsm_x4(bb, src);
-                    mma3(acc[nt8], ah, al, bb[0], bb[1], bb[2], bb[3]);
-                }
+                // B = (K^ or Q^)^T: rows of the ldmatrix are tokens t, 8 columns each
+                uint32_t bb[4];
+                const int trow = tb + 8 * nt8 + r;
+                const int col = 16 * kk + ((m & 1) ? 8 : 0);
+                const __nv_bfloat16 *src = (m & 2) ? (isq ? &sm.qlo[trow][col] : &sm.klo[trow][col])
+                                                   : (isq ? &sm.qhi[trow][col] : &sm.khi[trow][col]);
+                ldsm_x4(bb, src);
+                mma3(acc2[kk & 1], ah, al, bb[0], bb[1], bb[2], bb[3]);
             }
             // epilogue: entry (s, t) with s = g or g + 8, t = 8 nt8 + 2 tq (+1)
 #pragma unroll
-            for (int nt8 = 0; nt8 < 2; nt8++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const int s2 = g + ((e & 2) ? 8 : 0);
-                    const int t = 8 * nt8 + 2 * tq + (e & 1);
-                    const float4 tk = sm.tok[tb + t];      // alpha, beta, k^.q^
-                    float wgt = 0.f;                       // prod_{s<r<t} alpha_r
-                    if (s2 < t) wgt = expf(sm.dec[tb + t - 1].w - sm.dec[tb + s2].w);
-                    if (isq) {
-                        const float val = (s2 < t) ? tk.x * wgt * acc[nt8][e] : (s2 == t ? tk.z : 0.f);
-                        split1(val, sm.phi[blk][s2][t], sm.plo[blk][s2][t]);
-                    } else {
-                        sm.nm[blk][s2][t] = (s2 < t) ? tk.y * tk.x * wgt * acc[nt8][e] : 0.f;
-                    }
+            for (int e = 0; e < 4; e++) {
+                const int s2 = g + ((e & 2) ? 8 : 0);
+                const int t = 8 * nt8 + 2 * tq + (e & 1);
+                const float dot = acc2[0][e] + acc2[1][e];
+                const float4 tk = sm.tok[tb + t];          // alpha, beta, k^.q^
+                float wgt = 0.f;                           // prod_{s<r<t} alpha_r
+                if (s2 < t) wgt = expf(sm.dec[tb + t - 1].w - sm.dec[tb + s2].w);
+                if (isq) {
+                    const float val = (s2 < t) ? tk.x * wgt * dot : (s2 == t ? tk.z : 0.f);
+                    split1(val, sm.phi[blk][s2][t], sm.plo[blk][s2][t]);
+                } else {
+                    sm.nm[blk][s2][t] = (s2 < t) ? tk.y * tk.x * wgt * dot : 0.f;
                 }
+            }
         }
         __syncthreads();
         // T = (I + N)^-1 (unit upper triangular): lane s of warp blk builds row s by forward
@@ -480,7 +497,10 @@ gdn_scan_tc_kernel(const gdn_params p) {
         // ---- outputs of the chunk
         if (fused_norm) {
             float *yg = p.y + v_base;
-            for (int tt = warp; tt < nt; tt += NW) {
+#pragma unroll
+            for (int it = 0; it < kT / NW; it++) {
+                const int tt = warp + it * NW;
+                if (tt >= nt) break;                       // warp-uniform
                 constexpr int EPL = (D + 31) / 32;
                 const int64_t off = static_cast<int64_t>(t0 + tt) * v_ts;
                 float x[EPL];
@@ -496,7 +516,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
 #pragma unroll
                 for (int i = 0; i < EPL; i++) {
                     const int j = lane + 32 * i;
-                    if (j < D) yg[off + j] = x[i] * rr * p.gn[j];
+                    if (j < D) yg[off + j] = x[i] * rr * gnr[i];
                 }
             }
         } else {

@@ -278,7 +278,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
                 if (fused_norm) {
                     const float4 z4 = A::four(&sm.rawz[buf][tt][j]);
                     *reinterpret_cast<float4 *>(&sm.sz[tt][j]) =
-                        make_float4(silu(z4.x), silu(z4.y), silu(z4.z), silu(z4.w));
+                        make_float4(silu_fast(z4.x), silu_fast(z4.y), silu_fast(z4.z), silu_fast(z4.w));
                 }
             }
         }

@@ -327,7 +327,11 @@ def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float):
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                          "peak_note": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x "
-                                      f"{sm_mhz:.0f} MHz (max SM clock)"},
+                                      f"{sm_mhz:.0f} MHz (max SM clock)",
+                         "work": "algorithmic 6 Dk Dv FLOP per token-head (the sequential "
+                                 "recurrence), f32-equivalent",
+                         "implementation": "tensor cores, mma.sync m16n8k16 bf16 with hi/lo "
+                                           "operand split (3 MMAs per product)"},
             "hbm_bytes": scan_bytes(w)}
 
 

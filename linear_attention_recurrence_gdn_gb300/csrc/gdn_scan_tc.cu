@@ -2,12 +2,14 @@
 //
 // What is computed is the page's per-token recurrence (logicaffeine_compile::codegen_cuda::gdn,
 // module description; time loop of torch_to_nnef.op.gated_delta, gated_delta_reference), not
-// an approximation of it: blocks of B = 16 tokens are written out exactly.  With S' the
-// registers at the block start (true memory lam S') and x_t = S' k^_t, y_t = S' q^_t:
-//     u_t = lam D_t x_t + sum_{s<t} d_s KK[s][t]             (u: the page's S k)
-//     d_t = beta_t (v_t - alpha_t u_t)                         (d: the page's coef)
-//     o_t = alpha_t (lam D_t y_t + sum_{s<t} d_s QX[s][t]) + d_t (k^_t . q^_t)
-//     S'  <- S' + sum_s (W_s d_s / lam') k^_s,   lam' = lam Gam
+// an approximation of it: blocks of B = 16 tokens are written out exactly.  The l2 norms are
+// per-token scalars, k^_t = rk_t k_t and q^_t = rq_t q_t (rq_t carries 1/sqrt(Dk)), so the
+// products below run on the raw k and q.  With S' the registers at the block start (true
+// memory lam S') and x_t = S' k_t, y_t = S' q_t:
+//     u_t = lam D_t rk_t x_t + sum_{s<t} d_s KK[s][t]          (u: the page's S k)
+//     d_t = beta_t (v_t - alpha_t u_t)                           (d: the page's coef)
+//     o_t = alpha_t (lam D_t rq_t y_t + sum_{s<t} d_s QX[s][t]) + d_t (k^_t . q^_t)
+//     S'  <- S' + sum_s (W_s rk_s d_s / lam') k_s,   lam' = lam Gam
 // D_t = prod_{r<t} alpha_r, W_s = prod_{r>s} alpha_r, Gam = prod over the block,
 // KK[s][t] = prod_{s<r<t} alpha_r (k^_s . k^_t), QX[s][t] = prod_{s<r<t} alpha_r (k^_s . q^_t);
 // every decay product is exp of a non-positive sum of log_decay.  This is the page's update
@@ -18,21 +20,24 @@
 //     accumulator fragments of m16n8k16 tensor-core MMAs (16 x D per warp: D/8 n-tiles);
 //   * X = S' K^T and Y = S' Q^T for the block's 16 tokens are MMAs whose A operand is the
 //     accumulator itself (an m16n8 accumulator pair has the m16k16 A-fragment layout), and the
-//     rank-16 update S' += C K^ is an MMA accumulating into the same registers;
-//   * accuracy: every operand is split into bf16 hi + lo parts and a product is formed as
-//     hi.hi + hi.lo + lo.hi (relative error about 2^-16 per product, f32 accumulation), so the
-//     result tracks the f32 recurrence far inside the tolerance;
+//     rank-16 update S' += C K is an MMA accumulating into the same registers;
+//   * accuracy: f32 operands are split into bf16 hi + lo parts and a product is formed as
+//     hi.hi + hi.lo + lo.hi (relative error about 2^-16 per product, f32 accumulation).  bf16
+//     inputs are exact bf16 operands, so their products take two MMAs (hi.k + lo.k) and the
+//     raw rows are copied straight into the operand arrays; f16 inputs split exactly;
 //   * the block's coefficients solve a unit-triangular system that is the same for every row:
-//     with r_t = beta_t (v_t - alpha_t lam D_t x_t) and N[s][t] = beta_t alpha_t KK[s][t]
+//     with r_t = beta_t (v_t - alpha_t lam D_t rk_t x_t) and N[s][t] = beta_t alpha_t KK[s][t]
 //     (s < t), the recurrence d_t + sum_{s<t} N[s][t] d_s = r_t gives d = r (I + N)^-1, and
-//     O = lam alpha D Y + d QX' with QX'[s][t] = alpha_t QX[s][t] (s < t), QX'[t][t] =
+//     O = lam alpha D rq Y + d QX' with QX'[s][t] = alpha_t QX[s][t] (s < t), QX'[t][t] =
 //     k^_t . q^_t.  Per chunk, one small MMA per block forms KK and QX and one warp per block
 //     inverts I + N; every warp then gets d and O of its 16 rows as two more MMAs whose A
 //     operands are accumulator fragments (no per-row serial loop, no transposes);
-//   * chunks of 32 tokens of q, k, v, z are staged global -> shared with cp.async (double
-//     buffer) and normalised once per chunk into the bf16 hi/lo operand arrays;
-//   * when a CTA owns a whole head the gated RMSNorm runs in the CTA; otherwise raw o goes to y
-//     and gdn_gated_norm_kernel applies the norm afterwards.
+//   * warp specialisation: 4 producer warps stage chunk c+1 (cp.async copies of q, k, v, z two
+//     chunks ahead; the norms; decay products; KK, QX; the triangular inverse) and write y for
+//     finished chunks, while the row warps run chunk c.  Hand-off through rings of shared
+//     memory slots and named barriers (full / empty per chunk parity);
+//   * when a CTA owns a whole head the producers apply the gated RMSNorm; otherwise raw o goes
+//     to y and gdn_gated_norm_kernel applies the norm afterwards.
 #include <math.h>
 
 #include <algorithm>
@@ -49,40 +54,73 @@ constexpr int kB = 16;                     // tokens per MMA block
 static_assert(kT == 32 && kT % kB == 0, "one lane per chunk token in the decay prefix scan");
 constexpr float kMinLogDecay = -80.0f;     // exp(-80) ~ 1.8e-35: a full reset for f32 purposes
 
+template <typename TA> struct IsBf16 { static constexpr bool value = false; };
+template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
+
 template <typename TA, int D, int NW> struct TcCfg {
-    static constexpr int RB = 16 * NW;               // rows per CTA
+    static constexpr bool EXACT = IsBf16<TA>::value;  // raw rows are exact bf16 operands
+    static constexpr int RB = 16 * NW;               // rows per CTA (NW row warps)
     static constexpr int NRB = D / RB;               // CTAs per head
-    static constexpr int NT = 32 * NW;
+    static constexpr int NP = 4;                     // producer warps
+    static constexpr int PT = 32 * NP;               // producer threads
+    static constexpr int NT = 32 * (NW + NP);
     static constexpr int NTILE = D / 8;              // n-tiles of a warp's 16 x D memory block
     static constexpr int KST = D / 16;               // k-steps over D
     static constexpr int NBLK = kT / kB;
-    static constexpr int LDH = D + 8;                // padded bf16 row stride (conflict-free)
+    static constexpr int PADE = 16 / (int)sizeof(TA);  // 16 bytes of row padding, in elements
+    static constexpr int LDV = RB + PADE;            // raw v / z rows
+    static constexpr int LDO = RB + 4;               // o rows (f32)
+    static constexpr int NOP = EXACT ? 3 : 2;        // operand ring depth
+    static constexpr int NVZ = 3;                    // v / z ring depth
     static constexpr bool WHOLE_HEAD = (RB == D);
-    static constexpr int KPIECES = D * (int)sizeof(TA) / 16;
-    static constexpr int VPIECES = RB * (int)sizeof(TA) / 16;
+    static constexpr int KPIECES = D * (int)sizeof(TA) / 16;     // 16-byte pieces of a k row
+    static constexpr int VPIECES = RB * (int)sizeof(TA) / 16;    // ... of this CTA's v rows
+    static constexpr int TPK = KPIECES < 4 ? KPIECES : 4;        // norm-pass threads per token
     static_assert(D % RB == 0 && D % 16 == 0, "shape");
     static_assert(KPIECES >= 1 && VPIECES >= 1, "16-byte copy granularity");
+    static_assert(KPIECES % TPK == 0 && PT / TPK >= kT, "norm pass covers a chunk at once");
 };
 
+// k and q operands, rows padded by 16 bytes (conflict-free ldmatrix and 16-byte accesses).
+// bf16: the raw rows, copied in place into a ring of three slots.  Other types: a staging
+// slot for the raw rows and a ring of two slots of bf16 hi / lo parts.
+template <typename TA, int D, bool EXACT> struct TcOps;
+template <typename TA, int D> struct TcOps<TA, D, true> {
+    __nv_bfloat16 k[3][kT][D + 8], q[3][kT][D + 8];
+};
+template <typename TA, int D> struct TcOps<TA, D, false> {
+    TA kraw[kT][D + 16 / sizeof(TA)], qraw[kT][D + 16 / sizeof(TA)];
+    __nv_bfloat16 khi[2][kT][D + 8], klo[2][kT][D + 8];
+    __nv_bfloat16 qhi[2][kT][D + 8], qlo[2][kT][D + 8];
+};
+
+// Shared memory.  Slots are indexed by chunk: operands c % NOP, v / z c % 3, and everything
+// else the row warps read (o, per-token scalars, tables) c % 2.
 template <typename TA, int D, int NW> struct TcSmem {
     using C = TcCfg<TA, D, NW>;
-    TA rawk[2][kT][D];
-    TA rawq[2][kT][D];
-    TA rawv[2][kT][C::RB];
-    TA rawz[2][kT][C::RB];
-    __nv_bfloat16 khi[kT][C::LDH], klo[kT][C::LDH];
-    __nv_bfloat16 qhi[kT][C::LDH], qlo[kT][C::LDH];
-    float vf[kT][C::RB];
-    float ob[kT][C::RB];
-    float sz[kT][C::RB];
-    float4 tok[kT];                  // alpha, beta, k^.q^ (f32), log_decay (clamped)
-    float4 dec[kT];                  // D_t, W_t, Gam of the block, block-inclusive log sum
+    TcOps<TA, D, C::EXACT> op;
+    TA vr[C::NVZ][kT][C::LDV];       // raw v rows of this CTA
+    TA zr[C::NVZ][kT][C::LDV];       // raw z (whole-head CTAs with z)
+    float ob[2][kT][C::LDO];         // o of the chunk, written by the row warps
+    float4 cst[2][kT];               // row-warp scalars: beta, alpha D rk, alpha D rq, W rk
+    float4 tks[kT];                  // producer scalars: alpha, beta, rk, rq
+    float2 nrm[kT];                  // rk, rq from the norm pass
+    float cum[kT];                   // block-inclusive sums of the clamped log_decay
+    float gam[2][C::NBLK];           // Gam of each block
     float nm[C::NBLK][kB][kB];       // N[s][t] = beta_t alpha_t KK[s][t] for s < t, else 0
     // B operands [s][t] (k = s, n = t), bf16 hi/lo, rows padded to 24 (conflict-free ldmatrix):
-    __nv_bfloat16 thi[C::NBLK][kB][kB + 8], tlo[C::NBLK][kB][kB + 8];   // T = (I + N)^-1
-    __nv_bfloat16 phi[C::NBLK][kB][kB + 8], plo[C::NBLK][kB][kB + 8];   // QX'
-
+    __nv_bfloat16 thi[2][C::NBLK][kB][kB + 8], tlo[2][C::NBLK][kB][kB + 8];   // (I + N)^-1
+    __nv_bfloat16 phi[2][C::NBLK][kB][kB + 8], plo[2][C::NBLK][kB][kB + 8];   // QX'
 };
+
+// Named barriers (0 is __syncthreads): chunk parity b full / empty, and producers only.
+enum { kBarFull0 = 1, kBarEmpty0 = 3, kBarProd = 5 };
+__device__ __forceinline__ void bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -91,6 +129,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (hi + lo) . b for an exact bf16 B operand
+__device__ __forceinline__ void mma2(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                     uint32_t b0, uint32_t b1) {
+    mma16816(d, al, b0, b1);
+    mma16816(d, ah, b0, b1);
 }
 
 // hi.hi + hi.lo + lo.hi
@@ -127,13 +172,70 @@ __device__ __forceinline__ void split1(float x, __nv_bfloat16 &hi, __nv_bfloat16
     lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// Eight bf16 (a 16-byte piece) to f32; bf16 -> f32 is a 16-bit shift.
+__device__ __forceinline__ void unpack8(const uint4 w, float (&x)[8]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        x[2 * i] = __uint_as_float(u[i] << 16);
+        x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
+// Squares of a 16-byte piece of raw k or q into ss; for non-bf16 types also its bf16 hi / lo
+// parts, written to hi / lo (8 or 4 elements).
+template <typename TA> struct Piece;
+template <> struct Piece<__nv_bfloat16> {
+    __device__ __forceinline__ static void sq(const __nv_bfloat16 *src, float &ss) {
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4 *>(src), x);
+#pragma unroll
+        for (int i = 0; i < 8; i++) ss = fmaf(x[i], x[i], ss);
+    }
+};
+template <> struct Piece<__half> {
+    static constexpr int E = 8;
+    __device__ __forceinline__ static void split(const __half *src, __nv_bfloat16 *hi,
+                                                 __nv_bfloat16 *lo, float &ss) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(src);
+        const __half2 *h = reinterpret_cast<const __half2 *>(&w);
+        uint32_t ph[4], pl[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float2 f = __half22float2(h[i]);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+            split2(f.x, f.y, ph[i], pl[i]);
+        }
+        *reinterpret_cast<uint4 *>(hi) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        *reinterpret_cast<uint4 *>(lo) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+    }
+};
+template <> struct Piece<float> {
+    static constexpr int E = 4;
+    __device__ __forceinline__ static void split(const float *src, __nv_bfloat16 *hi,
+                                                 __nv_bfloat16 *lo, float &ss) {
+        const float4 f = *reinterpret_cast<const float4 *>(src);
+        ss = fmaf(f.x, f.x, ss);
+        ss = fmaf(f.y, f.y, ss);
+        ss = fmaf(f.z, f.z, ss);
+        ss = fmaf(f.w, f.w, ss);
+        uint32_t ph[2], pl[2];
+        split2(f.x, f.y, ph[0], pl[0]);
+        split2(f.z, f.w, ph[1], pl[1]);
+        *reinterpret_cast<uint2 *>(hi) = make_uint2(ph[0], ph[1]);
+        *reinterpret_cast<uint2 *>(lo) = make_uint2(pl[0], pl[1]);
+    }
+};
+
 template <typename TA, int D, int NW>
-__global__ void __launch_bounds__(TcCfg<TA, D, NW>::NT)
+__global__ void __launch_bounds__(TcCfg<TA, D, NW>::NT, 1)
 gdn_scan_tc_kernel(const gdn_params p) {
     using C = TcCfg<TA, D, NW>;
     using A = Act<TA>;
     using Sm = TcSmem<TA, D, NW>;
-    constexpr int RB = C::RB, NTILE = C::NTILE, KST = C::KST;
+    constexpr int RB = C::RB, NTILE = C::NTILE, KST = C::KST, NP = C::NP, NT = C::NT, PT = C::PT;
+    constexpr bool EXACT = C::EXACT;
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
@@ -144,11 +246,10 @@ gdn_scan_tc_kernel(const gdn_params p) {
     const int hv = static_cast<int>(head - static_cast<int64_t>(b) * p.Hv);
     const int hk = hv / (p.Hv / p.Hk);
     const int r0 = rblk * RB;                              // first memory row of this CTA
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;                // MMA fragment coordinates
-    const int wrow = warp * 16;                            // first local row of this warp
     const int S = p.S;
+    const int nchunks = (S + kT - 1) / kT;
 
     int64_t k_base, k_ts, v_base, v_ts, g_base, g_ts;
     if (p.head_major) {
@@ -160,203 +261,423 @@ gdn_scan_tc_kernel(const gdn_params p) {
         v_base = (static_cast<int64_t>(b) * S * p.Hv + hv) * D;  v_ts = static_cast<int64_t>(p.Hv) * D;
         g_base = static_cast<int64_t>(b) * S * p.Hv + hv;        g_ts = p.Hv;
     }
+    const bool fused_norm = C::WHOLE_HEAD && p.z != nullptr;
+
+    if (warp < NW) {
+        // ============================ row warps: the recurrence =============================
+        const int wrow = warp * 16;                        // first local row of this warp
+        const int m = lane >> 3, r = lane & 7;             // ldmatrix address roles
+        // the warp's 16 x D block of the memory as accumulator fragments:
+        // sacc[j] = S[wrow+g][8j+2tq], S[wrow+g][8j+2tq+1], S[wrow+g+8][8j+2tq], S[..+8][..+1]
+        float sacc[NTILE][4];
+        {
+            const float *s0 = p.s0 ? p.s0 + head * (D * D) + static_cast<int64_t>(r0 + wrow) * D : nullptr;
+#pragma unroll
+            for (int j = 0; j < NTILE; j++) {
+                float2 lo = make_float2(0.f, 0.f), hi = lo;
+                if (s0) {
+                    lo = *reinterpret_cast<const float2 *>(s0 + g * D + 8 * j + 2 * tq);
+                    hi = *reinterpret_cast<const float2 *>(s0 + (g + 8) * D + 8 * j + 2 * tq);
+                }
+                sacc[j][0] = lo.x; sacc[j][1] = lo.y; sacc[j][2] = hi.x; sacc[j][3] = hi.y;
+            }
+        }
+        float lam = 1.0f;                                  // true memory = lam * registers
+        for (int ch = 0; ch < nchunks; ch++) {
+            const int hb = ch & 1, os = ch % C::NOP, vs = ch % C::NVZ;
+            const int nt = min(kT, S - ch * kT);
+            bar_sync(kBarFull0 + hb, NT);                  // chunk ch staged
+            for (int blk = 0; blk * kB < nt; blk++) {
+                const int tb = blk * kB;
+                const int nb = min(kB, nt - tb);
+
+                // X = S' K^T, Y = S' Q^T for the block's 16 tokens (two n8 tiles each)
+                float xa[2][4] = {}, ya[2][4] = {};
+#pragma unroll
+                for (int kk = 0; kk < KST; kk++) {
+                    uint32_t ah[4], al[4];
+                    split2(sacc[2 * kk][0], sacc[2 * kk][1], ah[0], al[0]);
+                    split2(sacc[2 * kk][2], sacc[2 * kk][3], ah[1], al[1]);
+                    split2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ah[2], al[2]);
+                    split2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ah[3], al[3]);
+                    if constexpr (EXACT) {
+                        // matrices: (tokens 0-7 | 8-15) x (k 0-7 | 8-15): both n8 tiles at once
+                        const int trow = tb + 8 * (m >> 1) + r, col = 16 * kk + 8 * (m & 1);
+                        uint32_t kb[4], qb[4];
+                        ldsm_x4(kb, &sm.op.k[os][trow][col]);
+                        ldsm_x4(qb, &sm.op.q[os][trow][col]);
+                        mma2(xa[0], ah, al, kb[0], kb[1]);
+                        mma2(xa[1], ah, al, kb[2], kb[3]);
+                        mma2(ya[0], ah, al, qb[0], qb[1]);
+                        mma2(ya[1], ah, al, qb[2], qb[3]);
+                    } else {
+#pragma unroll
+                        for (int nt8 = 0; nt8 < 2; nt8++) {
+                            const int trow = tb + 8 * nt8 + r, col = 16 * kk + 8 * (m & 1);
+                            uint32_t kb[4], qb[4];
+                            ldsm_x4(kb, (m & 2) ? &sm.op.klo[os][trow][col] : &sm.op.khi[os][trow][col]);
+                            ldsm_x4(qb, (m & 2) ? &sm.op.qlo[os][trow][col] : &sm.op.qhi[os][trow][col]);
+                            mma3(xa[nt8], ah, al, kb[0], kb[1], kb[2], kb[3]);
+                            mma3(ya[nt8], ah, al, qb[0], qb[1], qb[2], qb[3]);
+                        }
+                    }
+                }
+                // r = beta (v - lam alpha D rk x) and lam alpha D rq y at this lane's positions;
+                // exact zeros past the sequence end (those columns meet every other token's
+                // terms in the d, O and update MMAs)
+                float ra[2][4], oa[2][4];
+#pragma unroll
+                for (int nt8 = 0; nt8 < 2; nt8++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int rr = g + ((e & 2) ? 8 : 0);
+                        const int t = 8 * nt8 + 2 * tq + (e & 1);
+                        const float4 cs = sm.cst[hb][tb + t];
+                        const float vv = A::one(&sm.vr[vs][tb + t][wrow + rr]);
+                        ra[nt8][e] = (t < nb) ? cs.x * (vv - lam * cs.y * xa[nt8][e]) : 0.f;
+                        oa[nt8][e] = lam * cs.z * ya[nt8][e];
+                    }
+                // d = r T  (A = r, rows x tokens s; B = T[s][t])
+                float da[2][4] = {};
+                {
+                    uint32_t rh[4], rl[4];
+                    split2(ra[0][0], ra[0][1], rh[0], rl[0]);
+                    split2(ra[0][2], ra[0][3], rh[1], rl[1]);
+                    split2(ra[1][0], ra[1][1], rh[2], rl[2]);
+                    split2(ra[1][2], ra[1][3], rh[3], rl[3]);
+#pragma unroll
+                    for (int nt8 = 0; nt8 < 2; nt8++) {
+                        uint32_t tbf[4];
+                        const int srow = r + ((m & 1) ? 8 : 0);
+                        ldsm_x4_t(tbf, (m & 2) ? &sm.tlo[hb][blk][srow][8 * nt8] : &sm.thi[hb][blk][srow][8 * nt8]);
+                        mma3(da[nt8], rh, rl, tbf[0], tbf[1], tbf[2], tbf[3]);
+                    }
+                }
+                // O = lam alpha D rq Y + d QX'
+                uint32_t dh[4], dl[4];
+                split2(da[0][0], da[0][1], dh[0], dl[0]);
+                split2(da[0][2], da[0][3], dh[1], dl[1]);
+                split2(da[1][0], da[1][1], dh[2], dl[2]);
+                split2(da[1][2], da[1][3], dh[3], dl[3]);
+#pragma unroll
+                for (int nt8 = 0; nt8 < 2; nt8++) {
+                    uint32_t pbf[4];
+                    const int srow = r + ((m & 1) ? 8 : 0);
+                    ldsm_x4_t(pbf, (m & 2) ? &sm.plo[hb][blk][srow][8 * nt8] : &sm.phi[hb][blk][srow][8 * nt8]);
+                    mma3(oa[nt8], dh, dl, pbf[0], pbf[1], pbf[2], pbf[3]);
+                }
+#pragma unroll
+                for (int nt8 = 0; nt8 < 2; nt8++) {
+                    const int t = 8 * nt8 + 2 * tq;
+                    if (t < nb) {
+                        sm.ob[hb][tb + t][wrow + g] = oa[nt8][0];
+                        sm.ob[hb][tb + t][wrow + g + 8] = oa[nt8][2];
+                    }
+                    if (t + 1 < nb) {
+                        sm.ob[hb][tb + t + 1][wrow + g] = oa[nt8][1];
+                        sm.ob[hb][tb + t + 1][wrow + g + 8] = oa[nt8][3];
+                    }
+                }
+                // the rank-16 update: C = d W rk / lam' (A fragment), S' += C K
+                const float lam_new = lam * sm.gam[hb][blk];
+                const bool fold = !(lam_new >= 0x1p-40f);  // uniform over the row warps
+                const float scale = fold ? 1.0f : 1.0f / lam_new;
+                float cf[2][4];
+#pragma unroll
+                for (int nt8 = 0; nt8 < 2; nt8++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int t = 8 * nt8 + 2 * tq + (e & 1);
+                        cf[nt8][e] = da[nt8][e] * sm.cst[hb][tb + t].w * scale;
+                    }
+                uint32_t ch_[4], cl_[4];
+                split2(cf[0][0], cf[0][1], ch_[0], cl_[0]);
+                split2(cf[0][2], cf[0][3], ch_[1], cl_[1]);
+                split2(cf[1][0], cf[1][1], ch_[2], cl_[2]);
+                split2(cf[1][2], cf[1][3], ch_[3], cl_[3]);
+                if (fold) {
+#pragma unroll
+                    for (int j = 0; j < NTILE; j++)
+#pragma unroll
+                        for (int e = 0; e < 4; e++) sacc[j][e] *= lam_new;
+                }
+                // S' += C K : B = K[tokens][cols 8j..8j+7], k = token (transposed ldmatrix)
+                if constexpr (EXACT) {
+#pragma unroll
+                    for (int j = 0; j < NTILE; j += 2) {
+                        uint32_t kb[4];
+                        const int trow = tb + r + ((m & 1) ? 8 : 0);
+                        ldsm_x4_t(kb, &sm.op.k[os][trow][8 * (j + (m >> 1))]);
+                        mma2(sacc[j], ch_, cl_, kb[0], kb[1]);
+                        mma2(sacc[j + 1], ch_, cl_, kb[2], kb[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NTILE; j++) {
+                        uint32_t kb[4];
+                        const int trow = tb + r + ((m & 1) ? 8 : 0);
+                        ldsm_x4_t(kb, (m & 2) ? &sm.op.klo[os][trow][8 * j] : &sm.op.khi[os][trow][8 * j]);
+                        mma3(sacc[j], ch_, cl_, kb[0], kb[1], kb[2], kb[3]);
+                    }
+                }
+                lam = fold ? 1.0f : lam_new;
+            }
+            bar_arrive(kBarEmpty0 + hb, NT);               // slots of chunk ch handed back
+        }
+        // final memory rows (undo the deferred decay)
+        float *so = p.state + head * (D * D) + static_cast<int64_t>(r0 + wrow) * D;
+#pragma unroll
+        for (int j = 0; j < NTILE; j++) {
+            *reinterpret_cast<float2 *>(so + g * D + 8 * j + 2 * tq) =
+                make_float2(lam * sacc[j][0], lam * sacc[j][1]);
+            *reinterpret_cast<float2 *>(so + (g + 8) * D + 8 * j + 2 * tq) =
+                make_float2(lam * sacc[j][2], lam * sacc[j][3]);
+        }
+        return;
+    }
+
+    // ============================== producer warps: staging ===============================
+    const int pw = warp - NW;                              // 0 .. NP-1
+    const int ptid = threadIdx.x - 32 * NW;                // 0 .. PT-1
     const TA *kg = static_cast<const TA *>(p.k) + k_base;
     const TA *qg = static_cast<const TA *>(p.q) + k_base;
     const TA *vg = static_cast<const TA *>(p.v) + v_base + r0;
-    const bool fused_norm = C::WHOLE_HEAD && p.z != nullptr;
     const TA *zg = fused_norm ? static_cast<const TA *>(p.z) + v_base : nullptr;
 
-    auto issue_chunk = [&](int t0, int buf) {
-        const int nt = min(kT, S - t0);
-        for (int i = tid; i < nt * C::KPIECES; i += C::NT) {
+    // copies of chunk c: raw k, q rows (into the operand ring for bf16, else the staging slot)
+    auto issue_kq = [&](int c) {
+        const int t0 = c * kT, nt = min(kT, S - t0);
+        for (int i = ptid; i < nt * C::KPIECES; i += PT) {
             const int tt = i / C::KPIECES, pc = i % C::KPIECES;
             const int64_t off = (t0 + tt) * k_ts;
-            cp_async16(reinterpret_cast<char *>(&sm.rawk[buf][tt][0]) + 16 * pc,
-                       reinterpret_cast<const char *>(kg + off) + 16 * pc);
-            cp_async16(reinterpret_cast<char *>(&sm.rawq[buf][tt][0]) + 16 * pc,
-                       reinterpret_cast<const char *>(qg + off) + 16 * pc);
+            char *dk, *dq;
+            if constexpr (EXACT) {
+                dk = reinterpret_cast<char *>(&sm.op.k[c % 3][tt][0]);
+                dq = reinterpret_cast<char *>(&sm.op.q[c % 3][tt][0]);
+            } else {
+                dk = reinterpret_cast<char *>(&sm.op.kraw[tt][0]);
+                dq = reinterpret_cast<char *>(&sm.op.qraw[tt][0]);
+            }
+            cp_async16(dk + 16 * pc, reinterpret_cast<const char *>(kg + off) + 16 * pc);
+            cp_async16(dq + 16 * pc, reinterpret_cast<const char *>(qg + off) + 16 * pc);
         }
-        for (int i = tid; i < nt * C::VPIECES; i += C::NT) {
+    };
+    auto issue_vz = [&](int c) {
+        const int t0 = c * kT, nt = min(kT, S - t0);
+        const int vs = c % C::NVZ;
+        for (int i = ptid; i < nt * C::VPIECES; i += PT) {
             const int tt = i / C::VPIECES, pc = i % C::VPIECES;
-            cp_async16(reinterpret_cast<char *>(&sm.rawv[buf][tt][0]) + 16 * pc,
-                       reinterpret_cast<const char *>(vg + (t0 + tt) * v_ts) + 16 * pc);
+            const int64_t off = (t0 + tt) * v_ts;
+            cp_async16(reinterpret_cast<char *>(&sm.vr[vs][tt][0]) + 16 * pc,
+                       reinterpret_cast<const char *>(vg + off) + 16 * pc);
             if (fused_norm)
-                cp_async16(reinterpret_cast<char *>(&sm.rawz[buf][tt][0]) + 16 * pc,
-                           reinterpret_cast<const char *>(zg + (t0 + tt) * v_ts) + 16 * pc);
+                cp_async16(reinterpret_cast<char *>(&sm.zr[vs][tt][0]) + 16 * pc,
+                           reinterpret_cast<const char *>(zg + off) + 16 * pc);
         }
-        cp_async_commit();
     };
 
-    // the warp's 16 x D block of the memory as accumulator fragments:
-    // sacc[j] = S[wrow+g][8j+2tq], S[wrow+g][8j+2tq+1], S[wrow+g+8][8j+2tq], S[wrow+g+8][8j+2tq+1]
-    float sacc[NTILE][4];
-    {
-        const float *s0 = p.s0 ? p.s0 + head * (D * D) + static_cast<int64_t>(r0 + wrow) * D : nullptr;
+    // y of a finished chunk.  Whole head with z: gated RMSNorm, 4 columns per thread, D / 4
+    // threads per token.  Otherwise this CTA's raw o rows (the norm kernel follows).
+    constexpr int TPT = D / 4;                             // threads per token (norm)
+    static_assert(TPT <= 32 && PT % TPT == 0, "norm thread groups");
+    float4 gn4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (fused_norm) gn4 = *reinterpret_cast<const float4 *>(p.gn + 4 * (ptid % TPT));
+    auto emit = [&](int c) {
+        const int hb = c & 1, vs = c % C::NVZ;
+        const int t0 = c * kT, nt = min(kT, S - t0);
+        if (fused_norm) {
+            const int col = 4 * (ptid % TPT);
 #pragma unroll
-        for (int j = 0; j < NTILE; j++) {
-            float2 lo = make_float2(0.f, 0.f), hi = lo;
-            if (s0) {
-                lo = *reinterpret_cast<const float2 *>(s0 + g * D + 8 * j + 2 * tq);
-                hi = *reinterpret_cast<const float2 *>(s0 + (g + 8) * D + 8 * j + 2 * tq);
+            for (int it = 0; it < kT * TPT / PT; it++) {
+                const int tt = ptid / TPT + it * (PT / TPT);
+                const float4 o4 = *reinterpret_cast<const float4 *>(&sm.ob[hb][tt][col]);
+                const float4 z4 = A::four(&sm.zr[vs][tt][col]);
+                const float x0 = o4.x * silu_fast(z4.x), x1 = o4.y * silu_fast(z4.y);
+                const float x2 = o4.z * silu_fast(z4.z), x3 = o4.w * silu_fast(z4.w);
+                float ss = fmaf(x0, x0, fmaf(x1, x1, fmaf(x2, x2, x3 * x3)));
+                ss = group_sum<TPT>(ss);
+                const float rr = rsqrtf(ss / static_cast<float>(D) + p.norm_eps);
+                if (tt < nt)
+                    *reinterpret_cast<float4 *>(p.y + v_base + (t0 + tt) * v_ts + col) =
+                        make_float4(x0 * rr * gn4.x, x1 * rr * gn4.y, x2 * rr * gn4.z, x3 * rr * gn4.w);
             }
-            sacc[j][0] = lo.x; sacc[j][1] = lo.y; sacc[j][2] = hi.x; sacc[j][3] = hi.y;
+        } else {
+            constexpr int TPR = RB / 4;                    // threads per token row
+            for (int i = ptid; i < nt * TPR; i += PT) {
+                const int tt = i / TPR, col = 4 * (i % TPR);
+                *reinterpret_cast<float4 *>(p.y + v_base + r0 + (t0 + tt) * v_ts + col) =
+                    *reinterpret_cast<const float4 *>(&sm.ob[hb][tt][col]);
+            }
         }
-    }
+    };
 
-    float gl = 0.f, gb = 0.f;
-    if (tid < kT && tid < S) {
-        gl = load_gate(p.log_decay, p.gate_dtype, g_base + tid * g_ts);
-        gb = load_gate(p.beta, p.gate_dtype, g_base + tid * g_ts);
+    float gl = 0.f, gb = 0.f;                              // gates of the chunk being staged
+    if (ptid < kT && ptid < S) {
+        gl = load_gate(p.log_decay, p.gate_dtype, g_base + ptid * g_ts);
+        gb = load_gate(p.beta, p.gate_dtype, g_base + ptid * g_ts);
     }
-    issue_chunk(0, 0);
-
+    issue_vz(0);
+    issue_kq(0);
+    cp_async_commit();
     const float inv_sqrt_dk = rsqrtf(static_cast<float>(D));
-    const int nchunks = (S + kT - 1) / kT;
-    constexpr int EPL_OUT = (D + 31) / 32;
-    float gnr[EPL_OUT];                                    // the norm weight, read once
-#pragma unroll
-    for (int i = 0; i < EPL_OUT; i++) {
-        const int j = lane + 32 * i;
-        gnr[i] = (fused_norm && j < D) ? p.gn[j] : 0.f;
-    }
-    float lam = 1.0f;                                      // true memory = lam * registers
+    // norm-pass roles: token nt_tok, pieces nq, nq + TPK, ...; a quarter-warp of 8 lanes
+    // covers 8 tokens (conflict-free 16-byte accesses on the padded rows)
+    constexpr int TPW = 32 / C::TPK;                       // tokens per warp in the norm pass
+    const int n_tok = pw * TPW + lane % TPW;
+    const int nq = lane / TPW;
+
     for (int ch = 0; ch < nchunks; ch++) {
+        const int hb = ch & 1, os = ch % C::NOP;
         const int t0 = ch * kT;
         const int nt = min(kT, S - t0);
-        const int buf = ch & 1;
-        if (ch + 1 < nchunks) {
-            issue_chunk(t0 + kT, buf ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+        if (ch >= 2) {                                     // chunk ch-2 is done with parity hb
+            bar_sync(kBarEmpty0 + hb, NT);
+            emit(ch - 2);
+            bar_sync(kBarProd, PT);                        // its z slot is read: refill it
         }
-        __syncthreads();
+        if (ch + 1 < nchunks) {
+            issue_vz(ch + 1);
+            if constexpr (EXACT) issue_kq(ch + 1);
+        }
+        cp_async_commit();
+        cp_async_wait<1>();                                // all but chunk ch+1's copies
+        bar_sync(kBarProd, PT);
 
-        // ---- stage 1: q^, k^ as bf16 hi/lo operand arrays (rows past the sequence end are
-        //      zero so that the block MMAs see exact zeros there); gates; v, silu(z)
+        // ---- norm pass: rk, rq per token; bf16 hi / lo operands for other input types; zero
+        //      operand rows past the sequence end
+        if (n_tok < kT) {
+            float ssk = 0.f, ssq = 0.f;
+            const bool valid = n_tok < nt;
 #pragma unroll
-        for (int it = 0; it < kT / NW; it++) {             // fixed trip count: tokens overlap
-            const int tt = warp + it * NW;
-            constexpr int EPL = (D + 31) / 32;
-            float kx[EPL], qx[EPL];
-            float ssk = 0.f, ssq = 0.f, skq = 0.f;
-            const bool valid = tt < nt;                    // warp-uniform
+            for (int i = 0; i < C::KPIECES / C::TPK; i++) {
+                const int pc = nq + C::TPK * i;
+                if constexpr (EXACT) {
+                    uint4 *dk = reinterpret_cast<uint4 *>(&sm.op.k[os][n_tok][8 * pc]);
+                    uint4 *dq = reinterpret_cast<uint4 *>(&sm.op.q[os][n_tok][8 * pc]);
+                    if (valid) {
+                        Piece<TA>::sq(&sm.op.k[os][n_tok][8 * pc], ssk);
+                        Piece<TA>::sq(&sm.op.q[os][n_tok][8 * pc], ssq);
+                    } else {
+                        *dk = make_uint4(0u, 0u, 0u, 0u);
+                        *dq = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                } else {
+                    constexpr int E = Piece<TA>::E;
+                    if (valid) {
+                        Piece<TA>::split(&sm.op.kraw[n_tok][E * pc], &sm.op.khi[os][n_tok][E * pc],
+                                         &sm.op.klo[os][n_tok][E * pc], ssk);
+                        Piece<TA>::split(&sm.op.qraw[n_tok][E * pc], &sm.op.qhi[os][n_tok][E * pc],
+                                         &sm.op.qlo[os][n_tok][E * pc], ssq);
+                    } else {
 #pragma unroll
-            for (int i = 0; i < EPL; i++) {
-                const int j = lane + 32 * i;
-                kx[i] = (valid && j < D) ? A::one(&sm.rawk[buf][tt][j]) : 0.f;
-                qx[i] = (valid && j < D) ? A::one(&sm.rawq[buf][tt][j]) : 0.f;
-                ssk = fmaf(kx[i], kx[i], ssk);
-                ssq = fmaf(qx[i], qx[i], ssq);
-                skq = fmaf(kx[i], qx[i], skq);
+                        for (int e = 0; e < E; e++) {
+                            sm.op.khi[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                            sm.op.klo[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                            sm.op.qhi[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                            sm.op.qlo[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                        }
+                    }
+                }
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {       // the three sums reduce together
+            for (int off = TPW; off < 32; off <<= 1) {
                 ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
                 ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
-                skq += __shfl_xor_sync(0xffffffffu, skq, off);
             }
-            const float rk = rsqrtf(ssk + p.qk_eps);
-            const float rq = rsqrtf(ssq + p.qk_eps) * inv_sqrt_dk;
-#pragma unroll
-            for (int i = 0; i < EPL; i++) {
-                const int j = lane + 32 * i;
-                if (j < D) {
-                    split1(kx[i] * rk, sm.khi[tt][j], sm.klo[tt][j]);
-                    split1(qx[i] * rq, sm.qhi[tt][j], sm.qlo[tt][j]);
-                }
-            }
-            if (lane == 0) sm.tok[tt].z = skq * rk * rq;
+            if (nq == 0)
+                sm.nrm[n_tok] = valid ? make_float2(rsqrtf(ssk + p.qk_eps), rsqrtf(ssq + p.qk_eps) * inv_sqrt_dk)
+                                      : make_float2(0.f, 0.f);
         }
-        static_assert((kT * RB / 4) % C::NT == 0, "4-element groups tile the chunk's v slice");
-#pragma unroll
-        for (int it = 0; it < kT * RB / 4 / C::NT; it++) {   // 4 consecutive values per thread
-            const int i = 4 * (tid + it * C::NT);
-            const int tt = i / RB, j = i % RB;
-            if (tt < nt) {
-                *reinterpret_cast<float4 *>(&sm.vf[tt][j]) = A::four(&sm.rawv[buf][tt][j]);
-                if (fused_norm) {
-                    const float4 z4 = A::four(&sm.rawz[buf][tt][j]);
-                    *reinterpret_cast<float4 *>(&sm.sz[tt][j]) =
-                        make_float4(silu_fast(z4.x), silu_fast(z4.y), silu_fast(z4.z), silu_fast(z4.w));
-                }
-            }
+        bar_sync(kBarProd, PT);                            // staging consumed, norms written
+        if constexpr (!EXACT) {
+            if (ch + 1 < nchunks) issue_kq(ch + 1);        // overlaps the rest of this chunk
+            cp_async_commit();
         }
-        if (tid < kT) {
-            const float gc = (tid < nt) ? fmaxf(gl, kMinLogDecay) : 0.f;
-            sm.tok[tid].x = expf(gc);
-            sm.tok[tid].y = (tid < nt) ? gb : 0.f;
-            sm.tok[tid].w = gc;
-        }
-        if (tid < kT && t0 + kT + tid < S) {
-            const int64_t gi = g_base + static_cast<int64_t>(t0 + kT + tid) * g_ts;
-            gl = load_gate(p.log_decay, p.gate_dtype, gi);
-            gb = load_gate(p.beta, p.gate_dtype, gi);
-        }
-        __syncthreads();
 
-        // ---- stage 2: decay products per token; KK, QX by MMA; N and QX' tables
-        if (warp == 0) {                                   // kT == 32: one lane per token
-            // block-relative inclusive prefix sum of log_decay (invalid tokens hold 0)
-            const float gj = sm.tok[lane].w;
-            float upto = gj;
+        // ---- decay products and the per-token scalars (kT == 32: one lane per token)
+        if (pw == 0) {
+            const bool valid = lane < nt;
+            const float2 nr = sm.nrm[lane];
+            const float gc = valid ? fmaxf(gl, kMinLogDecay) : 0.f;
+            const float alpha = expf(gc), beta = valid ? gb : 0.f;
+            float upto = gc;                               // block-inclusive prefix sum
 #pragma unroll
             for (int off = 1; off < kB; off <<= 1) {
                 const float o = __shfl_up_sync(0xffffffffu, upto, off, kB);
                 if ((lane & (kB - 1)) >= off) upto += o;
             }
             const float total = __shfl_sync(0xffffffffu, upto, kB - 1, kB);
-            sm.dec[lane] = make_float4(expf(upto - gj), expf(total - upto), expf(total), upto);
+            const float ad = expf(upto);                   // alpha_t D_t
+            const float w = expf(total - upto);            // W_t
+            sm.tks[lane] = make_float4(alpha, beta, nr.x, nr.y);
+            sm.cum[lane] = upto;
+            sm.cst[hb][lane] = make_float4(beta, ad * nr.x, ad * nr.y, w * nr.x);
+            if ((lane & (kB - 1)) == kB - 1) sm.gam[hb][lane / kB] = expf(total);
+            if (t0 + kT + lane < S) {                      // next chunk's gates, in flight
+                const int64_t gi = g_base + static_cast<int64_t>(t0 + kT + lane) * g_ts;
+                gl = load_gate(p.log_decay, p.gate_dtype, gi);
+                gb = load_gate(p.beta, p.gate_dtype, gi);
+            }
         }
-        __syncthreads();
-        for (int task = warp; task < 4 * C::NBLK; task += NW) {
-            const int blk = task >> 2;
-            const bool isq = (task >> 1) & 1;
-            const int nt8 = task & 1;                      // which 8 tokens t
+        bar_sync(kBarProd, PT);
+
+        // ---- KK and QX of each block by MMA (one warp per block and table); N and QX'
+        static_assert(2 * C::NBLK == NP, "one table task per producer warp");
+        {
+            const int blk = pw >> 1;
+            const bool isq = pw & 1;
             const int tb = blk * kB;
-            float acc2[2][4] = {};                          // even / odd k-steps (shorter chains)
+            const int m = lane >> 3, r = lane & 7;
+            float acc[2][4] = {};                          // n8 tiles: tokens t 0-7, 8-15
 #pragma unroll
             for (int kk = 0; kk < KST; kk++) {
-                // A = K^[s = tb..tb+15][cols 16kk..16kk+15]  (hi and lo)
-                uint32_t ah[4], al[4];
-                const int m = lane >> 3, r = lane & 7;       // matrix, row of ldmatrix
-                {
-                    const int srow = tb + r + ((m & 1) ? 8 : 0);
-                    const int col = 16 * kk + ((m & 2) ? 8 : 0);
-                    ldsm_x4(ah, &sm.khi[srow][col]);
-                    ldsm_x4(al, &sm.klo[srow][col]);
-                }
-                // B = (K^ or Q^)^T: rows of the ldmatrix are tokens t, 8 columns each
-                uint32_t bb[4];
-                const int trow = tb + 8 * nt8 + r;
-                const int col = 16 * kk + ((m & 1) ? 8 : 0);
-                const __nv_bfloat16 *src = (m & 2) ? (isq ? &sm.qlo[trow][col] : &sm.klo[trow][col])
-                                                   : (isq ? &sm.qhi[trow][col] : &sm.khi[trow][col]);
-                ldsm_x4(bb, src);
-                mma3(acc2[kk & 1], ah, al, bb[0], bb[1], bb[2], bb[3]);
-            }
-            // epilogue: entry (s, t) with s = g or g + 8, t = 8 nt8 + 2 tq (+1)
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int s2 = g + ((e & 2) ? 8 : 0);
-                const int t = 8 * nt8 + 2 * tq + (e & 1);
-                const float dot = acc2[0][e] + acc2[1][e];
-                const float4 tk = sm.tok[tb + t];          // alpha, beta, k^.q^
-                float wgt = 0.f;                           // prod_{s<r<t} alpha_r
-                if (s2 < t) wgt = expf(sm.dec[tb + t - 1].w - sm.dec[tb + s2].w);
-                if (isq) {
-                    const float val = (s2 < t) ? tk.x * wgt * dot : (s2 == t ? tk.z : 0.f);
-                    split1(val, sm.phi[blk][s2][t], sm.plo[blk][s2][t]);
+                const int arow = tb + r + ((m & 1) ? 8 : 0), acol = 16 * kk + ((m & 2) ? 8 : 0);
+                if constexpr (EXACT) {
+                    uint32_t a[4], bb[4];
+                    ldsm_x4(a, &sm.op.k[os][arow][acol]);
+                    const int trow = tb + 8 * (m >> 1) + r, col = 16 * kk + 8 * (m & 1);
+                    ldsm_x4(bb, isq ? &sm.op.q[os][trow][col] : &sm.op.k[os][trow][col]);
+                    mma16816(acc[0], a, bb[0], bb[1]);
+                    mma16816(acc[1], a, bb[2], bb[3]);
                 } else {
-                    sm.nm[blk][s2][t] = (s2 < t) ? tk.y * tk.x * wgt * dot : 0.f;
+                    uint32_t ah[4], al[4];
+                    ldsm_x4(ah, &sm.op.khi[os][arow][acol]);
+                    ldsm_x4(al, &sm.op.klo[os][arow][acol]);
+#pragma unroll
+                    for (int nt8 = 0; nt8 < 2; nt8++) {
+                        const int trow = tb + 8 * nt8 + r, col = 16 * kk + 8 * (m & 1);
+                        uint32_t bb[4];
+                        const __nv_bfloat16 *src =
+                            (m & 2) ? (isq ? &sm.op.qlo[os][trow][col] : &sm.op.klo[os][trow][col])
+                                    : (isq ? &sm.op.qhi[os][trow][col] : &sm.op.khi[os][trow][col]);
+                        ldsm_x4(bb, src);
+                        mma3(acc[nt8], ah, al, bb[0], bb[1], bb[2], bb[3]);
+                    }
                 }
             }
+#pragma unroll
+            for (int nt8 = 0; nt8 < 2; nt8++)
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int s2 = g + ((e & 2) ? 8 : 0);
+                    const int t = 8 * nt8 + 2 * tq + (e & 1);
+                    const float4 tk = sm.tks[tb + t];      // alpha, beta, rk, rq of token t
+                    const float dot = acc[nt8][e] * sm.tks[tb + s2].z;   // rk_s (k_s . x_t)
+                    float wgt = 0.f;                       // prod_{s<r<t} alpha_r
+                    if (s2 < t) wgt = expf(sm.cum[tb + t - 1] - sm.cum[tb + s2]);
+                    if (isq) {
+                        const float val = (s2 < t) ? tk.x * wgt * tk.w * dot : (s2 == t ? tk.w * dot : 0.f);
+                        split1(val, sm.phi[hb][blk][s2][t], sm.plo[hb][blk][s2][t]);
+                    } else {
+                        sm.nm[blk][s2][t] = (s2 < t) ? tk.y * tk.x * wgt * tk.z * dot : 0.f;
+                    }
+                }
         }
-        __syncthreads();
-        // T = (I + N)^-1 (unit upper triangular): lane s of warp blk builds row s by forward
-        // accumulation, T[s][t] = -sum_{s<=r<t} T[s][r] N[r][t].
-        if (warp < C::NBLK && lane < kB) {
-            const int blk = warp, srow = lane;
+        bar_sync(kBarProd, PT);
+        // T = (I + N)^-1 (unit upper triangular): lane s of producer warp blk builds row s by
+        // forward accumulation, T[s][t] = -sum_{s<=r<t} T[s][r] N[r][t].
+        if (pw < C::NBLK && lane < kB) {
+            const int blk = pw, srow = lane;
             float tr[kB], acc[kB];
 #pragma unroll
             for (int t = 0; t < kB; t++) { tr[t] = (t == srow) ? 1.f : 0.f; acc[t] = 0.f; }
@@ -368,174 +689,14 @@ gdn_scan_tc_kernel(const gdn_params p) {
             }
             if (kB - 1 > srow) tr[kB - 1] = -acc[kB - 1];
 #pragma unroll
-            for (int t = 0; t < kB; t++) split1(tr[t], sm.thi[blk][srow][t], sm.tlo[blk][srow][t]);
+            for (int t = 0; t < kB; t++) split1(tr[t], sm.thi[hb][blk][srow][t], sm.tlo[hb][blk][srow][t]);
         }
-        __syncthreads();
-
-        // ---- stage 3: the blocks; each warp on its own 16 rows, no inter-warp sync
-        for (int blk = 0; blk * kB < nt; blk++) {
-            const int tb = blk * kB;
-            const int nb = min(kB, nt - tb);
-
-            // X = S' K^T, Y = S' Q^T for the block's 16 tokens (two n8 tiles each)
-            float xa[2][4] = {}, ya[2][4] = {};
-#pragma unroll
-            for (int kk = 0; kk < KST; kk++) {
-                uint32_t ah[4], al[4];
-                split2(sacc[2 * kk][0], sacc[2 * kk][1], ah[0], al[0]);
-                split2(sacc[2 * kk][2], sacc[2 * kk][3], ah[1], al[1]);
-                split2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ah[2], al[2]);
-                split2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ah[3], al[3]);
-#pragma unroll
-                for (int nt8 = 0; nt8 < 2; nt8++) {
-                    const int m = lane >> 3, r = lane & 7;
-                    const int trow = tb + 8 * nt8 + r;
-                    const int col = 16 * kk + ((m & 1) ? 8 : 0);
-                    uint32_t kb[4], qb[4];
-                    ldsm_x4(kb, (m & 2) ? &sm.klo[trow][col] : &sm.khi[trow][col]);
-                    ldsm_x4(qb, (m & 2) ? &sm.qlo[trow][col] : &sm.qhi[trow][col]);
-                    mma3(xa[nt8], ah, al, kb[0], kb[1], kb[2], kb[3]);
-                    mma3(ya[nt8], ah, al, qb[0], qb[1], qb[2], qb[3]);
-                }
-            }
-            // r = beta (v - alpha lam D x), and lam alpha D Y, at this lane's fragment positions
-            float ra[2][4], oa[2][4];
-#pragma unroll
-            for (int nt8 = 0; nt8 < 2; nt8++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const int rr = g + ((e & 2) ? 8 : 0);
-                    const int t = 8 * nt8 + 2 * tq + (e & 1);
-                    const float4 tk = sm.tok[tb + t];     // alpha, beta
-                    const float lad = lam * tk.x * sm.dec[tb + t].x;
-                    // exact zeros past the sequence end: those columns meet every other
-                    // token's terms in the d, O and update MMAs
-                    ra[nt8][e] = (t < nb) ? tk.y * (sm.vf[tb + t][wrow + rr] - lad * xa[nt8][e]) : 0.f;
-                    oa[nt8][e] = lad * ya[nt8][e];
-                }
-            // d = r T  (A = r, rows x tokens s; B = T[s][t])
-            float da[2][4] = {};
-            {
-                uint32_t rh[4], rl[4];
-                split2(ra[0][0], ra[0][1], rh[0], rl[0]);
-                split2(ra[0][2], ra[0][3], rh[1], rl[1]);
-                split2(ra[1][0], ra[1][1], rh[2], rl[2]);
-                split2(ra[1][2], ra[1][3], rh[3], rl[3]);
-#pragma unroll
-                for (int nt8 = 0; nt8 < 2; nt8++) {
-                    uint32_t tbf[4];
-                    const int m = lane >> 3, r = lane & 7;
-                    const int srow = r + ((m & 1) ? 8 : 0);
-                    ldsm_x4_t(tbf, (m & 2) ? &sm.tlo[blk][srow][8 * nt8] : &sm.thi[blk][srow][8 * nt8]);
-                    mma3(da[nt8], rh, rl, tbf[0], tbf[1], tbf[2], tbf[3]);
-                }
-            }
-            // O = lam alpha D Y + d QX'
-            uint32_t dh[4], dl[4];
-            split2(da[0][0], da[0][1], dh[0], dl[0]);
-            split2(da[0][2], da[0][3], dh[1], dl[1]);
-            split2(da[1][0], da[1][1], dh[2], dl[2]);
-            split2(da[1][2], da[1][3], dh[3], dl[3]);
-#pragma unroll
-            for (int nt8 = 0; nt8 < 2; nt8++) {
-                uint32_t pbf[4];
-                const int m = lane >> 3, r = lane & 7;
-                const int srow = r + ((m & 1) ? 8 : 0);
-                ldsm_x4_t(pbf, (m & 2) ? &sm.plo[blk][srow][8 * nt8] : &sm.phi[blk][srow][8 * nt8]);
-                mma3(oa[nt8], dh, dl, pbf[0], pbf[1], pbf[2], pbf[3]);
-            }
-#pragma unroll
-            for (int nt8 = 0; nt8 < 2; nt8++) {
-                const int t = 8 * nt8 + 2 * tq;
-                if (t < nb) {
-                    sm.ob[tb + t][wrow + g] = oa[nt8][0];
-                    sm.ob[tb + t][wrow + g + 8] = oa[nt8][2];
-                }
-                if (t + 1 < nb) {
-                    sm.ob[tb + t + 1][wrow + g] = oa[nt8][1];
-                    sm.ob[tb + t + 1][wrow + g + 8] = oa[nt8][3];
-                }
-            }
-            // the rank-16 update: C = d W / lam' (A fragment), S' += C K^
-            const float gam = sm.dec[tb].z;
-            const float lam_new = lam * gam;
-            const bool fold = !(lam_new >= 0x1p-40f);      // CTA-uniform
-            const float scale = fold ? 1.0f : 1.0f / lam_new;
-            float cf[2][4];
-#pragma unroll
-            for (int nt8 = 0; nt8 < 2; nt8++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const int t = 8 * nt8 + 2 * tq + (e & 1);
-                    cf[nt8][e] = da[nt8][e] * sm.dec[tb + t].y * scale;
-                }
-            // A fragment of the coefficients (rows x tokens, k = token)
-            uint32_t ch_[4], cl_[4];
-            split2(cf[0][0], cf[0][1], ch_[0], cl_[0]);
-            split2(cf[0][2], cf[0][3], ch_[1], cl_[1]);
-            split2(cf[1][0], cf[1][1], ch_[2], cl_[2]);
-            split2(cf[1][2], cf[1][3], ch_[3], cl_[3]);
-            if (fold) {
-#pragma unroll
-                for (int j = 0; j < NTILE; j++)
-#pragma unroll
-                    for (int e = 0; e < 4; e++) sacc[j][e] *= lam_new;
-            }
-            // S' += C K^ : B = K^[tokens][cols 8j..8j+7], k = token (transposed ldmatrix)
-#pragma unroll
-            for (int j = 0; j < NTILE; j++) {
-                uint32_t kb[4];
-                const int m = lane >> 3, r = lane & 7;
-                const int trow = tb + r + ((m & 1) ? 8 : 0);
-                ldsm_x4_t(kb, (m & 2) ? &sm.klo[trow][8 * j] : &sm.khi[trow][8 * j]);
-                mma3(sacc[j], ch_, cl_, kb[0], kb[1], kb[2], kb[3]);
-            }
-            lam = fold ? 1.0f : lam_new;
-        }
-        __syncthreads();
-
-        // ---- outputs of the chunk
-        if (fused_norm) {
-            float *yg = p.y + v_base;
-#pragma unroll
-            for (int it = 0; it < kT / NW; it++) {
-                const int tt = warp + it * NW;
-                if (tt >= nt) break;                       // warp-uniform
-                constexpr int EPL = (D + 31) / 32;
-                const int64_t off = static_cast<int64_t>(t0 + tt) * v_ts;
-                float x[EPL];
-                float ss = 0.f;
-#pragma unroll
-                for (int i = 0; i < EPL; i++) {
-                    const int j = lane + 32 * i;
-                    x[i] = (j < D) ? sm.ob[tt][j] * sm.sz[tt][j] : 0.f;
-                    ss = fmaf(x[i], x[i], ss);
-                }
-                ss = group_sum<32>(ss);
-                const float rr = rsqrtf(ss / static_cast<float>(D) + p.norm_eps);
-#pragma unroll
-                for (int i = 0; i < EPL; i++) {
-                    const int j = lane + 32 * i;
-                    if (j < D) yg[off + j] = x[i] * rr * gnr[i];
-                }
-            }
-        } else {
-            float *yg = p.y + v_base + r0;
-            for (int i = tid; i < nt * RB; i += C::NT) {
-                const int tt = i / RB, j = i % RB;
-                yg[static_cast<int64_t>(t0 + tt) * v_ts + j] = sm.ob[tt][j];
-            }
-        }
+        bar_arrive(kBarFull0 + hb, NT);                    // chunk ch ready for the row warps
     }
-
-    // final memory rows (undo the deferred decay)
-    float *so = p.state + head * (D * D) + static_cast<int64_t>(r0 + wrow) * D;
-#pragma unroll
-    for (int j = 0; j < NTILE; j++) {
-        *reinterpret_cast<float2 *>(so + g * D + 8 * j + 2 * tq) =
-            make_float2(lam * sacc[j][0], lam * sacc[j][1]);
-        *reinterpret_cast<float2 *>(so + (g + 8) * D + 8 * j + 2 * tq) =
-            make_float2(lam * sacc[j][2], lam * sacc[j][3]);
+    // y of the last (up to two) chunks
+    for (int ch = max(0, nchunks - 2); ch < nchunks; ch++) {
+        bar_sync(kBarEmpty0 + (ch & 1), NT);
+        emit(ch);
     }
 }
 

@@ -476,30 +476,48 @@ gdn_scan_tc_kernel(const gdn_params p) {
         }
     };
 
-    // y of a finished chunk.  Whole head with z: gated RMSNorm, 4 columns per thread, D / 4
-    // threads per token.  Otherwise this CTA's raw o rows (the norm kernel follows).
-    constexpr int TPT = D / 4;                             // threads per token (norm)
-    static_assert(TPT <= 32 && PT % TPT == 0, "norm thread groups");
-    float4 gn4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (fused_norm) gn4 = *reinterpret_cast<const float4 *>(p.gn + 4 * (ptid % TPT));
+    // y of a finished chunk.  Whole head with z: gated RMSNorm, TPT threads per token, each
+    // with FPT float4 column groups interleaved (a quarter-warp reads 128 contiguous bytes).
+    // Otherwise this CTA's raw o rows (the norm kernel follows).
+    constexpr int TPT = (D / 4 < 8) ? D / 4 : 8;           // threads per token (norm)
+    constexpr int FPT = D / (4 * TPT);                     // float4 groups per thread
+    static_assert(PT % TPT == 0 && (kT * TPT) % PT == 0, "norm thread groups");
+    float4 gn4[FPT];
+#pragma unroll
+    for (int f = 0; f < FPT; f++)
+        gn4[f] = fused_norm ? *reinterpret_cast<const float4 *>(p.gn + 4 * (ptid % TPT + TPT * f))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float inv_d = 1.0f / static_cast<float>(D);
     auto emit = [&](int c) {
         const int hb = c & 1, vs = c % C::NVZ;
         const int t0 = c * kT, nt = min(kT, S - t0);
         if (fused_norm) {
-            const int col = 4 * (ptid % TPT);
 #pragma unroll
             for (int it = 0; it < kT * TPT / PT; it++) {
                 const int tt = ptid / TPT + it * (PT / TPT);
-                const float4 o4 = *reinterpret_cast<const float4 *>(&sm.ob[hb][tt][col]);
-                const float4 z4 = A::four(&sm.zr[vs][tt][col]);
-                const float x0 = o4.x * silu_fast(z4.x), x1 = o4.y * silu_fast(z4.y);
-                const float x2 = o4.z * silu_fast(z4.z), x3 = o4.w * silu_fast(z4.w);
-                float ss = fmaf(x0, x0, fmaf(x1, x1, fmaf(x2, x2, x3 * x3)));
+                float4 x[FPT];
+                float ss = 0.f;
+#pragma unroll
+                for (int f = 0; f < FPT; f++) {
+                    const int col = 4 * (ptid % TPT + TPT * f);
+                    const float4 o4 = *reinterpret_cast<const float4 *>(&sm.ob[hb][tt][col]);
+                    const float4 z4 = A::four(&sm.zr[vs][tt][col]);
+                    x[f] = make_float4(o4.x * silu_fast(z4.x), o4.y * silu_fast(z4.y),
+                                       o4.z * silu_fast(z4.z), o4.w * silu_fast(z4.w));
+                    ss = fmaf(x[f].x, x[f].x, fmaf(x[f].y, x[f].y, fmaf(x[f].z, x[f].z, fmaf(x[f].w, x[f].w, ss))));
+                }
                 ss = group_sum<TPT>(ss);
-                const float rr = rsqrtf(ss / static_cast<float>(D) + p.norm_eps);
-                if (tt < nt)
-                    *reinterpret_cast<float4 *>(p.y + v_base + (t0 + tt) * v_ts + col) =
-                        make_float4(x0 * rr * gn4.x, x1 * rr * gn4.y, x2 * rr * gn4.z, x3 * rr * gn4.w);
+                const float rr = rsqrtf(fmaf(ss, inv_d, p.norm_eps));
+                if (tt < nt) {
+                    float *yr = p.y + v_base + (t0 + tt) * v_ts;
+#pragma unroll
+                    for (int f = 0; f < FPT; f++) {
+                        const int col = 4 * (ptid % TPT + TPT * f);
+                        *reinterpret_cast<float4 *>(yr + col) =
+                            make_float4(x[f].x * rr * gn4[f].x, x[f].y * rr * gn4[f].y,
+                                        x[f].z * rr * gn4[f].z, x[f].w * rr * gn4[f].w);
+                    }
+                }
             }
         } else {
             constexpr int TPR = RB / 4;                    // threads per token row

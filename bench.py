@@ -38,6 +38,8 @@ from linear_attention_recurrence_gdn_gb300.workloads import (  # noqa: E402
 
 METRIC = "GDN decode step: state HBM GB/s (% of peak); gdn_scan tokens/sec"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+MMA_SYNC_MAC_PER_CLK_SM = 1024  # measured issue rate of mma.sync bf16 m16n8k16 per SM
 FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM
 MAX_SM_MHZ_FALLBACK = 2070.0
 
@@ -57,6 +59,21 @@ def scan_flops(w: Workload) -> int:
     return 6 * w.Dk * w.Dv * w.B * w.S * w.Hv
 
 
+def scan_mma_flops(w: Workload) -> int:
+    """Tensor-core FLOPs the block form issues per launch for its row MMAs.
+
+    Per warp (16 memory rows) and 16-token block: X and Y (4 KST MMAs per operand term), d and
+    O (6 each, hi/lo split operands on both sides), the update (NTILE per term); bf16 inputs are
+    exact bf16 operands (2 terms), other types split into hi + lo (3 terms).  Each m16n8k16 MMA
+    is 2 * 16 * 8 * 16 FLOP.  The per-chunk KK / QX tables (under 4% more) are not counted.
+    """
+    terms = 2 if w.act == "bf16" else 3
+    kst, ntile = w.Dk // 16, w.Dv // 8
+    per_warp_block = 4 * kst * terms + 12 + ntile * terms
+    warps_per_head = w.Dv // 16
+    return (w.B * w.Hv * warps_per_head * per_warp_block * 2 * 16 * 8 * 16 * w.S) // 16
+
+
 def scan_bytes(w: Workload) -> int:
     e = w.elem_bytes
     s0 = 4 * w.B * w.Hv * w.Dv * w.Dk if w.s0_std is not None else 0
@@ -70,10 +87,11 @@ def load_peaks() -> dict:
         with open(path) as f:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured",
+                "bf16_tflops": float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)),
                 "sm_max_mhz": float(d.get("sm_max_mhz", MAX_SM_MHZ_FALLBACK))}
     except (OSError, KeyError, ValueError):
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback",
-                "sm_max_mhz": MAX_SM_MHZ_FALLBACK}
+                "bf16_tflops": FALLBACK_BF16_TFLOPS, "sm_max_mhz": MAX_SM_MHZ_FALLBACK}
 
 
 def profiled_traffic(kernel_file: str, summary: str):
@@ -298,7 +316,7 @@ def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
 
 # ------------------------------------------------------------------------------ scan
 
-def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float):
+def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks: dict):
     inp = make_inputs(w)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     y = torch.empty(d["v"].shape, dtype=torch.float32, device=dev)
@@ -320,18 +338,31 @@ def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float):
         torch.cuda.synchronize(dev)
         times.append(e0.elapsed_time(e1))
     ms = statistics.median(times)
-    peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
-    achieved = scan_flops(w) / (ms * 1e-3) / 1e12
-    return {"config": w.as_config(), "value": w.B * w.S / (ms * 1e-3), "unit": "tokens/s",
+    secs = ms * 1e-3
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    fp32_eq = scan_flops(w) / secs / 1e12
+    mma = scan_mma_flops(w) / secs / 1e12
+    mma_sync_peak = sms * MMA_SYNC_MAC_PER_CLK_SM * 2 * sm_mhz * 1e6 / 1e12
+    bf16 = peaks["bf16_tflops"]
+    return {"config": w.as_config(), "value": w.B * w.S / secs, "unit": "tokens/s",
             "ms": ms, "reps": reps,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                         "peak_note": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x "
-                                      f"{sm_mhz:.0f} MHz (max SM clock)",
-                         "work": "algorithmic 6 Dk Dv FLOP per token-head (the sequential "
-                                 "recurrence), f32-equivalent",
-                         "implementation": "tensor cores, mma.sync m16n8k16 bf16 with hi/lo "
-                                           "operand split (3 MMAs per product)"},
+            "roofline": {"bound": "tensor", "achieved": mma, "peak": bf16, "unit": "TFLOP/s",
+                         "frac": mma / bf16, "traffic": None,
+                         "peak_note": f"{peaks['source']} cuBLAS bf16 dense (tcgen05); the "
+                                      f"kernel issues mma.sync, whose own ceiling is "
+                                      f"{MMA_SYNC_MAC_PER_CLK_SM} MAC/clk/SM = "
+                                      f"{mma_sync_peak:.0f} TFLOP/s at {sm_mhz:.0f} MHz "
+                                      f"(frac {mma / mma_sync_peak:.3f} of it)",
+                         "work": "tensor-core FLOPs of the block form's row MMAs (X, Y, d, O, "
+                                 "update; hi/lo operand terms counted)"},
+            "fp32_equivalent": {"achieved": fp32_eq, "peak": fp32_peak, "unit": "TFLOP/s",
+                                "frac": fp32_eq / fp32_peak,
+                                "work": "6 Dk Dv FLOP per token-head (the sequential "
+                                        "recurrence's own count)",
+                                "peak_note": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
+                                             f"x {sm_mhz:.0f} MHz: the sequential form's "
+                                             f"FP32 roofline, which the tensor-core form "
+                                             f"may exceed"},
             "hbm_bytes": scan_bytes(w)}
 
 
@@ -442,7 +473,7 @@ def main(argv=None):
                           for x in scan_workloads]
     if args.only == "scan":
         out = [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
-                          peaks["sm_max_mhz"]) for x in scan_workloads]
+                          peaks["sm_max_mhz"], peaks) for x in scan_workloads]
         if rank == 0:
             print(json.dumps({"scan": out}), flush=True)
         return 0
@@ -462,7 +493,7 @@ def main(argv=None):
         sm_mhz = peaks["sm_max_mhz"]
         scan = {"metric": "gdn_scan tokens/sec", "note": "supplementary, not the headline",
                 "workloads": [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
-                                         sm_mhz) for x in scan_workloads]}
+                                         sm_mhz, peaks) for x in scan_workloads]}
     if sampler:
         sampler.stop()
 

@@ -66,6 +66,8 @@ def test_roofline_byte_and_flop_models():
     # 8 B per state element (read + write) dominates; the closed form of the bench's docstring
     assert bench.decode_bytes(DECODE_B64) == 271_073_792
     assert bench.scan_flops(PREFILL_B4) == 6 * 128 * 128 * 4 * 4096 * 32
+    # bf16 block form: per warp and 16-token block 64 (X, Y) + 12 (d, O) + 32 (update) MMAs
+    assert bench.scan_mma_flops(PREFILL_B4) == 4 * 32 * 8 * 108 * 4096 * 4096 // 16
 
 
 def test_reference_arm_prints_one_line(capsys):

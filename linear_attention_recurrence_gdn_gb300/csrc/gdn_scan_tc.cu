@@ -61,9 +61,17 @@ template <typename TA, int D, int NW> struct TcCfg {
     static constexpr bool EXACT = IsBf16<TA>::value;  // raw rows are exact bf16 operands
     static constexpr int RB = 16 * NW;               // rows per CTA (NW row warps)
     static constexpr int NRB = D / RB;               // CTAs per head
-    static constexpr int NP = 4;                     // producer warps
+    static constexpr int NP = (NW == 8) ? 8 : 4;     // producer warps
     static constexpr int PT = 32 * NP;               // producer threads
     static constexpr int NT = 32 * (NW + NP);
+    // 16 warps launch with 128 registers each; the row warps then take 168 from the producer
+    // warps, which keep 88 (setmaxnreg; 8 x 168 + 8 x 88 = 16 x 128)
+    static constexpr bool REG_SPLIT = (NT == 512);
+    static constexpr int REG_ROW = 168, REG_PROD = 88;
+    static_assert(!REG_SPLIT || (NW * REG_ROW + NP * REG_PROD == (NW + NP) * 128 &&
+                                 NW % 4 == 0 && NP % 4 == 0),
+                  "register split within the launch's registers, whole warpgroups");
+    static constexpr bool SPLIT_KQ = (NP == 8);      // norm pass: k on 4 warps, q on the others
     static constexpr int NTILE = D / 8;              // n-tiles of a warp's 16 x D memory block
     static constexpr int KST = D / 16;               // k-steps over D
     static constexpr int NBLK = kT / kB;
@@ -78,7 +86,8 @@ template <typename TA, int D, int NW> struct TcCfg {
     static constexpr int TPK = KPIECES < 4 ? KPIECES : 4;        // norm-pass threads per token
     static_assert(D % RB == 0 && D % 16 == 0, "shape");
     static_assert(KPIECES >= 1 && VPIECES >= 1, "16-byte copy granularity");
-    static_assert(KPIECES % TPK == 0 && PT / TPK >= kT, "norm pass covers a chunk at once");
+    static_assert(KPIECES % TPK == 0 && (SPLIT_KQ ? PT / 2 : PT) / TPK >= kT,
+                  "norm pass covers a chunk at once");
 };
 
 // k and q operands, rows padded by 16 bytes (conflict-free ldmatrix and 16-byte accesses).
@@ -149,6 +158,12 @@ __device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], con
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(addr)));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void *addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
                  : "r"(smem_u32(addr)));
 }
 
@@ -262,6 +277,10 @@ gdn_scan_tc_kernel(const gdn_params p) {
         g_base = static_cast<int64_t>(b) * S * p.Hv + hv;        g_ts = p.Hv;
     }
     const bool fused_norm = C::WHOLE_HEAD && p.z != nullptr;
+    if constexpr (C::REG_SPLIT) {
+        if (warp < NW) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(C::REG_ROW));
+        else asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(C::REG_PROD));
+    }
 
     if (warp < NW) {
         // ============================ row warps: the recurrence =============================
@@ -541,7 +560,9 @@ gdn_scan_tc_kernel(const gdn_params p) {
     // norm-pass roles: token nt_tok, pieces nq, nq + TPK, ...; a quarter-warp of 8 lanes
     // covers 8 tokens (conflict-free 16-byte accesses on the padded rows)
     constexpr int TPW = 32 / C::TPK;                       // tokens per warp in the norm pass
-    const int n_tok = pw * TPW + lane % TPW;
+    const bool do_k = !C::SPLIT_KQ || pw < NP / 2;         // this warp's rows: k, q or both
+    const bool do_q = !C::SPLIT_KQ || pw >= NP / 2;
+    const int n_tok = (C::SPLIT_KQ ? pw % (NP / 2) : pw) * TPW + lane % TPW;
     const int nq = lane / TPW;
 
     for (int ch = 0; ch < nchunks; ch++) {
@@ -573,26 +594,32 @@ gdn_scan_tc_kernel(const gdn_params p) {
                     uint4 *dk = reinterpret_cast<uint4 *>(&sm.op.k[os][n_tok][8 * pc]);
                     uint4 *dq = reinterpret_cast<uint4 *>(&sm.op.q[os][n_tok][8 * pc]);
                     if (valid) {
-                        Piece<TA>::sq(&sm.op.k[os][n_tok][8 * pc], ssk);
-                        Piece<TA>::sq(&sm.op.q[os][n_tok][8 * pc], ssq);
+                        if (do_k) Piece<TA>::sq(&sm.op.k[os][n_tok][8 * pc], ssk);
+                        if (do_q) Piece<TA>::sq(&sm.op.q[os][n_tok][8 * pc], ssq);
                     } else {
-                        *dk = make_uint4(0u, 0u, 0u, 0u);
-                        *dq = make_uint4(0u, 0u, 0u, 0u);
+                        if (do_k) *dk = make_uint4(0u, 0u, 0u, 0u);
+                        if (do_q) *dq = make_uint4(0u, 0u, 0u, 0u);
                     }
                 } else {
                     constexpr int E = Piece<TA>::E;
                     if (valid) {
-                        Piece<TA>::split(&sm.op.kraw[n_tok][E * pc], &sm.op.khi[os][n_tok][E * pc],
-                                         &sm.op.klo[os][n_tok][E * pc], ssk);
-                        Piece<TA>::split(&sm.op.qraw[n_tok][E * pc], &sm.op.qhi[os][n_tok][E * pc],
-                                         &sm.op.qlo[os][n_tok][E * pc], ssq);
+                        if (do_k)
+                            Piece<TA>::split(&sm.op.kraw[n_tok][E * pc], &sm.op.khi[os][n_tok][E * pc],
+                                             &sm.op.klo[os][n_tok][E * pc], ssk);
+                        if (do_q)
+                            Piece<TA>::split(&sm.op.qraw[n_tok][E * pc], &sm.op.qhi[os][n_tok][E * pc],
+                                             &sm.op.qlo[os][n_tok][E * pc], ssq);
                     } else {
 #pragma unroll
                         for (int e = 0; e < E; e++) {
-                            sm.op.khi[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
-                            sm.op.klo[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
-                            sm.op.qhi[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
-                            sm.op.qlo[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                            if (do_k) {
+                                sm.op.khi[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                                sm.op.klo[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                            }
+                            if (do_q) {
+                                sm.op.qhi[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                                sm.op.qlo[os][n_tok][E * pc + e] = __float2bfloat16_rn(0.f);
+                            }
                         }
                     }
                 }
@@ -602,9 +629,10 @@ gdn_scan_tc_kernel(const gdn_params p) {
                 ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
                 ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
             }
-            if (nq == 0)
-                sm.nrm[n_tok] = valid ? make_float2(rsqrtf(ssk + p.qk_eps), rsqrtf(ssq + p.qk_eps) * inv_sqrt_dk)
-                                      : make_float2(0.f, 0.f);
+            if (nq == 0) {
+                if (do_k) sm.nrm[n_tok].x = valid ? rsqrtf(ssk + p.qk_eps) : 0.f;
+                if (do_q) sm.nrm[n_tok].y = valid ? rsqrtf(ssq + p.qk_eps) * inv_sqrt_dk : 0.f;
+            }
         }
         bar_sync(kBarProd, PT);                            // staging consumed, norms written
         if constexpr (!EXACT) {
@@ -639,48 +667,55 @@ gdn_scan_tc_kernel(const gdn_params p) {
         }
         bar_sync(kBarProd, PT);
 
-        // ---- KK and QX of each block by MMA (one warp per block and table); N and QX'
-        static_assert(2 * C::NBLK == NP, "one table task per producer warp");
+        // ---- KK and QX of each block by MMA; N and QX'.  The 4 NBLK n8 tiles, ordered
+        //      (block, table, tokens t 0-7 | 8-15), go NT8W to a producer warp.
         {
-            const int blk = pw >> 1;
-            const bool isq = pw & 1;
+            constexpr int NT8W = 4 * C::NBLK / NP;
+            static_assert(NT8W * NP == 4 * C::NBLK, "table tiles per producer warp");
+            const int tile0 = pw * NT8W;
+            const int blk = tile0 >> 2, nt0 = tile0 & 1;
+            const bool isq = (tile0 >> 1) & 1;
             const int tb = blk * kB;
             const int m = lane >> 3, r = lane & 7;
-            float acc[2][4] = {};                          // n8 tiles: tokens t 0-7, 8-15
+            float acc[NT8W][4] = {};
 #pragma unroll
             for (int kk = 0; kk < KST; kk++) {
                 const int arow = tb + r + ((m & 1) ? 8 : 0), acol = 16 * kk + ((m & 2) ? 8 : 0);
                 if constexpr (EXACT) {
-                    uint32_t a[4], bb[4];
+                    uint32_t a[4];
                     ldsm_x4(a, &sm.op.k[os][arow][acol]);
-                    const int trow = tb + 8 * (m >> 1) + r, col = 16 * kk + 8 * (m & 1);
-                    ldsm_x4(bb, isq ? &sm.op.q[os][trow][col] : &sm.op.k[os][trow][col]);
-                    mma16816(acc[0], a, bb[0], bb[1]);
-                    mma16816(acc[1], a, bb[2], bb[3]);
+#pragma unroll
+                    for (int j = 0; j < NT8W; j++) {
+                        // matrices (k 0-7 | 8-15) of tokens tb + 8 (nt0 + j) ..; lanes 16-31 mirror
+                        const int trow = tb + 8 * (nt0 + j) + r, col = 16 * kk + 8 * (m & 1);
+                        uint32_t bb[2];
+                        ldsm_x2(bb, isq ? &sm.op.q[os][trow][col] : &sm.op.k[os][trow][col]);
+                        mma16816(acc[j], a, bb[0], bb[1]);
+                    }
                 } else {
                     uint32_t ah[4], al[4];
                     ldsm_x4(ah, &sm.op.khi[os][arow][acol]);
                     ldsm_x4(al, &sm.op.klo[os][arow][acol]);
 #pragma unroll
-                    for (int nt8 = 0; nt8 < 2; nt8++) {
-                        const int trow = tb + 8 * nt8 + r, col = 16 * kk + 8 * (m & 1);
+                    for (int j = 0; j < NT8W; j++) {
+                        const int trow = tb + 8 * (nt0 + j) + r, col = 16 * kk + 8 * (m & 1);
                         uint32_t bb[4];
                         const __nv_bfloat16 *src =
                             (m & 2) ? (isq ? &sm.op.qlo[os][trow][col] : &sm.op.klo[os][trow][col])
                                     : (isq ? &sm.op.qhi[os][trow][col] : &sm.op.khi[os][trow][col]);
                         ldsm_x4(bb, src);
-                        mma3(acc[nt8], ah, al, bb[0], bb[1], bb[2], bb[3]);
+                        mma3(acc[j], ah, al, bb[0], bb[1], bb[2], bb[3]);
                     }
                 }
             }
 #pragma unroll
-            for (int nt8 = 0; nt8 < 2; nt8++)
+            for (int j = 0; j < NT8W; j++)
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     const int s2 = g + ((e & 2) ? 8 : 0);
-                    const int t = 8 * nt8 + 2 * tq + (e & 1);
+                    const int t = 8 * (nt0 + j) + 2 * tq + (e & 1);
                     const float4 tk = sm.tks[tb + t];      // alpha, beta, rk, rq of token t
-                    const float dot = acc[nt8][e] * sm.tks[tb + s2].z;   // rk_s (k_s . x_t)
+                    const float dot = acc[j][e] * sm.tks[tb + s2].z;   // rk_s (k_s . x_t)
                     float wgt = 0.f;                       // prod_{s<r<t} alpha_r
                     if (s2 < t) wgt = expf(sm.cum[tb + t - 1] - sm.cum[tb + s2]);
                     if (isq) {

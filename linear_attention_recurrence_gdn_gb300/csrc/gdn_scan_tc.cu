@@ -103,23 +103,25 @@ template <typename TA, int D> struct TcOps<TA, D, false> {
     __nv_bfloat16 qhi[2][kT][D + 8], qlo[2][kT][D + 8];
 };
 
-// Shared memory.  Slots are indexed by chunk: operands c % NOP, v / z c % 3, and everything
-// else the row warps read (o, per-token scalars, tables) c % 2.
+// Shared memory; every member 16-byte aligned (vector accesses, ldmatrix rows, cp.async).
+// Slots are indexed by chunk: operands c % NOP, v / z c % 3, and everything else the row warps
+// read (o, per-token scalars, tables) c % 2.
 template <typename TA, int D, int NW> struct TcSmem {
     using C = TcCfg<TA, D, NW>;
-    TcOps<TA, D, C::EXACT> op;
-    TA vr[C::NVZ][kT][C::LDV];       // raw v rows of this CTA
-    TA zr[C::NVZ][kT][C::LDV];       // raw z (whole-head CTAs with z)
-    float ob[2][kT][C::LDO];         // o of the chunk, written by the row warps
-    float4 cst[2][kT];               // row-warp scalars: beta, alpha D rk, alpha D rq, W rk
-    float4 tks[kT];                  // producer scalars: alpha, beta, rk, rq
-    float2 nrm[kT];                  // rk, rq from the norm pass
-    float cum[kT];                   // block-inclusive sums of the clamped log_decay
-    float gam[2][C::NBLK];           // Gam of each block
-    float nm[C::NBLK][kB][kB];       // N[s][t] = beta_t alpha_t KK[s][t] for s < t, else 0
+    alignas(16) TcOps<TA, D, C::EXACT> op;
+    alignas(16) TA vr[C::NVZ][kT][C::LDV];       // raw v rows of this CTA
+    alignas(16) TA zr[C::NVZ][kT][C::LDV];       // raw z (whole-head CTAs with z)
+    alignas(16) float ob[2][kT][C::LDO];         // o of the chunk, written by the row warps
+    alignas(16) float4 cst[2][kT];               // row-warp scalars: beta, alpha D rk, alpha D rq, W rk
+    alignas(16) float4 gts[kT];                  // producer: alpha, beta, alpha D, W of the staged chunk
+    alignas(16) float2 nrm[kT];                  // rk, rq from the norm pass
+    alignas(16) float cum[kT];                   // block-inclusive sums of the clamped log_decay
+    alignas(16) float gamp[C::NBLK];             // producer: Gam of each block of the staged chunk
+    alignas(16) float gam[2][C::NBLK];           // Gam of each block
+    alignas(16) float nm[C::NBLK][kB][kB];       // N[s][t] = beta_t alpha_t KK[s][t] for s < t, else 0
     // B operands [s][t] (k = s, n = t), bf16 hi/lo, rows padded to 24 (conflict-free ldmatrix):
-    __nv_bfloat16 thi[2][C::NBLK][kB][kB + 8], tlo[2][C::NBLK][kB][kB + 8];   // (I + N)^-1
-    __nv_bfloat16 phi[2][C::NBLK][kB][kB + 8], plo[2][C::NBLK][kB][kB + 8];   // QX'
+    alignas(16) __nv_bfloat16 thi[2][C::NBLK][kB][kB + 8], tlo[2][C::NBLK][kB][kB + 8];   // (I + N)^-1
+    alignas(16) __nv_bfloat16 phi[2][C::NBLK][kB][kB + 8], plo[2][C::NBLK][kB][kB + 8];   // QX'
 };
 
 // Named barriers (0 is __syncthreads): chunk parity b full / empty, and producers only.
@@ -548,10 +550,38 @@ gdn_scan_tc_kernel(const gdn_params p) {
         }
     };
 
-    float gl = 0.f, gb = 0.f;                              // gates of the chunk being staged
-    if (ptid < kT && ptid < S) {
-        gl = load_gate(p.log_decay, p.gate_dtype, g_base + ptid * g_ts);
-        gb = load_gate(p.beta, p.gate_dtype, g_base + ptid * g_ts);
+    // The gate warp computes a chunk's decay products one chunk ahead, beside the triangular
+    // inverse of the previous chunk (kT == 32: one lane per token); its lanes hold the gates
+    // of the chunk after that, in flight.
+    constexpr int GATE_WARP = NP - 1;
+    static_assert(GATE_WARP >= 1, "the gate warp is not the inverse warp");
+    float gl = 0.f, gb = 0.f;
+    auto load_gates = [&](int c) {
+        const int t = c * kT + lane;
+        if (t < S) {
+            const int64_t gi = g_base + static_cast<int64_t>(t) * g_ts;
+            gl = load_gate(p.log_decay, p.gate_dtype, gi);
+            gb = load_gate(p.beta, p.gate_dtype, gi);
+        }
+    };
+    auto decay_products = [&](int c) {                     // gates in gl, gb -> gts, cum, gamp
+        const bool valid = c * kT + lane < S;
+        const float gc = valid ? fmaxf(gl, kMinLogDecay) : 0.f;
+        float upto = gc;                                   // block-inclusive prefix sum
+#pragma unroll
+        for (int off = 1; off < kB; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, upto, off, kB);
+            if ((lane & (kB - 1)) >= off) upto += o;
+        }
+        const float total = __shfl_sync(0xffffffffu, upto, kB - 1, kB);
+        sm.gts[lane] = make_float4(expf(gc), valid ? gb : 0.f, expf(upto), expf(total - upto));
+        sm.cum[lane] = upto;
+        if ((lane & (kB - 1)) == kB - 1) sm.gamp[lane / kB] = expf(total);
+    };
+    if (pw == GATE_WARP) {
+        load_gates(0);
+        decay_products(0);
+        if (kT < S) load_gates(1);
     }
     issue_vz(0);
     issue_kq(0);
@@ -640,33 +670,6 @@ gdn_scan_tc_kernel(const gdn_params p) {
             cp_async_commit();
         }
 
-        // ---- decay products and the per-token scalars (kT == 32: one lane per token)
-        if (pw == 0) {
-            const bool valid = lane < nt;
-            const float2 nr = sm.nrm[lane];
-            const float gc = valid ? fmaxf(gl, kMinLogDecay) : 0.f;
-            const float alpha = expf(gc), beta = valid ? gb : 0.f;
-            float upto = gc;                               // block-inclusive prefix sum
-#pragma unroll
-            for (int off = 1; off < kB; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, upto, off, kB);
-                if ((lane & (kB - 1)) >= off) upto += o;
-            }
-            const float total = __shfl_sync(0xffffffffu, upto, kB - 1, kB);
-            const float ad = expf(upto);                   // alpha_t D_t
-            const float w = expf(total - upto);            // W_t
-            sm.tks[lane] = make_float4(alpha, beta, nr.x, nr.y);
-            sm.cum[lane] = upto;
-            sm.cst[hb][lane] = make_float4(beta, ad * nr.x, ad * nr.y, w * nr.x);
-            if ((lane & (kB - 1)) == kB - 1) sm.gam[hb][lane / kB] = expf(total);
-            if (t0 + kT + lane < S) {                      // next chunk's gates, in flight
-                const int64_t gi = g_base + static_cast<int64_t>(t0 + kT + lane) * g_ts;
-                gl = load_gate(p.log_decay, p.gate_dtype, gi);
-                gb = load_gate(p.beta, p.gate_dtype, gi);
-            }
-        }
-        bar_sync(kBarProd, PT);
-
         // ---- KK and QX of each block by MMA; N and QX'.  The 4 NBLK n8 tiles, ordered
         //      (block, table, tokens t 0-7 | 8-15), go NT8W to a producer warp.
         {
@@ -677,6 +680,12 @@ gdn_scan_tc_kernel(const gdn_params p) {
             const bool isq = (tile0 >> 1) & 1;
             const int tb = blk * kB;
             const int m = lane >> 3, r = lane & 7;
+            if (pw == 0) {                                 // the row warps' per-token scalars
+                const float4 gt = sm.gts[lane];
+                const float2 nr = sm.nrm[lane];
+                sm.cst[hb][lane] = make_float4(gt.y, gt.z * nr.x, gt.z * nr.y, gt.w * nr.x);
+                if (lane < C::NBLK) sm.gam[hb][lane] = sm.gamp[lane];
+            }
             float acc[NT8W][4] = {};
 #pragma unroll
             for (int kk = 0; kk < KST; kk++) {
@@ -714,35 +723,46 @@ gdn_scan_tc_kernel(const gdn_params p) {
                 for (int e = 0; e < 4; e++) {
                     const int s2 = g + ((e & 2) ? 8 : 0);
                     const int t = 8 * (nt0 + j) + 2 * tq + (e & 1);
-                    const float4 tk = sm.tks[tb + t];      // alpha, beta, rk, rq of token t
-                    const float dot = acc[j][e] * sm.tks[tb + s2].z;   // rk_s (k_s . x_t)
-                    float wgt = 0.f;                       // prod_{s<r<t} alpha_r
-                    if (s2 < t) wgt = expf(sm.cum[tb + t - 1] - sm.cum[tb + s2]);
+                    const float4 gt = sm.gts[tb + t];      // alpha, beta of token t
+                    const float2 nt_ = sm.nrm[tb + t];     // rk, rq of token t
+                    const float dot = acc[j][e] * sm.nrm[tb + s2].x;   // rk_s (k_s . x_t)
+                    // prod_{s<r<t} alpha_r: exp of a non-positive sum (fast exp: a few ulp,
+                    // about 1e-5 relative at the largest arguments that do not underflow)
+                    const float wgt = (s2 < t) ? __expf(sm.cum[tb + t - 1] - sm.cum[tb + s2]) : 0.f;
                     if (isq) {
-                        const float val = (s2 < t) ? tk.x * wgt * tk.w * dot : (s2 == t ? tk.w * dot : 0.f);
+                        const float val = (s2 < t) ? gt.x * wgt * nt_.y * dot : (s2 == t ? nt_.y * dot : 0.f);
                         split1(val, sm.phi[hb][blk][s2][t], sm.plo[hb][blk][s2][t]);
                     } else {
-                        sm.nm[blk][s2][t] = (s2 < t) ? tk.y * tk.x * wgt * tk.z * dot : 0.f;
+                        sm.nm[blk][s2][t] = (s2 < t) ? gt.y * gt.x * wgt * nt_.x * dot : 0.f;
                     }
                 }
         }
         bar_sync(kBarProd, PT);
-        // T = (I + N)^-1 (unit upper triangular): lane s of producer warp blk builds row s by
-        // forward accumulation, T[s][t] = -sum_{s<=r<t} T[s][r] N[r][t].
-        if (pw < C::NBLK && lane < kB) {
-            const int blk = pw, srow = lane;
+        // T = (I + N)^-1 (unit upper triangular): lane s of block blk (producer warp 0, lanes
+        // 16 blk + s) builds row s by forward accumulation, T[s][t] = -sum_{s<=r<t} T[s][r] N[r][t].
+        // Meanwhile the gate warp prepares the next chunk's decay products.
+        static_assert(C::NBLK * kB == 32, "one lane per row of the blocks' inverses");
+        if (pw == 0) {
+            const int blk = lane / kB, srow = lane % kB;
             float tr[kB], acc[kB];
 #pragma unroll
             for (int t = 0; t < kB; t++) { tr[t] = (t == srow) ? 1.f : 0.f; acc[t] = 0.f; }
 #pragma unroll
             for (int r = 0; r < kB - 1; r++) {
                 if (r > srow) tr[r] = -acc[r];
+                float nr[kB];
 #pragma unroll
-                for (int t = r + 1; t < kB; t++) acc[t] = fmaf(tr[r], sm.nm[blk][r][t], acc[t]);
+                for (int t4 = 0; t4 < kB / 4; t4++)
+                    *reinterpret_cast<float4 *>(&nr[4 * t4]) = *reinterpret_cast<const float4 *>(&sm.nm[blk][r][4 * t4]);
+#pragma unroll
+                for (int t = r + 1; t < kB; t++) acc[t] = fmaf(tr[r], nr[t], acc[t]);
             }
             if (kB - 1 > srow) tr[kB - 1] = -acc[kB - 1];
 #pragma unroll
             for (int t = 0; t < kB; t++) split1(tr[t], sm.thi[hb][blk][srow][t], sm.tlo[hb][blk][srow][t]);
+        } else if (pw == GATE_WARP && ch + 1 < nchunks) {
+            decay_products(ch + 1);                        // tables of chunk ch are done with them
+            if (ch + 2 < nchunks) load_gates(ch + 2);
         }
         bar_arrive(kBarFull0 + hb, NT);                    // chunk ch ready for the row warps
     }

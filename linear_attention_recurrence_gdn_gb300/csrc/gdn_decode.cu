@@ -120,6 +120,12 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
         mbar_init_fence();
     }
     __syncthreads();
+    // Programmatic dependent launch: the next kernel on the stream may start its set-up now;
+    // this one reads nothing from global memory before the previous kernel (the step that
+    // wrote the state, or whatever produced the inputs) has completed.  Both are no-ops in a
+    // plain launch.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     auto head_of = [&](int64_t i) -> int64_t { return blockIdx.x + i * gridDim.x; };
 #if GDN_DECODE_LDGSTS
@@ -363,7 +369,21 @@ cudaError_t launch_typed(const gdn_params &p, cudaStream_t stream) {
     }
     const int64_t heads = static_cast<int64_t>(p.B) * p.Hv;
     const int64_t grid = std::min<int64_t>(heads, slots);
-    kern<<<static_cast<unsigned>(grid), C::NT, bytes, stream>>>(p, heads);
+    // launched as a programmatic dependent of the previous kernel on the stream: its CTAs
+    // become resident as that kernel's CTAs retire and wait (griddepcontrol.wait) for its
+    // completion, which hides the launch gap between consecutive decode steps
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, heads);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

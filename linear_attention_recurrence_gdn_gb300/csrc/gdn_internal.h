@@ -19,7 +19,4 @@ cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
 // The scan on tensor cores (gdn_scan_tc.cu).
 cudaError_t launch_scan_tc(const gdn_params &p, cudaStream_t stream);
 
-// In-place gated RMSNorm of raw o in y (for scans whose heads are split over CTAs).
-cudaError_t launch_gated_norm(const gdn_params &p, cudaStream_t stream);
-
 }  // namespace gdn

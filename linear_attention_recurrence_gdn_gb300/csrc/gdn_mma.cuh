@@ -18,6 +18,24 @@ __device__ __forceinline__ void bar_arrive(int id, int count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Every thread of every CTA in the cluster meets here (hardware cluster barrier).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// v -> the same shared-memory location in the cluster's CTA `rank` (distributed shared
+// memory), counted as 4 bytes on that CTA's mbarrier `bar` (the local address of it).
+__device__ __forceinline__ void st_async_peer(const float *dst, float v, const uint64_t *bar,
+                                              int rank) {
+    uint32_t rd, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(smem_u32(dst)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(rd),
+                 "f"(v), "r"(rb)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
     asm volatile(

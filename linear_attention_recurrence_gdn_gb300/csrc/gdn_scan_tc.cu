@@ -36,8 +36,10 @@
 //     chunks ahead; the norms; decay products; KK, QX; the triangular inverse) and write y for
 //     finished chunks, while the row warps run chunk c.  Hand-off through rings of shared
 //     memory slots and named barriers (full / empty per chunk parity);
-//   * when a CTA owns a whole head the producers apply the gated RMSNorm; otherwise raw o goes
-//     to y and gdn_gated_norm_kernel applies the norm afterwards.
+//   * the producers apply the gated RMSNorm: over the CTA when it owns a whole head; when a
+//     head's rows are split over NRB CTAs, those CTAs form a thread-block cluster and each
+//     token's partial sum of squares goes to the other CTAs through distributed shared memory
+//     (st.async completing on their mbarriers) before every CTA normalises its own rows.
 #include <math.h>
 
 #include <algorithm>
@@ -123,6 +125,10 @@ template <typename TA, int D, int NW> struct TcSmem {
     // B operands [s][t] (k = s, n = t), bf16 hi/lo, rows padded to 24 (conflict-free ldmatrix):
     alignas(16) __nv_bfloat16 thi[2][C::NBLK][kB][kB + 8], tlo[2][C::NBLK][kB][kB + 8];   // (I + N)^-1
     alignas(16) __nv_bfloat16 phi[2][C::NBLK][kB][kB + 8], plo[2][C::NBLK][kB][kB + 8];   // QX'
+    // heads split over a cluster of NRB CTAs: the other CTAs' partial sums of squares of each
+    // token's gated output, per chunk parity and sender, and their arrival
+    alignas(16) float peer_ss[2][C::NRB][kT];
+    alignas(8) uint64_t peer_bar[2];
 };
 
 // Named barriers (0 is __syncthreads): chunk parity b full / empty, and producers only.
@@ -162,7 +168,17 @@ gdn_scan_tc_kernel(const gdn_params p) {
         v_base = (static_cast<int64_t>(b) * S * p.Hv + hv) * D;  v_ts = static_cast<int64_t>(p.Hv) * D;
         g_base = static_cast<int64_t>(b) * S * p.Hv + hv;        g_ts = p.Hv;
     }
-    const bool fused_norm = C::WHOLE_HEAD && p.z != nullptr;
+    // gated RMSNorm in this kernel: over the CTA when it owns the whole head, else over the
+    // cluster of the head's NRB CTAs (partial sums exchanged through distributed shared memory)
+    const bool fused_norm = p.z != nullptr;
+    if (!C::WHOLE_HEAD && fused_norm) {
+        if (threadIdx.x == 0) {
+            mbar_init(&sm.peer_bar[0], 1);
+            mbar_init(&sm.peer_bar[1], 1);
+            mbar_init_fence();
+        }
+        cluster_sync_all();                                // every CTA's barriers initialised
+    }
     if constexpr (C::REG_SPLIT) {
         if (warp < NW) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(C::REG_ROW));
         else asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(C::REG_PROD));
@@ -347,7 +363,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
     const TA *kg = static_cast<const TA *>(p.k) + k_base;
     const TA *qg = static_cast<const TA *>(p.q) + k_base;
     const TA *vg = static_cast<const TA *>(p.v) + v_base + r0;
-    const TA *zg = fused_norm ? static_cast<const TA *>(p.z) + v_base : nullptr;
+    const TA *zg = fused_norm ? static_cast<const TA *>(p.z) + v_base + r0 : nullptr;
 
     // copies of chunk c: raw k, q rows (into the operand ring for bf16, else the staging slot)
     auto issue_kq = [&](int c) {
@@ -381,46 +397,68 @@ gdn_scan_tc_kernel(const gdn_params p) {
         }
     };
 
-    // y of a finished chunk.  Whole head with z: gated RMSNorm, TPT threads per token, each
-    // with FPT float4 column groups interleaved (a quarter-warp reads 128 contiguous bytes).
-    // Otherwise this CTA's raw o rows (the norm kernel follows).
-    constexpr int TPT = (D / 4 < 8) ? D / 4 : 8;           // threads per token (norm)
-    constexpr int FPT = D / (4 * TPT);                     // float4 groups per thread
+    // y of a finished chunk: gated RMSNorm, TPT threads per token, each with FPT float4 column
+    // groups of this CTA's RB columns interleaved (a quarter-warp reads 128 contiguous bytes);
+    // a split head first sends each token's partial sum of squares to the other CTAs of its
+    // cluster and waits for theirs.  Without z: this CTA's raw o rows.
+    constexpr int TPT = (RB / 4 < 8) ? RB / 4 : 8;         // threads per token (norm)
+    constexpr int FPT = RB / (4 * TPT);                    // float4 groups per thread
+    constexpr int NIT = kT * TPT / PT;                     // token passes
     static_assert(PT % TPT == 0 && (kT * TPT) % PT == 0, "norm thread groups");
     float4 gn4[FPT];
 #pragma unroll
     for (int f = 0; f < FPT; f++)
-        gn4[f] = fused_norm ? *reinterpret_cast<const float4 *>(p.gn + 4 * (ptid % TPT + TPT * f))
+        gn4[f] = fused_norm ? *reinterpret_cast<const float4 *>(p.gn + r0 + 4 * (ptid % TPT + TPT * f))
                             : make_float4(0.f, 0.f, 0.f, 0.f);
     const float inv_d = 1.0f / static_cast<float>(D);
     auto emit = [&](int c) {
         const int hb = c & 1, vs = c % C::NVZ;
         const int t0 = c * kT, nt = min(kT, S - t0);
         if (fused_norm) {
+            float4 x[NIT][FPT];
+            float ss[NIT];
+            if (!C::WHOLE_HEAD && ptid == 0)               // this chunk's partner bytes
+                mbar_arrive_expect_tx(&sm.peer_bar[hb], (C::NRB - 1) * kT * 4);
 #pragma unroll
-            for (int it = 0; it < kT * TPT / PT; it++) {
+            for (int it = 0; it < NIT; it++) {
                 const int tt = ptid / TPT + it * (PT / TPT);
-                float4 x[FPT];
-                float ss = 0.f;
+                ss[it] = 0.f;
 #pragma unroll
                 for (int f = 0; f < FPT; f++) {
                     const int col = 4 * (ptid % TPT + TPT * f);
                     const float4 o4 = *reinterpret_cast<const float4 *>(&sm.ob[hb][tt][col]);
                     const float4 z4 = A::four(&sm.zr[vs][tt][col]);
-                    x[f] = make_float4(o4.x * silu_fast(z4.x), o4.y * silu_fast(z4.y),
-                                       o4.z * silu_fast(z4.z), o4.w * silu_fast(z4.w));
-                    ss = fmaf(x[f].x, x[f].x, fmaf(x[f].y, x[f].y, fmaf(x[f].z, x[f].z, fmaf(x[f].w, x[f].w, ss))));
+                    x[it][f] = make_float4(o4.x * silu_fast(z4.x), o4.y * silu_fast(z4.y),
+                                           o4.z * silu_fast(z4.z), o4.w * silu_fast(z4.w));
+                    ss[it] = fmaf(x[it][f].x, x[it][f].x, fmaf(x[it][f].y, x[it][f].y,
+                             fmaf(x[it][f].z, x[it][f].z, fmaf(x[it][f].w, x[it][f].w, ss[it]))));
                 }
-                ss = group_sum<TPT>(ss);
-                const float rr = rsqrtf(fmaf(ss, inv_d, p.norm_eps));
+                ss[it] = group_sum<TPT>(ss[it]);
+                if (!C::WHOLE_HEAD && ptid % TPT == 0) {   // every token, also past the end
+#pragma unroll
+                    for (int pr = 0; pr < C::NRB; pr++)
+                        if (pr != rblk) st_async_peer(&sm.peer_ss[hb][rblk][tt], ss[it], &sm.peer_bar[hb], pr);
+                }
+            }
+            if (!C::WHOLE_HEAD) mbar_wait_bounded(&sm.peer_bar[hb], static_cast<unsigned>((c >> 1) & 1));
+#pragma unroll
+            for (int it = 0; it < NIT; it++) {
+                const int tt = ptid / TPT + it * (PT / TPT);
+                float tot = ss[it];
+                if (!C::WHOLE_HEAD) {
+#pragma unroll
+                    for (int pr = 0; pr < C::NRB; pr++)
+                        if (pr != rblk) tot += sm.peer_ss[hb][pr][tt];
+                }
+                const float rr = rsqrtf(fmaf(tot, inv_d, p.norm_eps));
                 if (tt < nt) {
-                    float *yr = p.y + v_base + (t0 + tt) * v_ts;
+                    float *yr = p.y + v_base + r0 + (t0 + tt) * v_ts;
 #pragma unroll
                     for (int f = 0; f < FPT; f++) {
                         const int col = 4 * (ptid % TPT + TPT * f);
                         *reinterpret_cast<float4 *>(yr + col) =
-                            make_float4(x[f].x * rr * gn4[f].x, x[f].y * rr * gn4[f].y,
-                                        x[f].z * rr * gn4[f].z, x[f].w * rr * gn4[f].w);
+                            make_float4(x[it][f].x * rr * gn4[f].x, x[it][f].y * rr * gn4[f].y,
+                                        x[it][f].z * rr * gn4[f].z, x[it][f].w * rr * gn4[f].w);
                     }
                 }
             }
@@ -681,11 +719,23 @@ cudaError_t launch_tc_cfg(const gdn_params &p, cudaStream_t stream) {
     using C = TcCfg<TA, D, NW>;
     const int bytes = static_cast<int>(sizeof(TcSmem<TA, D, NW>));
     const int64_t ctas = static_cast<int64_t>(p.B) * p.Hv * C::NRB;
-    gdn_scan_tc_kernel<TA, D, NW><<<static_cast<unsigned>(ctas), C::NT, bytes, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (!C::WHOLE_HEAD && p.z != nullptr) {                // a head's CTAs form one cluster
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C::NRB;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gdn_scan_tc_kernel<TA, D, NW>, p);
     if (e != cudaSuccess) return e;
-    if (!C::WHOLE_HEAD && p.z != nullptr) e = launch_gated_norm(p, stream);
-    return e;
+    return cudaGetLastError();
 }
 
 int device_sms() {

@@ -147,6 +147,17 @@ GDN_API const char *gdn_last_error(void);
  */
 GDN_API int gdn_device_status(void *stream);
 
+/*
+ * gdn_selftest_wait_timeout -- exercises the failure path above without a GPU fault: launches
+ * one CTA on `stream` whose mbarrier wait can never complete (the barrier expects 16 bytes
+ * that no copy sends); the wait gives up after `limit_ms` milliseconds, sets the watchdog word
+ * and the CTA returns.  The next gdn_device_status on that device then reports
+ * GDN_ERR_TIMEOUT (and clears it).  Returns GDN_ERR_BAD_ARG unless 0 < limit_ms <= 2000,
+ * GDN_ERR_CUDA on a launch error, GDN_OK otherwise (asynchronous on `stream`).
+ * Source: none on the pages -- a test hook for the bounded waits.
+ */
+GDN_API int gdn_selftest_wait_timeout(void *stream, double limit_ms);
+
 /* gdn_version -- GDN_VERSION of the loaded library. */
 GDN_API int gdn_version(void);
 

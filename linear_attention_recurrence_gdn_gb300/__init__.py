@@ -39,7 +39,7 @@ GDN_ERR_TIMEOUT = -9
 
 # Symbols declared in include/gdn.h (checked by the tests against the header).
 EXPORTED = ("gdn_decode_step", "gdn_scan", "gdn_reject_reason", "gdn_status_string",
-            "gdn_last_error", "gdn_device_status", "gdn_version")
+            "gdn_last_error", "gdn_device_status", "gdn_selftest_wait_timeout", "gdn_version")
 
 
 class GdnParams(ctypes.Structure):
@@ -89,6 +89,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.gdn_last_error.restype = ctypes.c_char_p
     lib.gdn_device_status.argtypes = [ctypes.c_void_p]
     lib.gdn_device_status.restype = ctypes.c_int
+    lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_void_p, ctypes.c_double]
+    lib.gdn_selftest_wait_timeout.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = ctypes.c_int
     if path is None:
@@ -232,6 +234,11 @@ def gdn_last_error() -> str:
 def gdn_device_status(stream=None, device=None) -> int:
     """GDN_OK, or GDN_ERR_TIMEOUT if a kernel abandoned work since the last check."""
     return library().gdn_device_status(_stream_handle(stream, device))
+
+
+def gdn_selftest_wait_timeout(limit_ms: float = 1.0, stream=None, device=None) -> int:
+    """Launch the test hook whose bounded mbarrier wait runs out after ``limit_ms``."""
+    return library().gdn_selftest_wait_timeout(_stream_handle(stream, device), float(limit_ms))
 
 
 def gdn_version() -> int:

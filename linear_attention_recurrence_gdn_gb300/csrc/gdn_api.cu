@@ -196,6 +196,12 @@ int gdn_device_status(void *stream) {
     return flag ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
+int gdn_selftest_wait_timeout(void *stream, double limit_ms) {
+    if (!(limit_ms > 0.0 && limit_ms <= 2000.0)) return GDN_ERR_BAD_ARG;
+    const uint64_t ns = static_cast<uint64_t>(limit_ms * 1e6);
+    return cuda_status(gdn::launch_wait_timeout(static_cast<cudaStream_t>(stream), ns));
+}
+
 int gdn_version(void) { return GDN_VERSION; }
 
 }  // extern "C"

@@ -409,6 +409,26 @@ cudaError_t launch_decode(const gdn_params &p, cudaStream_t stream) {
     }
 }
 
+namespace {
+// A wait that cannot complete: the barrier's one arrival comes with 16 expected bytes and no
+// copy ever sends them, so the bounded wait runs out, sets the watchdog word and returns.
+__global__ void gdn_wait_timeout_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+        mbar_arrive_expect_tx(&bar, 16);
+    }
+    __syncthreads();
+    mbar_wait_bounded(&bar, 0, limit_ns);
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout(cudaStream_t stream, uint64_t limit_ns) {
+    gdn_wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t decode_watchdog(unsigned *flag, cudaStream_t stream) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_watchdog, sizeof(unsigned), 0,
                                               cudaMemcpyDeviceToHost, stream);

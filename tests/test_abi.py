@@ -214,3 +214,9 @@ def test_binding_shape_and_dtype_checks():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no fallback"):
         gdn.library(str(tmp_path / "libgdn.so"))
+
+
+def test_selftest_wait_timeout_rejects_bad_limits_without_a_gpu(lib):
+    # argument checks run before any CUDA call
+    for bad in (0.0, -1.0, 2000.5, float("nan")):
+        assert lib.gdn_selftest_wait_timeout(None, bad) == -7   # GDN_ERR_BAD_ARG

@@ -139,10 +139,12 @@ GDN_API const char *gdn_last_error(void);
 
 /*
  * gdn_device_status -- waits for `stream`, then reports whether a kernel of this library,
- * since the last call on this device, abandoned its work because a wait for its own bulk
- * copies into shared memory exceeded its time limit (about 2 s; never expected on a healthy
- * GPU).  Returns GDN_ERR_TIMEOUT then (the outputs of that call are incomplete) and clears
- * the condition; GDN_OK otherwise; GDN_ERR_CUDA if the runtime reports an error.
+ * since the last call on this device, gave up a wait on an mbarrier after its time limit
+ * (about 2 s; never expected on a healthy GPU): the decode kernel's wait for its own bulk
+ * copies (it then abandons its work), or the scan's wait for the partial norm sums of the
+ * other CTAs of its cluster (it then carries on with what it has).  Returns GDN_ERR_TIMEOUT
+ * then (the outputs of that call are incomplete or invalid) and clears the condition; GDN_OK
+ * otherwise; GDN_ERR_CUDA if the runtime reports an error.
  * Source: none on the pages -- failure detection for the asynchronous-copy waits.
  */
 GDN_API int gdn_device_status(void *stream);

@@ -190,10 +190,13 @@ const char *gdn_status_string(int status) {
 const char *gdn_last_error(void) { return g_last_error; }
 
 int gdn_device_status(void *stream) {
-    unsigned flag = 0;
-    const int st = cuda_status(gdn::decode_watchdog(&flag, static_cast<cudaStream_t>(stream)));
+    unsigned flag_decode = 0, flag_scan = 0;
+    const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+    int st = cuda_status(gdn::decode_watchdog(&flag_decode, st_));
     if (st != GDN_OK) return st;
-    return flag ? GDN_ERR_TIMEOUT : GDN_OK;
+    st = cuda_status(gdn::scan_watchdog(&flag_scan, st_));
+    if (st != GDN_OK) return st;
+    return (flag_decode | flag_scan) ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
 int gdn_selftest_wait_timeout(void *stream, double limit_ms) {

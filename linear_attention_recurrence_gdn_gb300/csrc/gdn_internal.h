@@ -23,4 +23,7 @@ cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
 // The scan on tensor cores (gdn_scan_tc.cu).
 cudaError_t launch_scan_tc(const gdn_params &p, cudaStream_t stream);
 
+// Reads and clears the scan kernels' watchdog word (synchronises `stream`).
+cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream);
+
 }  // namespace gdn

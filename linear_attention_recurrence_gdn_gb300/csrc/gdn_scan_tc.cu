@@ -797,6 +797,18 @@ cudaError_t launch_tc_dim(const gdn_params &p, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_watchdog, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+    const unsigned zero = 0;
+    if (*flag) e = cudaMemcpyToSymbolAsync(g_watchdog, &zero, sizeof(unsigned), 0,
+                                           cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    return e;
+}
+
 cudaError_t launch_scan_tc(const gdn_params &p, cudaStream_t stream) {
     switch (p.act_dtype) {
         case GDN_F32: return launch_tc_dim<float>(p, stream);

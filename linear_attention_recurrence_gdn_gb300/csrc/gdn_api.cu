@@ -64,7 +64,6 @@ int check(const gdn_params *p, int is_decode, const char **why) {
         *why = "Dk and Dv must be 16, 32, 64 or 128";
         return GDN_ERR_UNSUPPORTED_DIM;
     }
-    if (p->Dk != p->Dv) { *why = "Dk != Dv is not supported"; return GDN_ERR_UNSUPPORTED_DIM; }
     const int64_t eact = dtype_bytes(p->act_dtype);
     if (eact == 0) { *why = "act_dtype must be GDN_F32, GDN_BF16 or GDN_F16"; return GDN_ERR_BAD_DTYPE; }
     if (p->gate_dtype != GDN_F32 && p->gate_dtype != p->act_dtype) {
@@ -176,7 +175,7 @@ const char *gdn_status_string(int status) {
         case GDN_OK: return "ok";
         case GDN_ERR_NULL_PTR: return "a required pointer is NULL (or only one of z, gn given)";
         case GDN_ERR_BAD_SHAPE: return "bad shape (dims, Hv % Hk, or S != 1 on decode)";
-        case GDN_ERR_UNSUPPORTED_DIM: return "unsupported head dim (Dk = Dv in {16, 32, 64, 128})";
+        case GDN_ERR_UNSUPPORTED_DIM: return "unsupported head dim (Dk, Dv in {16, 32, 64, 128})";
         case GDN_ERR_BAD_DTYPE: return "bad dtype";
         case GDN_ERR_MISALIGNED: return "misaligned pointer";
         case GDN_ERR_ALIASING: return "output overlaps an operand";

@@ -344,11 +344,11 @@ struct LaunchSlots {
     int slots[kMaxDevices] = {};   // resident CTAs on the whole device; 0 = not computed
 };
 
-template <typename TA, int D>
+template <typename TA, int DK, int DV>
 cudaError_t launch_typed(const gdn_params &p, cudaStream_t stream) {
-    using C = DecodeCfg<TA, D, D>;
+    using C = DecodeCfg<TA, DK, DV>;
     static LaunchSlots cache;
-    auto kern = gdn_decode_kernel<TA, D, D>;
+    auto kern = gdn_decode_kernel<TA, DK, DV>;
     const int bytes = static_cast<int>(C::BYTES);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -387,13 +387,24 @@ cudaError_t launch_typed(const gdn_params &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <typename TA, int DK>
+cudaError_t launch_dv(const gdn_params &p, cudaStream_t stream) {
+    switch (p.Dv) {
+        case 16: return launch_typed<TA, DK, 16>(p, stream);
+        case 32: return launch_typed<TA, DK, 32>(p, stream);
+        case 64: return launch_typed<TA, DK, 64>(p, stream);
+        case 128: return launch_typed<TA, DK, 128>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename TA>
 cudaError_t launch_dim(const gdn_params &p, cudaStream_t stream) {
     switch (p.Dk) {
-        case 16: return launch_typed<TA, 16>(p, stream);
-        case 32: return launch_typed<TA, 32>(p, stream);
-        case 64: return launch_typed<TA, 64>(p, stream);
-        case 128: return launch_typed<TA, 128>(p, stream);
+        case 16: return launch_dv<TA, 16>(p, stream);
+        case 32: return launch_dv<TA, 32>(p, stream);
+        case 64: return launch_dv<TA, 64>(p, stream);
+        case 128: return launch_dv<TA, 128>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

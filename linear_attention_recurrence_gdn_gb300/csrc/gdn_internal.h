@@ -20,10 +20,18 @@ cudaError_t launch_wait_timeout(cudaStream_t stream, uint64_t limit_ns);
 // Multi-token scan (S >= 1): state resident on chip across the time axis.
 cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
 
-// The scan on tensor cores (gdn_scan_tc.cu).
-cudaError_t launch_scan_tc(const gdn_params &p, cudaStream_t stream);
+// The scan on tensor cores, one translation unit per key head dim (gdn_scan_tc_dk*.cu), and
+// each unit's watchdog word (read and cleared; synchronises `stream`).
+cudaError_t launch_scan_tc_dk16(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk32(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk64(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk128(const gdn_params &p, cudaStream_t stream);
+cudaError_t scan_watchdog_dk16(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_watchdog_dk32(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_watchdog_dk64(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_watchdog_dk128(unsigned *flag, cudaStream_t stream);
 
-// Reads and clears the scan kernels' watchdog word (synchronises `stream`).
+// Reads and clears the scan kernels' watchdog words (synchronises `stream`).
 cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream);
 
 }  // namespace gdn

@@ -1,4 +1,6 @@
-// gdn_scan_tc.cu -- multi-token GDN recurrence on tensor cores, memory resident in registers.
+// gdn_scan_tc.cuh -- multi-token GDN recurrence on tensor cores, memory resident in registers.
+// Kernel and launchers as templates over the activation type, Dk, Dv and the rows per CTA;
+// gdn_scan_tc_dk{16,32,64,128}.cu instantiate one key head dim each (parallel compilation).
 //
 // What is computed is the page's per-token recurrence (logicaffeine_compile::codegen_cuda::gdn,
 // module description; time loop of torch_to_nnef.op.gated_delta, gated_delta_reference), not
@@ -40,7 +42,10 @@
 //     head's rows are split over NRB CTAs, those CTAs form a thread-block cluster and each
 //     token's partial sum of squares goes to the other CTAs through distributed shared memory
 //     (st.async completing on their mbarriers) before every CTA normalises its own rows.
+#pragma once
+
 #include <math.h>
+#include <stdint.h>
 
 #include <algorithm>
 
@@ -60,10 +65,10 @@ constexpr float kMinLogDecay = -80.0f;     // exp(-80) ~ 1.8e-35: a full reset f
 template <typename TA> struct IsBf16 { static constexpr bool value = false; };
 template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
 
-template <typename TA, int D, int NW> struct TcCfg {
+template <typename TA, int DK, int DV, int NW> struct TcCfg {
     static constexpr bool EXACT = IsBf16<TA>::value;  // raw rows are exact bf16 operands
     static constexpr int RB = 16 * NW;               // rows per CTA (NW row warps)
-    static constexpr int NRB = D / RB;               // CTAs per head
+    static constexpr int NRB = DV / RB;              // CTAs per head
     static constexpr int NP = (NW == 8) ? 8 : 4;     // producer warps
     static constexpr int PT = 32 * NP;               // producer threads
     static constexpr int NT = 32 * (NW + NP);
@@ -75,19 +80,19 @@ template <typename TA, int D, int NW> struct TcCfg {
                                  NW % 4 == 0 && NP % 4 == 0),
                   "register split within the launch's registers, whole warpgroups");
     static constexpr bool SPLIT_KQ = (NP == 8);      // norm pass: k on 4 warps, q on the others
-    static constexpr int NTILE = D / 8;              // n-tiles of a warp's 16 x D memory block
-    static constexpr int KST = D / 16;               // k-steps over D
+    static constexpr int NTILE = DK / 8;             // n-tiles of a warp's 16 x Dk memory block
+    static constexpr int KST = DK / 16;              // k-steps over Dk
     static constexpr int NBLK = kT / kB;
     static constexpr int PADE = 16 / (int)sizeof(TA);  // 16 bytes of row padding, in elements
     static constexpr int LDV = RB + PADE;            // raw v / z rows
     static constexpr int LDO = RB + 4;               // o rows (f32)
     static constexpr int NOP = EXACT ? 3 : 2;        // operand ring depth
     static constexpr int NVZ = 3;                    // v / z ring depth
-    static constexpr bool WHOLE_HEAD = (RB == D);
-    static constexpr int KPIECES = D * (int)sizeof(TA) / 16;     // 16-byte pieces of a k row
+    static constexpr bool WHOLE_HEAD = (RB == DV);
+    static constexpr int KPIECES = DK * (int)sizeof(TA) / 16;    // 16-byte pieces of a k row
     static constexpr int VPIECES = RB * (int)sizeof(TA) / 16;    // ... of this CTA's v rows
     static constexpr int TPK = KPIECES < 4 ? KPIECES : 4;        // norm-pass threads per token
-    static_assert(D % RB == 0 && D % 16 == 0, "shape");
+    static_assert(DV % RB == 0 && DK % 16 == 0 && DV % 16 == 0, "shape");
     static_assert(KPIECES >= 1 && VPIECES >= 1, "16-byte copy granularity");
     static_assert(KPIECES % TPK == 0 && (SPLIT_KQ ? PT / 2 : PT) / TPK >= kT,
                   "norm pass covers a chunk at once");
@@ -109,9 +114,9 @@ template <typename TA, int D> struct TcOps<TA, D, false> {
 // Shared memory; every member 16-byte aligned (vector accesses, ldmatrix rows, cp.async).
 // Slots are indexed by chunk: operands c % NOP, v / z c % 3, and everything else the row warps
 // read (o, per-token scalars, tables) c % 2.
-template <typename TA, int D, int NW> struct TcSmem {
-    using C = TcCfg<TA, D, NW>;
-    alignas(16) TcOps<TA, D, C::EXACT> op;
+template <typename TA, int DK, int DV, int NW> struct TcSmem {
+    using C = TcCfg<TA, DK, DV, NW>;
+    alignas(16) TcOps<TA, DK, C::EXACT> op;
     alignas(16) TA vr[C::NVZ][kT][C::LDV];       // raw v rows of this CTA
     alignas(16) TA zr[C::NVZ][kT][C::LDV];       // raw z (whole-head CTAs with z)
     alignas(16) float ob[2][kT][C::LDO];         // o of the chunk, written by the row warps
@@ -135,12 +140,12 @@ template <typename TA, int D, int NW> struct TcSmem {
 enum { kBarFull0 = 1, kBarEmpty0 = 3, kBarProd = 5 };
 
 
-template <typename TA, int D, int NW>
-__global__ void __launch_bounds__(TcCfg<TA, D, NW>::NT, 1)
+template <typename TA, int DK, int DV, int NW>
+__global__ void __launch_bounds__(TcCfg<TA, DK, DV, NW>::NT, 1)
 gdn_scan_tc_kernel(const gdn_params p) {
-    using C = TcCfg<TA, D, NW>;
+    using C = TcCfg<TA, DK, DV, NW>;
     using A = Act<TA>;
-    using Sm = TcSmem<TA, D, NW>;
+    using Sm = TcSmem<TA, DK, DV, NW>;
     constexpr int RB = C::RB, NTILE = C::NTILE, KST = C::KST, NP = C::NP, NT = C::NT, PT = C::PT;
     constexpr bool EXACT = C::EXACT;
 
@@ -160,12 +165,12 @@ gdn_scan_tc_kernel(const gdn_params p) {
 
     int64_t k_base, k_ts, v_base, v_ts, g_base, g_ts;
     if (p.head_major) {
-        k_base = (static_cast<int64_t>(b) * p.Hk + hk) * S * D;  k_ts = D;
-        v_base = head * S * D;                                   v_ts = D;
+        k_base = (static_cast<int64_t>(b) * p.Hk + hk) * S * DK;  k_ts = DK;
+        v_base = head * S * DV;                                   v_ts = DV;
         g_base = head * S;                                       g_ts = 1;
     } else {
-        k_base = (static_cast<int64_t>(b) * S * p.Hk + hk) * D;  k_ts = static_cast<int64_t>(p.Hk) * D;
-        v_base = (static_cast<int64_t>(b) * S * p.Hv + hv) * D;  v_ts = static_cast<int64_t>(p.Hv) * D;
+        k_base = (static_cast<int64_t>(b) * S * p.Hk + hk) * DK;  k_ts = static_cast<int64_t>(p.Hk) * DK;
+        v_base = (static_cast<int64_t>(b) * S * p.Hv + hv) * DV;  v_ts = static_cast<int64_t>(p.Hv) * DV;
         g_base = static_cast<int64_t>(b) * S * p.Hv + hv;        g_ts = p.Hv;
     }
     // gated RMSNorm in this kernel: over the CTA when it owns the whole head, else over the
@@ -192,13 +197,13 @@ gdn_scan_tc_kernel(const gdn_params p) {
         // sacc[j] = S[wrow+g][8j+2tq], S[wrow+g][8j+2tq+1], S[wrow+g+8][8j+2tq], S[..+8][..+1]
         float sacc[NTILE][4];
         {
-            const float *s0 = p.s0 ? p.s0 + head * (D * D) + static_cast<int64_t>(r0 + wrow) * D : nullptr;
+            const float *s0 = p.s0 ? p.s0 + head * (DV * DK) + static_cast<int64_t>(r0 + wrow) * DK : nullptr;
 #pragma unroll
             for (int j = 0; j < NTILE; j++) {
                 float2 lo = make_float2(0.f, 0.f), hi = lo;
                 if (s0) {
-                    lo = *reinterpret_cast<const float2 *>(s0 + g * D + 8 * j + 2 * tq);
-                    hi = *reinterpret_cast<const float2 *>(s0 + (g + 8) * D + 8 * j + 2 * tq);
+                    lo = *reinterpret_cast<const float2 *>(s0 + g * DK + 8 * j + 2 * tq);
+                    hi = *reinterpret_cast<const float2 *>(s0 + (g + 8) * DK + 8 * j + 2 * tq);
                 }
                 sacc[j][0] = lo.x; sacc[j][1] = lo.y; sacc[j][2] = hi.x; sacc[j][3] = hi.y;
             }
@@ -346,12 +351,12 @@ gdn_scan_tc_kernel(const gdn_params p) {
             bar_arrive(kBarEmpty0 + hb, NT);               // slots of chunk ch handed back
         }
         // final memory rows (undo the deferred decay)
-        float *so = p.state + head * (D * D) + static_cast<int64_t>(r0 + wrow) * D;
+        float *so = p.state + head * (DV * DK) + static_cast<int64_t>(r0 + wrow) * DK;
 #pragma unroll
         for (int j = 0; j < NTILE; j++) {
-            *reinterpret_cast<float2 *>(so + g * D + 8 * j + 2 * tq) =
+            *reinterpret_cast<float2 *>(so + g * DK + 8 * j + 2 * tq) =
                 make_float2(lam * sacc[j][0], lam * sacc[j][1]);
-            *reinterpret_cast<float2 *>(so + (g + 8) * D + 8 * j + 2 * tq) =
+            *reinterpret_cast<float2 *>(so + (g + 8) * DK + 8 * j + 2 * tq) =
                 make_float2(lam * sacc[j][2], lam * sacc[j][3]);
         }
         return;
@@ -410,7 +415,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
     for (int f = 0; f < FPT; f++)
         gn4[f] = fused_norm ? *reinterpret_cast<const float4 *>(p.gn + r0 + 4 * (ptid % TPT + TPT * f))
                             : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float inv_d = 1.0f / static_cast<float>(D);
+    const float inv_d = 1.0f / static_cast<float>(DV);
     auto emit = [&](int c) {
         const int hb = c & 1, vs = c % C::NVZ;
         const int t0 = c * kT, nt = min(kT, S - t0);
@@ -508,7 +513,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
     issue_vz(0);
     issue_kq(0);
     cp_async_commit();
-    const float inv_sqrt_dk = rsqrtf(static_cast<float>(D));
+    const float inv_sqrt_dk = rsqrtf(static_cast<float>(DK));
     // norm-pass roles: token nt_tok, pieces nq, nq + TPK, ...; a quarter-warp of 8 lanes
     // covers 8 tokens (conflict-free 16-byte accesses on the padded rows)
     constexpr int TPW = 32 / C::TPK;                       // tokens per warp in the norm pass
@@ -697,11 +702,11 @@ gdn_scan_tc_kernel(const gdn_params p) {
 
 // Occupancy of one variant; a variant whose shared memory exceeds the per-CTA limit of this
 // device reports 0 (the caller then uses a variant with fewer rows per CTA).
-template <typename TA, int D, int NW>
+template <typename TA, int DK, int DV, int NW>
 cudaError_t prepare_tc(int *occupancy) {
-    using C = TcCfg<TA, D, NW>;
-    auto kern = gdn_scan_tc_kernel<TA, D, NW>;
-    const int bytes = static_cast<int>(sizeof(TcSmem<TA, D, NW>));
+    using C = TcCfg<TA, DK, DV, NW>;
+    auto kern = gdn_scan_tc_kernel<TA, DK, DV, NW>;
+    const int bytes = static_cast<int>(sizeof(TcSmem<TA, DK, DV, NW>));
     *occupancy = 0;
     int dev = 0, limit = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -714,10 +719,10 @@ cudaError_t prepare_tc(int *occupancy) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, C::NT, bytes);
 }
 
-template <typename TA, int D, int NW>
+template <typename TA, int DK, int DV, int NW>
 cudaError_t launch_tc_cfg(const gdn_params &p, cudaStream_t stream) {
-    using C = TcCfg<TA, D, NW>;
-    const int bytes = static_cast<int>(sizeof(TcSmem<TA, D, NW>));
+    using C = TcCfg<TA, DK, DV, NW>;
+    const int bytes = static_cast<int>(sizeof(TcSmem<TA, DK, DV, NW>));
     const int64_t ctas = static_cast<int64_t>(p.B) * p.Hv * C::NRB;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
@@ -733,29 +738,29 @@ cudaError_t launch_tc_cfg(const gdn_params &p, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gdn_scan_tc_kernel<TA, D, NW>, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gdn_scan_tc_kernel<TA, DK, DV, NW>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-int device_sms() {
+inline int device_sms() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return n;
 }
 
-// Rows per CTA for D = 128: the fewest warps on the busiest SM with every CTA resident at
+// Rows per CTA for Dv = 128: the fewest warps on the busiest SM with every CTA resident at
 // once (a sequential scan must not run in waves); ties go to the larger CTA.
-template <typename TA>
-cudaError_t launch_tc_128(const gdn_params &p, cudaStream_t stream) {
+template <typename TA, int DK>
+cudaError_t launch_tc_dv128(const gdn_params &p, cudaStream_t stream) {
     const int sms = std::max(1, device_sms());
     const int64_t heads = static_cast<int64_t>(p.B) * p.Hv;
     int occ[3] = {0, 0, 0};
     cudaError_t e;
-    if ((e = prepare_tc<TA, 128, 8>(&occ[0])) != cudaSuccess) return e;
-    if ((e = prepare_tc<TA, 128, 4>(&occ[1])) != cudaSuccess) return e;
-    if ((e = prepare_tc<TA, 128, 2>(&occ[2])) != cudaSuccess) return e;
+    if ((e = prepare_tc<TA, DK, 128, 8>(&occ[0])) != cudaSuccess) return e;
+    if ((e = prepare_tc<TA, DK, 128, 4>(&occ[1])) != cudaSuccess) return e;
+    if ((e = prepare_tc<TA, DK, 128, 2>(&occ[2])) != cudaSuccess) return e;
     const int nws[3] = {8, 4, 2};
     int best = -1;
     int64_t best_cost = INT64_MAX;
@@ -769,35 +774,47 @@ cudaError_t launch_tc_128(const gdn_params &p, cudaStream_t stream) {
     }
     if (best < 0) return cudaErrorInvalidConfiguration;
     switch (nws[best]) {
-        case 8: return launch_tc_cfg<TA, 128, 8>(p, stream);
-        case 4: return launch_tc_cfg<TA, 128, 4>(p, stream);
-        default: return launch_tc_cfg<TA, 128, 2>(p, stream);
+        case 8: return launch_tc_cfg<TA, DK, 128, 8>(p, stream);
+        case 4: return launch_tc_cfg<TA, DK, 128, 4>(p, stream);
+        default: return launch_tc_cfg<TA, DK, 128, 2>(p, stream);
     }
 }
 
-template <typename TA, int D>
+// Dv < 128: one CTA per head, Dv / 16 row warps.
+template <typename TA, int DK, int DV>
 cudaError_t launch_tc_small(const gdn_params &p, cudaStream_t stream) {
     int occ = 0;
-    cudaError_t e = prepare_tc<TA, D, D / 16>(&occ);
+    cudaError_t e = prepare_tc<TA, DK, DV, DV / 16>(&occ);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
-    return launch_tc_cfg<TA, D, D / 16>(p, stream);
+    return launch_tc_cfg<TA, DK, DV, DV / 16>(p, stream);
 }
 
-template <typename TA>
-cudaError_t launch_tc_dim(const gdn_params &p, cudaStream_t stream) {
-    switch (p.Dk) {
-        case 16: return launch_tc_small<TA, 16>(p, stream);
-        case 32: return launch_tc_small<TA, 32>(p, stream);
-        case 64: return launch_tc_small<TA, 64>(p, stream);
-        case 128: return launch_tc_128<TA>(p, stream);
+template <typename TA, int DK>
+cudaError_t launch_tc_dv(const gdn_params &p, cudaStream_t stream) {
+    switch (p.Dv) {
+        case 16: return launch_tc_small<TA, DK, 16>(p, stream);
+        case 32: return launch_tc_small<TA, DK, 32>(p, stream);
+        case 64: return launch_tc_small<TA, DK, 64>(p, stream);
+        case 128: return launch_tc_dv128<TA, DK>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-}  // namespace
+// Every activation type and value head dim for one key head dim.
+template <int DK>
+cudaError_t launch_tc_dk(const gdn_params &p, cudaStream_t stream) {
+    switch (p.act_dtype) {
+        case GDN_F32: return launch_tc_dv<float, DK>(p, stream);
+        case GDN_BF16: return launch_tc_dv<__nv_bfloat16, DK>(p, stream);
+        case GDN_F16: return launch_tc_dv<__half, DK>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
-cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {
+// This translation unit's watchdog word (set by a cluster-exchange wait that ran out): read
+// and clear (synchronises `stream`).
+inline cudaError_t read_watchdog(unsigned *flag, cudaStream_t stream) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_watchdog, sizeof(unsigned), 0,
                                               cudaMemcpyDeviceToHost, stream);
     if (e != cudaSuccess) return e;
@@ -809,13 +826,5 @@ cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {
     return e;
 }
 
-cudaError_t launch_scan_tc(const gdn_params &p, cudaStream_t stream) {
-    switch (p.act_dtype) {
-        case GDN_F32: return launch_tc_dim<float>(p, stream);
-        case GDN_BF16: return launch_tc_dim<__nv_bfloat16>(p, stream);
-        case GDN_F16: return launch_tc_dim<__half>(p, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
+}  // namespace
 }  // namespace gdn

@@ -17,8 +17,8 @@ CPUS = os.cpu_count() or 1
 
 
 def small_workload(B=1, S=4, Hk=1, Hv=2, D=16, act="f32", head_major=False, s0_std=0.1,
-                   seed=5, ldr=(-3.0, 0.0)) -> Workload:
-    return TINY.replace(name="case", B=B, S=S, Hk=Hk, Hv=Hv, Dk=D, Dv=D, act=act,
+                   seed=5, ldr=(-3.0, 0.0), Dk=None, Dv=None) -> Workload:
+    return TINY.replace(name="case", B=B, S=S, Hk=Hk, Hv=Hv, Dk=Dk or D, Dv=Dv or D, act=act,
                         head_major=head_major, s0_std=s0_std, seed=seed,
                         log_decay_range=ldr)
 

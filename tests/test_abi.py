@@ -110,6 +110,10 @@ def test_valid_params_have_no_reject_reason(lib):
                                    beta=None), 0) is None
     for d in (16, 32, 128):
         assert reject(lib, fake_params(Dk=d, Dv=d), 0) is None
+    # separate key and value head dims
+    for dk, dv in ((64, 128), (128, 32), (16, 64)):
+        assert reject(lib, fake_params(Dk=dk, Dv=dv), 0) is None
+        assert reject(lib, fake_params(Dk=dk, Dv=dv, S=1), 1) is None
 
 
 REJECTIONS = [
@@ -122,7 +126,7 @@ REJECTIONS = [
     (dict(S=0), 1, gdn.GDN_ERR_BAD_SHAPE, "S == 1"),
     (dict(Dk=48, Dv=48), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "16, 32, 64 or 128"),
     (dict(Dk=256, Dv=256), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "16, 32, 64 or 128"),
-    (dict(Dk=64, Dv=128), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "Dk != Dv"),
+    (dict(Dk=64, Dv=96), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "16, 32, 64 or 128"),
     (dict(act_dtype=7), 0, gdn.GDN_ERR_BAD_DTYPE, "act_dtype"),
     (dict(act_dtype=gdn.GDN_BF16, gate_dtype=gdn.GDN_F16), 0, gdn.GDN_ERR_BAD_DTYPE, "gate_dtype"),
     (dict(qk_eps=-1.0), 0, gdn.GDN_ERR_BAD_ARG, "eps"),

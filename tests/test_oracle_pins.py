@@ -33,8 +33,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def small(B=1, S=3, Hk=1, Hv=1, D=4, *, head_major=False, s0_std=0.1, seed=7,
-          ldr=(-3.0, 0.0), act="f32"):
-    w = TINY.replace(name="small", B=B, S=S, Hk=Hk, Hv=Hv, Dk=D, Dv=D, head_major=head_major,
+          ldr=(-3.0, 0.0), act="f32", Dk=None, Dv=None):
+    w = TINY.replace(name="small", B=B, S=S, Hk=Hk, Hv=Hv, Dk=Dk or D, Dv=Dv or D,
+                     head_major=head_major,
                      s0_std=s0_std, seed=seed, log_decay_range=ldr, act=act)
     inp = {k: (None if v is None else v.double()) for k, v in make_inputs(w).items()}
     return w, inp
@@ -87,6 +88,31 @@ def test_oracle_matches_decimal_closed_form(case, mode):
         inp["beta"].numpy(), z=inp["z"].numpy() if gated else None,
         gn=inp["gn"].numpy() if gated else None,
         s0=None if inp["s0"] is None else inp["s0"].numpy(), head_major=hm)
+    assert rel_err(y, yd) <= 1e-12
+    assert rel_err(st, sd) <= 1e-12
+
+
+# separate key and value head dims: a transposed index anywhere (state rows vs columns, the
+# norm's axis, q / k vs v / z strides) fails these
+RECT_CASES = [
+    # B, S, Hk, Hv, Dk, Dv, head_major, gated, seed
+    (1, 4, 1, 2, 3, 5, False, True, 31),
+    (2, 3, 1, 2, 6, 2, True, True, 32),
+    (1, 5, 2, 4, 4, 7, False, False, 33),
+]
+
+
+@pytest.mark.parametrize("case", RECT_CASES, ids=lambda c: "x".join(map(str, c[:6])))
+@pytest.mark.parametrize("mode", ["literal", "fused"])
+def test_oracle_matches_decimal_closed_form_rectangular_heads(case, mode):
+    B, S, Hk, Hv, Dk, Dv, hm, gated, seed = case
+    _, inp = small(B, S, Hk, Hv, head_major=hm, seed=seed, Dk=Dk, Dv=Dv)
+    y, st = orun(inp, gated=gated, head_major=hm, mode=mode)
+    assert st.shape == (B, Hv, Dv, Dk)
+    yd, sd = closed_form_decimal.run(
+        inp["q"].numpy(), inp["k"].numpy(), inp["v"].numpy(), inp["log_decay"].numpy(),
+        inp["beta"].numpy(), z=inp["z"].numpy() if gated else None,
+        gn=inp["gn"].numpy() if gated else None, s0=inp["s0"].numpy(), head_major=hm)
     assert rel_err(y, yd) <= 1e-12
     assert rel_err(st, sd) <= 1e-12
 

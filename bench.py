@@ -444,8 +444,9 @@ def main(argv=None):
     ap.add_argument("--no-scan", action="store_true", help="skip the supplementary scans")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "decode", "scan"], default="all",
-                    help="decode: skip the scans; scan: time only the scans (profiling runs)")
+    ap.add_argument("--only", choices=["all", "decode", "scan", "rect"], default="all",
+                    help="decode: skip the scans; scan: time only the scans (profiling runs); "
+                         "rect: time the separate-key/value-head-dim workloads")
     ap.add_argument("--scan-S", type=int, default=0,
                     help="override the scan workloads' sequence length (profiling runs)")
     args = ap.parse_args(argv)
@@ -476,6 +477,20 @@ def main(argv=None):
                           peaks["sm_max_mhz"], peaks) for x in scan_workloads]
         if rank == 0:
             print(json.dumps({"scan": out}), flush=True)
+        return 0
+    if args.only == "rect":
+        # the headline workloads with Dk != Dv (same heads, same token counts)
+        rd = DECODE_B64.replace(name="decode_bf16_b64_hk16_hv32_dk128_dv64", Dv=64)
+        dec = bench_decode(gdn, rd, dev, args.steps, args.warmup, world, None)
+        gbs = decode_bytes(rd) / (dec["ms_per_step"] * 1e-3) / 1e9
+        rs = PREFILL_B4.replace(name="prefill_bf16_b4_s4096_hk16_hv32_dk64_dv128", Dk=64)
+        scan = bench_scan(gdn, rs, dev, args.scan_reps, props.multi_processor_count,
+                          peaks["sm_max_mhz"], peaks)
+        if rank == 0:
+            print(json.dumps({"rect": [
+                {"config": rd.as_config(), "metric": "decode state HBM GB/s", "value": gbs,
+                 "ms_per_step": dec["ms_per_step"], "frac_of_measured_hbm": gbs / peaks["hbm_gbs"]},
+                scan]}), flush=True)
         return 0
 
     sampler = ClockSampler(device_uuid(dev)) if rank == 0 else None

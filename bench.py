@@ -74,6 +74,25 @@ def scan_mma_flops(w: Workload) -> int:
     return (w.B * w.Hv * warps_per_head * per_warp_block * 2 * 16 * 8 * 16 * w.S) // 16
 
 
+def scan_tmem_mma_flops(w: Workload) -> int:
+    """Tensor-core FLOPs the tensor-memory chunked kernel issues per launch (M = 128 MMAs).
+
+    Per head and 32-token chunk c of n: the chunk tables (8 MMAs with N = 32, 16 from the
+    second chunk on, when the cross table with the previous chunk's keys is added), [x | y]
+    from S' hi / lo (16, N = 64), d = R T (6, N = 32), O (6, N = 32), the update (4, N = 128)
+    and the next chunk's correction (6, N = 64, all chunks but the last).  Each M x N x 16 MMA
+    is 2 * 128 * N * 16 FLOP; rows the tables compute beyond the 64 real ones are counted too.
+    """
+    n = (w.S + 31) // 32
+    per = 2 * 128 * 16
+    tables = (8 + 16 * (n - 1)) * 32
+    pre = 16 * n * 64
+    d_o = 12 * n * 32
+    upd = 4 * n * 128
+    corr = 6 * (n - 1) * 64
+    return w.B * w.Hv * per * (tables + pre + d_o + upd + corr)
+
+
 def scan_bytes(w: Workload) -> int:
     e = w.elem_bytes
     s0 = 4 * w.B * w.Hv * w.Dv * w.Dk if w.s0_std is not None else 0
@@ -316,7 +335,8 @@ def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
 
 # ------------------------------------------------------------------------------ scan
 
-def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks: dict):
+def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks: dict,
+               tmem: bool = False):
     inp = make_inputs(w)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     y = torch.empty(d["v"].shape, dtype=torch.float32, device=dev)
@@ -324,7 +344,7 @@ def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks:
 
     def run():
         gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, y, s0=d["s0"],
-                     z=d["z"], gn=d["gn"], head_major=w.head_major)
+                     z=d["z"], gn=d["gn"], head_major=w.head_major, tmem=tmem)
 
     run()
     torch.cuda.synchronize(dev)
@@ -344,6 +364,21 @@ def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks:
     mma = scan_mma_flops(w) / secs / 1e12
     mma_sync_peak = sms * MMA_SYNC_MAC_PER_CLK_SM * 2 * sm_mhz * 1e6 / 1e12
     bf16 = peaks["bf16_tflops"]
+    if tmem:
+        tc = scan_tmem_mma_flops(w) / secs / 1e12
+        cfg = dict(w.as_config(), kernel="tensor-memory chunked (GDN_FLAG_SCAN_TMEM)")
+        return {"config": cfg, "value": w.B * w.S / secs, "unit": "tokens/s", "ms": ms,
+                "reps": reps,
+                "roofline": {"bound": "tensor", "achieved": tc, "peak": bf16, "unit": "TFLOP/s",
+                             "frac": tc / bf16, "traffic": None,
+                             "peak_note": f"{peaks['source']} cuBLAS bf16 dense; this kernel "
+                                          f"issues tcgen05 MMAs (M = 128, N = 32..128)",
+                             "work": "tensor-core FLOPs of the chunked kernel's tcgen05 MMAs "
+                                     "(tables, [x | y], d, O, update, correction; hi/lo terms "
+                                     "counted)"},
+                "fp32_equivalent": {"achieved": fp32_eq, "peak": fp32_peak, "unit": "TFLOP/s",
+                                    "frac": fp32_eq / fp32_peak},
+                "hbm_bytes": scan_bytes(w)}
     return {"config": w.as_config(), "value": w.B * w.S / secs, "unit": "tokens/s",
             "ms": ms, "reps": reps,
             "roofline": {"bound": "tensor", "achieved": mma, "peak": bf16, "unit": "TFLOP/s",
@@ -475,6 +510,8 @@ def main(argv=None):
     if args.only == "scan":
         out = [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
                           peaks["sm_max_mhz"], peaks) for x in scan_workloads]
+        out.append(bench_scan(gdn, scan_workloads[0], dev, args.scan_reps,
+                              props.multi_processor_count, peaks["sm_max_mhz"], peaks, tmem=True))
         if rank == 0:
             print(json.dumps({"scan": out}), flush=True)
         return 0
@@ -509,6 +546,8 @@ def main(argv=None):
         scan = {"metric": "gdn_scan tokens/sec", "note": "supplementary, not the headline",
                 "workloads": [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
                                          sm_mhz, peaks) for x in scan_workloads]}
+        scan["workloads"].append(bench_scan(gdn, scan_workloads[0], dev, args.scan_reps,
+                                            props.multi_processor_count, sm_mhz, peaks, tmem=True))
     if sampler:
         sampler.stop()
 

@@ -77,6 +77,14 @@ typedef enum {
     GDN_ERR_TIMEOUT = -9          /* a kernel gave up waiting for its own async copies       */
 } gdn_status;
 
+/* Option bits of gdn_params.flags.
+ *   GDN_FLAG_SCAN_TMEM  gdn_scan only (gdn_decode_step rejects it): run the chunked kernel that
+ *                       keeps each head's memory in tensor memory and does every product on
+ *                       tcgen05 MMAs, where it applies (bf16 activations, Dk == Dv == 128);
+ *                       other shapes run the default kernel.  Same results within the scan
+ *                       tolerance; the default kernel is faster on the reference workloads. */
+#define GDN_FLAG_SCAN_TMEM 1
+
 /* Operands of one call.  Shape fields follow GDNShape (num_key_heads = Hk, num_value_heads
  * = Hv, key_head_dim = Dk, value_head_dim = Dv) plus batch B and sequence length S. */
 typedef struct gdn_params {
@@ -84,7 +92,7 @@ typedef struct gdn_params {
     int32_t head_major;       /* 0: [B,S,H,W] / [B,S,H] operands; 1: [B,H,S,W] / [B,H,S]     */
     int32_t act_dtype;        /* gdn_dtype of q, k, v, z                                      */
     int32_t gate_dtype;       /* gdn_dtype of log_decay and beta: GDN_F32 or act_dtype        */
-    int32_t reserved;         /* must be 0                                                    */
+    int32_t flags;            /* GDN_FLAG_* bits (0 = defaults); unknown bits are rejected    */
     const void *q, *k;        /* [B,S,Hk,Dk] / [B,Hk,S,Dk]                                    */
     const void *v;            /* [B,S,Hv,Dv] / [B,Hv,S,Dv]                                    */
     const void *log_decay;    /* [B,S,Hv] / [B,Hv,S]                                          */

@@ -24,6 +24,7 @@ from . import build as _build
 LIBRARY = _build.LIBRARY
 
 GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
+GDN_FLAG_SCAN_TMEM = 1          # gdn_params.flags: tensor-memory chunked scan where it applies
 _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
 
 GDN_OK = 0
@@ -48,7 +49,7 @@ class GdnParams(ctypes.Structure):
         ("B", ctypes.c_int32), ("S", ctypes.c_int32), ("Hk", ctypes.c_int32),
         ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32), ("Dv", ctypes.c_int32),
         ("head_major", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
-        ("gate_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("gate_dtype", ctypes.c_int32), ("flags", ctypes.c_int32),
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
         ("log_decay", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("z", ctypes.c_void_p),
         ("gn", ctypes.c_void_p), ("s0", ctypes.c_void_p),
@@ -103,7 +104,7 @@ def _ptr(t) -> int | None:
 
 
 def make_params(q, k, v, log_decay, beta, state, y, *, z=None, gn=None, s0=None,
-                head_major=False, qk_eps=1e-6, norm_eps=1e-6) -> GdnParams:
+                head_major=False, qk_eps=1e-6, norm_eps=1e-6, flags=0) -> GdnParams:
     """Fill a :class:`GdnParams` from tensors (shapes read per ``head_major``).
 
     Tensors must be contiguous; nothing is copied or converted here.
@@ -149,7 +150,7 @@ def make_params(q, k, v, log_decay, beta, state, y, *, z=None, gn=None, s0=None,
         if t is not None and t.dtype != torch.float32:
             raise GdnError(GDN_ERR_BAD_DTYPE, f"{name} must be float32")
     return GdnParams(B=B, S=S, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, head_major=int(bool(head_major)),
-                     act_dtype=act, gate_dtype=gate, reserved=0,
+                     act_dtype=act, gate_dtype=gate, flags=int(flags),
                      q=_ptr(q), k=_ptr(k), v=_ptr(v), log_decay=_ptr(log_decay),
                      beta=_ptr(beta), z=_ptr(z), gn=_ptr(gn), s0=_ptr(s0),
                      state=_ptr(state), y=_ptr(y), qk_eps=qk_eps, norm_eps=norm_eps)
@@ -194,10 +195,11 @@ def gdn_decode_step(q, k, v, log_decay, beta, state, y=None, *, z=None, gn=None,
 
 
 def gdn_scan(q, k, v, log_decay, beta, state=None, y=None, *, s0=None, z=None, gn=None,
-             head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None):
+             head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None, tmem=False):
     """The recurrence over the time axis from ``s0`` (None = zeros).
 
-    Returns ``(y, state)``; ``state`` may be ``s0`` itself (in-place resume).
+    Returns ``(y, state)``; ``state`` may be ``s0`` itself (in-place resume).  ``tmem=True``
+    sets GDN_FLAG_SCAN_TMEM (the tensor-memory chunked kernel where it applies).
     """
     _require_cuda(q, k, v, log_decay, beta, state, y, z, gn, s0)
     if head_major:
@@ -211,7 +213,8 @@ def gdn_scan(q, k, v, log_decay, beta, state=None, y=None, *, s0=None, z=None, g
     if state is None:
         state = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=v.device)
     prm = make_params(q, k, v, log_decay, beta, state, y, z=z, gn=gn, s0=s0,
-                      head_major=head_major, qk_eps=qk_eps, norm_eps=norm_eps)
+                      head_major=head_major, qk_eps=qk_eps, norm_eps=norm_eps,
+                      flags=GDN_FLAG_SCAN_TMEM if tmem else 0)
     lib = library()
     st = lib.gdn_scan(ctypes.byref(prm), _stream_handle(stream, v.device))
     _raise(lib, st, prm, 0)

@@ -47,7 +47,11 @@ bool supported_dim(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 int check(const gdn_params *p, int is_decode, const char **why) {
     *why = nullptr;
     if (p == nullptr) { *why = "params pointer is NULL"; return GDN_ERR_NULL_PTR; }
-    if (p->reserved != 0) { *why = "reserved field must be 0"; return GDN_ERR_BAD_ARG; }
+    if ((p->flags & ~GDN_FLAG_SCAN_TMEM) != 0) { *why = "unknown flags bit"; return GDN_ERR_BAD_ARG; }
+    if (is_decode && p->flags != 0) {
+        *why = "flags: GDN_FLAG_SCAN_TMEM applies to gdn_scan only";
+        return GDN_ERR_BAD_ARG;
+    }
     if (p->B < 0 || p->S < 0) { *why = "B and S must be >= 0"; return GDN_ERR_BAD_SHAPE; }
     if (p->Hk < 1 || p->Hv < 1) { *why = "Hk and Hv must be >= 1"; return GDN_ERR_BAD_SHAPE; }
     if (p->Hv % p->Hk != 0) {
@@ -179,7 +183,7 @@ const char *gdn_status_string(int status) {
         case GDN_ERR_BAD_DTYPE: return "bad dtype";
         case GDN_ERR_MISALIGNED: return "misaligned pointer";
         case GDN_ERR_ALIASING: return "output overlaps an operand";
-        case GDN_ERR_BAD_ARG: return "bad argument (eps, flag, reserved field or size)";
+        case GDN_ERR_BAD_ARG: return "bad argument (eps, flag, flags bits or size)";
         case GDN_ERR_CUDA: return "CUDA error (see gdn_last_error)";
         case GDN_ERR_TIMEOUT: return "a kernel timed out waiting for its own copies";
         default: return "unknown status";

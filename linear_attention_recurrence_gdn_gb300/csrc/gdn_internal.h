@@ -31,6 +31,12 @@ cudaError_t scan_watchdog_dk32(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk64(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk128(unsigned *flag, cudaStream_t stream);
 
+// The chunked scan with the memory in tensor memory (bf16, Dk = Dv = 128, 16-byte aligned
+// operands; chosen by GDN_FLAG_SCAN_TMEM), and its watchdog word.
+bool scan_umma_supported(const gdn_params &p);
+cudaError_t launch_scan_umma(const gdn_params &p, cudaStream_t stream);
+cudaError_t scan_umma_watchdog(unsigned *flag, cudaStream_t stream);
+
 // Reads and clears the scan kernels' watchdog words (synchronises `stream`).
 cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream);
 

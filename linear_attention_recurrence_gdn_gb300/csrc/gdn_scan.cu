@@ -10,6 +10,7 @@
 namespace gdn {
 
 cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
+    if ((p.flags & GDN_FLAG_SCAN_TMEM) && scan_umma_supported(p)) return launch_scan_umma(p, stream);
     switch (p.Dk) {
         case 16: return launch_scan_tc_dk16(p, stream);
         case 32: return launch_scan_tc_dk32(p, stream);
@@ -20,13 +21,14 @@ cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
 }
 
 cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {
-    unsigned f[4] = {0, 0, 0, 0};
+    unsigned f[5] = {0, 0, 0, 0, 0};
     cudaError_t e;
     if ((e = scan_watchdog_dk16(&f[0], stream)) != cudaSuccess) return e;
     if ((e = scan_watchdog_dk32(&f[1], stream)) != cudaSuccess) return e;
     if ((e = scan_watchdog_dk64(&f[2], stream)) != cudaSuccess) return e;
     if ((e = scan_watchdog_dk128(&f[3], stream)) != cudaSuccess) return e;
-    *flag = f[0] | f[1] | f[2] | f[3];
+    if ((e = scan_umma_watchdog(&f[4], stream)) != cudaSuccess) return e;
+    *flag = f[0] | f[1] | f[2] | f[3] | f[4];
     return cudaSuccess;
 }
 

@@ -78,7 +78,7 @@ GAP = 1 << 32
 def fake_params(**kw):
     """A launchable parameter set on fake pointers (B, S, Hk, Hv, D = 2, 3, 2, 4, 64)."""
     p = dict(B=2, S=3, Hk=2, Hv=4, Dk=64, Dv=64, head_major=0, act_dtype=gdn.GDN_BF16,
-             gate_dtype=gdn.GDN_F32, reserved=0, qk_eps=1e-6, norm_eps=1e-6)
+             gate_dtype=gdn.GDN_F32, flags=0, qk_eps=1e-6, norm_eps=1e-6)
     names = ["q", "k", "v", "log_decay", "beta", "z", "gn", "s0", "state", "y"]
     for i, n in enumerate(names):
         p[n] = BASE + i * GAP
@@ -133,7 +133,8 @@ REJECTIONS = [
     (dict(norm_eps=float("nan")), 0, gdn.GDN_ERR_BAD_ARG, "eps"),
     (dict(norm_eps=float("inf")), 0, gdn.GDN_ERR_BAD_ARG, "eps"),
     (dict(head_major=2), 0, gdn.GDN_ERR_BAD_ARG, "head_major"),
-    (dict(reserved=1), 0, gdn.GDN_ERR_BAD_ARG, "reserved"),
+    (dict(flags=2), 0, gdn.GDN_ERR_BAD_ARG, "unknown flags"),
+    (dict(S=1, flags=gdn.GDN_FLAG_SCAN_TMEM), 1, gdn.GDN_ERR_BAD_ARG, "gdn_scan only"),
     (dict(B=1 << 20, S=1 << 20), 0, gdn.GDN_ERR_BAD_ARG, "too large"),
     (dict(state=None), 0, gdn.GDN_ERR_NULL_PTR, "state and y"),
     (dict(S=1, y=None), 1, gdn.GDN_ERR_NULL_PTR, "state and y"),

@@ -68,6 +68,10 @@ def test_roofline_byte_and_flop_models():
     assert bench.scan_flops(PREFILL_B4) == 6 * 128 * 128 * 4 * 4096 * 32
     # bf16 block form: per warp and 16-token block 64 (X, Y) + 12 (d, O) + 32 (update) MMAs
     assert bench.scan_mma_flops(PREFILL_B4) == 4 * 32 * 8 * 108 * 4096 * 4096 // 16
+    # tensor-memory chunked kernel: per head and steady chunk 16x32 (tables) + 16x64 ([x|y])
+    # + 12x32 (d, O) + 4x128 (update) + 6x64 (correction) = 2816 columns of 128x16 MMAs;
+    # the first chunk has no cross table (8x32 fewer), the last no correction (6x64 fewer)
+    assert bench.scan_tmem_mma_flops(PREFILL_B4) == 128 * (2 * 128 * 16) * (2816 * 128 - 640)
 
 
 def test_reference_arm_prints_one_line(capsys):

@@ -106,27 +106,31 @@ struct alignas(1024) U3Smem {
     alignas(16) float ob[2][uC][uD + 4];          // o of a chunk (row warps -> staging warps)
     alignas(16) float cb[2][uC], cx[2][uC], cy[2][uC], cw[2][uC];  // per-token row constants
     alignas(16) float gam[2][4];                  // e^{cum_31} of the chunk
-    alignas(16) float4 gts[uC];                   // beta, e^{cum_t}, e^{cum_31 - cum_t}
-    alignas(16) float cum[uC];
-    alignas(16) float gamp[4];
-    alignas(16) float rk[uC], rq[uC], cumk[uC];
+    alignas(16) float4 gts[2][uC];                // beta, e^{cum_t}, e^{cum_31 - cum_t} (by chunk parity)
+    alignas(16) float cum[2][uC];
+    alignas(16) float gamp[2][4];                 // e^{cum_31}, reference m, factored-exp flag
+    alignas(16) float rk[uC], rq[uC], cumk[uC], fk[uC];
     alignas(16) float nT[uC][uNM];                // nT[t][s] = N[s][t]
+    alignas(16) float tT[uC][20];                 // column t of the diagonal block of T holding t
+    alignas(16) float tR[16][20];                 // T[0:16][0:16] row-major
     alignas(8) uint64_t bar_load[uSlots];         // a slot's copies landed
     alignas(8) uint64_t bar_tab, bar_d, bar_o, bar_pre;   // MMA groups completed
     alignas(8) uint64_t bar_g[2];                 // correction operand written (64 arrivals)
+    alignas(8) uint64_t bar_gates[2];             // decay products of a chunk written (32)
     uint32_t tmem_base;
 };
 static_assert(sizeof(U3Smem) + 1024 <= 227 * 1024, "shared memory");
 
 // Named barriers.  FULL: row warps sync, table + staging warps arrive (chunk operands ready).
-// EMPTY: row warps arrive, staging warps sync (o rows of a chunk written).  GATES / NORMS:
-// staging arrive, table warps sync (NORMS also means the row warps are done with chunk ch-1, so
-// its per-chunk buffers may be rewritten).  TDONE: table warps arrive, staging sync (table
-// warps done with the previous chunk's shared buffers).  TBAR: rk from table warp 0 to table
-// warp 1.  TLD: both table warps have read the chunk tables out of tensor memory, so table
-// warp 0 may issue the next chunk's table MMAs into the same columns.
+// EMPTY: row warps arrive, staging warps sync (o rows of a chunk written).  NORMS: staging
+// arrive, table warps sync (the q norms are written, and the row warps are done with chunk
+// ch-2, so its per-chunk buffers may be rewritten).  TDONE: table warps arrive, staging sync
+// (table warps done with the previous chunk's shared buffers).  TBAR: rk and the factored
+// exponentials from table warp 0 to table warp 1; TBAR2: the diagonal blocks of T likewise.
+// TLD: both table warps have read the chunk tables out of tensor memory, so table warp 1 may
+// issue the next chunk's table MMAs into the same columns.
 enum {
-    uBarFull0 = 1, uBarEmpty0 = 3, uBarRow = 5, uBarStg = 6, uBarGates = 7, uBarNorms = 8,
+    uBarFull0 = 1, uBarEmpty0 = 3, uBarRow = 5, uBarStg = 6, uBarT2 = 7, uBarNorms = 8,
     uBarTdone = 9, uBarT = 10, uBarTld = 11
 };
 
@@ -157,6 +161,8 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         mbar_init(&sm.bar_pre, 1);
         mbar_init(&sm.bar_g[0], 64);
         mbar_init(&sm.bar_g[1], 64);
+        mbar_init(&sm.bar_gates[0], 32);
+        mbar_init(&sm.bar_gates[1], 32);
         mbar_init_fence();
     }
     __syncwarp();
@@ -453,7 +459,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             tc_fence_before();
             bar_sync(uBarTld, 64);                         // both table warps hold the tables
             if (ch + 1 < nchunks) {                        // the next chunk's tables, early
-                issue(uTabW0, [&] {
+                issue(uTabW0 + 1, [&] {
                     tc_fence_after();
                     mbar_wait_bounded(&sm.bar_load[ch % uSlots], load_parity(ch));
                     mbar_wait_bounded(&sm.bar_load[(ch + 1) % uSlots], load_parity(ch + 1));
@@ -475,11 +481,12 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.bar_g[hb]);
             }
-            bar_sync(uBarGates, 64 + uST);                 // decay products of chunk ch
-            const float4 gt = sm.gts[t];                   // beta, e^cum, e^{cum_31 - cum}
-            const float cum_t = sm.cum[t];
-            char *dst_hi, *dst_lo;
-            float col[uC];
+            mbar_wait_bounded(&sm.bar_gates[hb], static_cast<unsigned>((ch >> 1) & 1));
+            __syncwarp();
+            const float4 gt = sm.gts[hb][t];               // beta, e^cum, e^{cum_31 - cum}
+            const float cum_t = sm.cum[hb][t];
+            const float mref = sm.gamp[hb][1];
+            const bool factored = sm.gamp[hb][2] != 0.f;   // e^{cum_t - m}, e^{m - cum_s} finite
             if (tq == 0) {
                 // rk from the diagonal of K K^T
                 float dg = 0.f;
@@ -488,19 +495,36 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 const float rk_t = (t < nt) ? rsqrtf(dg + p.qk_eps) : 0.f;
                 sm.rk[t] = rk_t;
                 sm.cumk[t] = cum_t;
+                sm.fk[t] = factored ? rk_t * __expf(mref - cum_t) : 0.f;
                 __syncwarp();
+                bar_arrive(uBarT, 64);                     // rk, fk ready for the q-row warp
                 // N column t: N[s][t] = beta_t e^{cum_t - cum_s} rk_s rk_t (k_s . k_t), s < t
-                const float bt = gt.x * rk_t;
+                float col[uC];
+                if (factored) {
+                    const float g = gt.x * rk_t * __expf(cum_t - mref);
 #pragma unroll
-                for (int s4 = 0; s4 < uC / 4; s4++) {
-                    const float4 r4 = *reinterpret_cast<const float4 *>(&sm.rk[4 * s4]);
-                    const float4 c4 = *reinterpret_cast<const float4 *>(&sm.cumk[4 * s4]);
-                    const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, cc[4] = {c4.x, c4.y, c4.z, c4.w};
+                    for (int s4 = 0; s4 < uC / 4; s4++) {
+                        const float4 f4 = *reinterpret_cast<const float4 *>(&sm.fk[4 * s4]);
+                        const float ff[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int s = 4 * s4 + e;
-                        const float m = (s < t) ? bt : 0.f;  // exp argument <= 0: finite
-                        col[s] = m * __expf(fminf(cum_t - cc[e], 0.f)) * rr[e] * tab[32 + s];
+                        for (int e = 0; e < 4; e++) {
+                            const int s_ = 4 * s4 + e;
+                            col[s_] = ((s_ < t) ? g : 0.f) * ff[e] * tab[32 + s_];
+                        }
+                    }
+                } else {
+                    const float bt = gt.x * rk_t;
+#pragma unroll
+                    for (int s4 = 0; s4 < uC / 4; s4++) {
+                        const float4 r4 = *reinterpret_cast<const float4 *>(&sm.rk[4 * s4]);
+                        const float4 c4 = *reinterpret_cast<const float4 *>(&sm.cumk[4 * s4]);
+                        const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const int s_ = 4 * s4 + e;
+                            const float m = (s_ < t) ? bt : 0.f;   // exp argument <= 0: finite
+                            col[s_] = m * __expf(fminf(cum_t - cc[e], 0.f)) * rr[e] * tab[32 + s_];
+                        }
                     }
                 }
 #pragma unroll
@@ -508,62 +532,159 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                     *reinterpret_cast<float4 *>(&sm.nT[t][4 * s4]) =
                         make_float4(col[4 * s4], col[4 * s4 + 1], col[4 * s4 + 2], col[4 * s4 + 3]);
                 __syncwarp();
-                bar_arrive(uBarT, 64);                     // rk ready for the q-row warp
-                // T = (I + N)^-1, column t by back substitution:
-                // T[r][t] = -sum_{r < r' <= t} N[r][r'] T[r'][t]
-                float acc[uC];
+                // The diagonal 16 x 16 blocks of T = (I + N)^-1 (block upper triangular: T11 =
+                // (I + N11)^-1, T22 = (I + N22)^-1, T12 = -T11 N12 T22).  Lane t solves column t
+                // of its block by back substitution, T[r][t] = -sum_{r < r' <= t} N[r][r'] T[r'][t].
+                const int base = t & 16, tl = t & 15;
+                float acc[16], colb[16];
 #pragma unroll
-                for (int s = 0; s < uC; s++) acc[s] = 0.f;
+                for (int j = 0; j < 16; j++) acc[j] = 0.f;
 #pragma unroll
-                for (int r = uC - 1; r >= 0; r--) {
-                    const float tr = (r == t) ? 1.f : ((r < t) ? -acc[r] : 0.f);
-                    col[r] = tr;
-                    if (r > 0) {
+                for (int rr = 15; rr >= 0; rr--) {
+                    const float tr = (rr == tl) ? 1.f : ((rr < tl) ? -acc[rr] : 0.f);
+                    colb[rr] = tr;
+                    if (rr > 0) {
+                        const float *nrow = &sm.nT[base + rr][base];
 #pragma unroll
-                        for (int s4 = 0; s4 < (r + 3) / 4; s4++) {
-                            const float4 n4 = *reinterpret_cast<const float4 *>(&sm.nT[r][4 * s4]);
+                        for (int s4 = 0; s4 < (rr + 3) / 4; s4++) {
+                            const float4 n4 = *reinterpret_cast<const float4 *>(nrow + 4 * s4);
                             const float nn[4] = {n4.x, n4.y, n4.z, n4.w};
 #pragma unroll
                             for (int e = 0; e < 4; e++)
-                                if (4 * s4 + e < r) acc[4 * s4 + e] = fmaf(nn[e], tr, acc[4 * s4 + e]);
+                                if (4 * s4 + e < rr) acc[4 * s4 + e] = fmaf(nn[e], tr, acc[4 * s4 + e]);
                         }
                     }
                 }
-                bar_sync(uBarNorms, 64 + uST);             // row warps done with chunk ch-1
-                dst_hi = reinterpret_cast<char *>(&sm.thi[hb][0]);
-                dst_lo = reinterpret_cast<char *>(&sm.tlo[hb][0]);
+#pragma unroll
+                for (int j4 = 0; j4 < 4; j4++)
+                    *reinterpret_cast<float4 *>(&sm.tT[t][4 * j4]) =
+                        make_float4(colb[4 * j4], colb[4 * j4 + 1], colb[4 * j4 + 2], colb[4 * j4 + 3]);
+                if (t < 16) {
+#pragma unroll
+                    for (int j = 0; j < 16; j++) sm.tR[j][t] = colb[j];
+                }
+                __syncwarp();
+                bar_arrive(uBarT2, 64);                    // diagonal blocks ready
+                bar_sync(uBarNorms, 64 + uST);             // row warps done with chunk ch-2
+                // column t of T as B [s][t]: rows of the lane's diagonal block; zeros below
+                // the diagonal block for t < 16 (rows 16-31 of T11's columns)
+                char *dh = reinterpret_cast<char *>(&sm.thi[hb][0]);
+                char *dl = reinterpret_cast<char *>(&sm.tlo[hb][0]);
+#pragma unroll
+                for (int kk = 0; kk < 2; kk++) {
+                    uint32_t h4[4], l4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) split2(colb[8 * kk + 2 * i], colb[8 * kk + 2 * i + 1], h4[i], l4[i]);
+                    const int kg = (base >> 3) + kk;
+                    *reinterpret_cast<uint4 *>(dh + core_run(t, kg)) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+                    *reinterpret_cast<uint4 *>(dl + core_run(t, kg)) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+                }
+                if (t < 16) {
+#pragma unroll
+                    for (int kg = 2; kg < 4; kg++) {
+                        *reinterpret_cast<uint4 *>(dh + core_run(t, kg)) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(dl + core_run(t, kg)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
             } else {
                 bar_sync(uBarNorms, 64 + uST);             // rq of chunk ch
-                bar_sync(uBarT, 64);                       // rk of chunk ch
+                bar_sync(uBarT, 64);                       // rk, fk of chunk ch
                 const float rq_t = sm.rq[t], rk_own = sm.rk[t];
                 // QX' column t: e^{cum_t - cum_s} rk_s rq_t (k_s . q_t), s <= t
+                float col[uC];
+                if (factored) {
+                    const float h = rq_t * __expf(cum_t - mref);
 #pragma unroll
-                for (int s4 = 0; s4 < uC / 4; s4++) {
-                    const float4 r4 = *reinterpret_cast<const float4 *>(&sm.rk[4 * s4]);
-                    const float4 c4 = *reinterpret_cast<const float4 *>(&sm.cumk[4 * s4]);
-                    const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, cc[4] = {c4.x, c4.y, c4.z, c4.w};
+                    for (int s4 = 0; s4 < uC / 4; s4++) {
+                        const float4 f4 = *reinterpret_cast<const float4 *>(&sm.fk[4 * s4]);
+                        const float ff[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int s = 4 * s4 + e;
-                        const float m = (s <= t) ? rq_t : 0.f;
-                        col[s] = m * __expf(fminf(cum_t - cc[e], 0.f)) * rr[e] * tab[32 + s];
+                        for (int e = 0; e < 4; e++) {
+                            const int s_ = 4 * s4 + e;
+                            col[s_] = ((s_ <= t) ? h : 0.f) * ff[e] * tab[32 + s_];
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int s4 = 0; s4 < uC / 4; s4++) {
+                        const float4 r4 = *reinterpret_cast<const float4 *>(&sm.rk[4 * s4]);
+                        const float4 c4 = *reinterpret_cast<const float4 *>(&sm.cumk[4 * s4]);
+                        const float rr[4] = {r4.x, r4.y, r4.z, r4.w}, cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const int s_ = 4 * s4 + e;
+                            const float m = (s_ <= t) ? rq_t : 0.f;
+                            col[s_] = m * __expf(fminf(cum_t - cc[e], 0.f)) * rr[e] * tab[32 + s_];
+                        }
                     }
                 }
                 sm.cb[hb][t] = gt.x;
                 sm.cx[hb][t] = gt.y * rk_own;
                 sm.cy[hb][t] = gt.y * rq_t;
                 sm.cw[hb][t] = gt.z * rk_own;
-                if (t == 0) sm.gam[hb][0] = sm.gamp[0];
-                dst_hi = reinterpret_cast<char *>(&sm.phi[hb][0]);
-                dst_lo = reinterpret_cast<char *>(&sm.plo[hb][0]);
-            }
+                if (t == 0) sm.gam[hb][0] = sm.gamp[hb][0];
+                char *ph_ = reinterpret_cast<char *>(&sm.phi[hb][0]);
+                char *pl_ = reinterpret_cast<char *>(&sm.plo[hb][0]);
 #pragma unroll
-            for (int kg = 0; kg < 4; kg++) {               // column t as B [s][t], hi / lo
+                for (int kg = 0; kg < 4; kg++) {           // column t as B [s][t], hi / lo
+                    uint32_t h4[4], l4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) split2(col[8 * kg + 2 * i], col[8 * kg + 2 * i + 1], h4[i], l4[i]);
+                    *reinterpret_cast<uint4 *>(ph_ + core_run(t, kg)) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+                    *reinterpret_cast<uint4 *>(pl_ + core_run(t, kg)) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+                }
+                // T12 = -T11 N12 T22: lane -> column tc = 16 + (lane & 15), rows 8 hf .. 8 hf + 7
+                bar_sync(uBarT2, 64);
+                const int tc = 16 + (t & 15), hf = t >> 4;
+                float u[16];                               // u = N12 T22[:, tc]
+#pragma unroll
+                for (int e = 0; e < 8; e++) u[e] = 0.f;
+#pragma unroll
+                for (int j4 = 0; j4 < 4; j4++) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(&sm.tT[tc][4 * j4]);
+                    const float tj[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                    for (int jj = 0; jj < 4; jj++) {
+                        const float *nrow = &sm.nT[16 + 4 * j4 + jj][8 * hf];
+                        const float4 a4 = *reinterpret_cast<const float4 *>(nrow);
+                        const float4 b4 = *reinterpret_cast<const float4 *>(nrow + 4);
+                        const float nn[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                        for (int e = 0; e < 8; e++) u[e] = fmaf(nn[e], tj[jj], u[e]);
+                    }
+                }
+                // u[0:8] holds rows 8 hf .. 8 hf + 7; the partner lane (t ^ 16) holds the others
+                float uo[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) uo[e] = __shfl_xor_sync(0xffffffffu, u[e], 16);
+                float uf[16];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    uf[e] = hf ? uo[e] : u[e];
+                    uf[8 + e] = hf ? u[e] : uo[e];
+                }
+                float t12[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int srow = 8 * hf + e;
+                    float a = 0.f;
+#pragma unroll
+                    for (int r4 = 0; r4 < 4; r4++) {
+                        const float4 w4 = *reinterpret_cast<const float4 *>(&sm.tR[srow][4 * r4]);
+                        a = fmaf(w4.x, uf[4 * r4], a);
+                        a = fmaf(w4.y, uf[4 * r4 + 1], a);
+                        a = fmaf(w4.z, uf[4 * r4 + 2], a);
+                        a = fmaf(w4.w, uf[4 * r4 + 3], a);
+                    }
+                    t12[e] = -a;
+                }
                 uint32_t h4[4], l4[4];
 #pragma unroll
-                for (int i = 0; i < 4; i++) split2(col[8 * kg + 2 * i], col[8 * kg + 2 * i + 1], h4[i], l4[i]);
-                *reinterpret_cast<uint4 *>(dst_hi + core_run(t, kg)) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
-                *reinterpret_cast<uint4 *>(dst_lo + core_run(t, kg)) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+                for (int i = 0; i < 4; i++) split2(t12[2 * i], t12[2 * i + 1], h4[i], l4[i]);
+                *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(&sm.thi[hb][0]) + core_run(tc, hf)) =
+                    make_uint4(h4[0], h4[1], h4[2], h4[3]);
+                *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(&sm.tlo[hb][0]) + core_run(tc, hf)) =
+                    make_uint4(l4[0], l4[1], l4[2], l4[3]);
             }
             fence_proxy_async_smem();                      // operands for the tensor core
             if (ch + 1 < nchunks) bar_arrive(uBarTdone, 64 + uST);
@@ -655,7 +776,11 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             gbv = load_gate(p.beta, p.gate_dtype, gi);
         }
     };
+    // Written into the buffer of the chunk's parity, announced on bar_gates[parity]; also the
+    // reference m = mid-range of cum and whether every e^{+-(cum - m)} stays finite (range <= 120),
+    // so the table warps may factor e^{cum_t - cum_s} = e^{cum_t - m} e^{m - cum_s}.
     auto decay_products = [&](int c) {
+        const int gb = c & 1;
         const bool valid = c * uC + lane < S;
         const float gc = valid ? fmaxf(gl, uMinLogDecay) : 0.f;
         float upto = gc;                                   // chunk-inclusive prefix sum
@@ -665,13 +790,29 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             if (lane >= off) upto += o;
         }
         const float total = __shfl_sync(0xffffffffu, upto, 31);
-        sm.gts[lane] = make_float4(valid ? gbv : 0.f, expf(upto), expf(total - upto), 0.f);
-        sm.cum[lane] = upto;
-        if (lane == 0) sm.gamp[0] = expf(total);
+        float hi = upto, lo = upto;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+        }
+        sm.gts[gb][lane] = make_float4(valid ? gbv : 0.f, expf(upto), expf(total - upto), 0.f);
+        sm.cum[gb][lane] = upto;
+        if (lane == 0) {
+            sm.gamp[gb][0] = expf(total);
+            sm.gamp[gb][1] = 0.5f * (hi + lo);
+            sm.gamp[gb][2] = (hi - lo <= 120.f) ? 1.f : 0.f;
+        }
+        __syncwarp();
+        mbar_arrive(&sm.bar_gates[gb]);
     };
 
     const float inv_sqrt_dk = rsqrtf(static_cast<float>(D));
-    if (sw == uGateW) load_gates(0);
+    if (sw == uGateW) {                                    // chunk 0's decay products
+        load_gates(0);
+        decay_products(0);
+        if (nchunks > 1) load_gates(1);
+    }
     if (stid == 0) {
         issue_chunk(0);
         if (nchunks > 1) issue_chunk(1);
@@ -680,11 +821,10 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         const int hb = ch & 1, slot = ch % uSlots;
         const int nt = min(uC, S - ch * uC);
         if (ch > 0) bar_sync(uBarTdone, 64 + uST);         // table warps done with chunk ch-1
-        if (sw == uGateW) {
-            decay_products(ch);
-            if (ch + 1 < nchunks) load_gates(ch + 1);
+        if (sw == uGateW && ch + 1 < nchunks) {            // one chunk ahead: the buffer of
+            decay_products(ch + 1);                        // parity ch+1 was last read in ch-1
+            if (ch + 2 < nchunks) load_gates(ch + 2);
         }
-        bar_arrive(uBarGates, 64 + uST);
         if (ch >= 2) {                                     // chunk ch-2's o rows are written
             bar_sync(uBarEmpty0 + hb, uRT + uST);
             emit(ch - 2);

@@ -720,29 +720,29 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         if (gated) tma_load_4d(&sm.z[slot][0][0], &mz, 0, hv, t0, b, bar);
     };
 
-    // y of a finished chunk: 4 lanes per token (8 tokens per warp pass), lane part q holds
-    // the float4 column groups q + 4 i; gated RMSNorm or the raw o rows
-    const int eq = lane & 3;
-    float4 gn4[8];
+    // y of a finished chunk: 8 lanes per token (4 tokens per warp pass), lane part q holds
+    // the float4 column groups q + 8 i; gated RMSNorm or the raw o rows
+    const int eq = lane & 7;
+    float4 gn4[4];
 #pragma unroll
-    for (int i = 0; i < 8; i++)
-        gn4[i] = gated ? *reinterpret_cast<const float4 *>(p.gn + 4 * (eq + 4 * i))
+    for (int i = 0; i < 4; i++)
+        gn4[i] = gated ? *reinterpret_cast<const float4 *>(p.gn + 4 * (eq + 8 * i))
                        : make_float4(0.f, 0.f, 0.f, 0.f);
     const float inv_d = 1.0f / static_cast<float>(D);
     auto emit = [&](int c) {
         const int hb = c & 1, slot = c % uSlots;
         const int t0 = c * uC, nt = min(uC, S - t0);
-        for (int base = 8 * sw; base < nt; base += 8 * uStgW) {
-            const int tt = base + (lane >> 2);
+        for (int base = 4 * sw; base < nt; base += 4 * uStgW) {
+            const int tt = base + (lane >> 3);
             const bool valid = tt < nt;
             const int tr = valid ? tt : base;              // rows past the end: any valid row
             float4 *yr = reinterpret_cast<float4 *>(p.y + v_base + (t0 + tr) * v_ts);
             if (gated) {
-                float4 x[8];
+                float4 x[4];
                 float ss = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    const int c4 = eq + 4 * i;
+                for (int i = 0; i < 4; i++) {
+                    const int c4 = eq + 8 * i;
                     const float4 o4 = *reinterpret_cast<const float4 *>(&sm.ob[hb][tr][4 * c4]);
                     const float4 z4 = A::four(&sm.z[slot][tr][4 * c4]);
                     x[i] = make_float4(o4.x * silu_fast(z4.x), o4.y * silu_fast(z4.y),
@@ -751,17 +751,18 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 }
                 ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                 ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 4);
                 const float rr = rsqrtf(fmaf(ss, inv_d, p.norm_eps));
                 if (valid) {
 #pragma unroll
-                    for (int i = 0; i < 8; i++)
-                        yr[eq + 4 * i] = make_float4(x[i].x * rr * gn4[i].x, x[i].y * rr * gn4[i].y,
+                    for (int i = 0; i < 4; i++)
+                        yr[eq + 8 * i] = make_float4(x[i].x * rr * gn4[i].x, x[i].y * rr * gn4[i].y,
                                                      x[i].z * rr * gn4[i].z, x[i].w * rr * gn4[i].w);
                 }
             } else if (valid) {
 #pragma unroll
-                for (int i = 0; i < 8; i++)
-                    yr[eq + 4 * i] = *reinterpret_cast<const float4 *>(&sm.ob[hb][tr][4 * (eq + 4 * i)]);
+                for (int i = 0; i < 4; i++)
+                    yr[eq + 8 * i] = *reinterpret_cast<const float4 *>(&sm.ob[hb][tr][4 * (eq + 8 * i)]);
             }
         }
     };
@@ -825,12 +826,9 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             decay_products(ch + 1);                        // parity ch+1 was last read in ch-1
             if (ch + 2 < nchunks) load_gates(ch + 2);
         }
-        if (ch >= 2) {                                     // chunk ch-2's o rows are written
-            bar_sync(uBarEmpty0 + hb, uRT + uST);
-            emit(ch - 2);
-        }
-        bar_sync(uBarStg, uST);                            // its z slot is read: refill it
-        if (stid == 0 && ch + 2 < nchunks) issue_chunk(ch + 2);
+        // the row warps are done with chunk ch-2 (its per-chunk buffers may be rewritten once
+        // NORMS below has been passed)
+        if (ch >= 2) bar_sync(uBarEmpty0 + hb, uRT + uST);
         // q norms of chunk ch (warps 0-3: token 8 w + lane % 8, pieces lane / 8 + 4 i)
         if (sw < 4) {
             mbar_wait_bounded(&sm.bar_load[slot], load_parity(ch));
@@ -849,6 +847,9 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             if (nq == 0) sm.rq[tok] = (tok < nt) ? rsqrtf(ss + p.qk_eps) * inv_sqrt_dk : 0.f;
         }
         bar_arrive(uBarNorms, 64 + uST);
+        if (ch >= 2) emit(ch - 2);
+        bar_sync(uBarStg, uST);                            // its z slot is read: refill it
+        if (stid == 0 && ch + 2 < nchunks) issue_chunk(ch + 2);
         bar_arrive(uBarFull0 + hb, uNT);
     }
     for (int ch = max(0, nchunks - 2); ch < nchunks; ch++) {

@@ -569,7 +569,7 @@ def main(argv=None):
                        bytes_per_step=decode_bytes(w)),
         "roofline": {"bound": "hbm", "achieved": per_launch, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": per_launch / peaks["hbm_gbs"],
-                     "traffic": profiled_traffic("gdn_decode.cu", "decode_b64_dram_traffic.txt"),
+                     "traffic": profiled_traffic("gdn_decode.cuh", "decode_b64_dram_traffic.txt"),
                      "peak_source": peaks["source"], "kernel": "gdn_decode_kernel",
                      "frac_of_nominal_8tbs": per_launch / 8000.0},
         "cpu_baseline": cpu,

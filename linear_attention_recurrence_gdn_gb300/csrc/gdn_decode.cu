@@ -1,428 +1,34 @@
-// gdn_decode.cu -- single-token GDN step, one HBM read and one HBM write of every state row.
-//
-// Algorithm: logicaffeine_compile::codegen_cuda::gdn, "The fusion": because the update is
-// affine in S, o[a] = alpha (S_old q^)[a] + coef[a] (k^ . q^) with coef[a] = beta (v[a] -
-// alpha u[a]), so one pass over a state row gives u[a] = S_old[a,:] k^ and w[a] = S_old[a,:] q^,
-// and the updated row alpha S_old[a,:] + coef[a] k^ is written back from the registers that
-// already hold it.  The gated RMSNorm (GDN_KERNELS: "needs the whole head") runs in the same
-// CTA because one CTA owns a whole head at a time, so there is no second kernel and o never
-// round-trips through memory.
-//
-// GB300 mapping (differs from the page's one-block-per-(head, row) launch):
-//   * persistent CTAs, one per SM for Dk = Dv = 128: CTA c processes heads c, c + grid, ...
-//     A head's whole state (64 KB), its q, k, v and z rows arrive in shared memory by bulk
-//     asynchronous copies (TMA, cp.async.bulk) that complete on an mbarrier; NST stages keep
-//     the next head's copy in flight while the current head is computed.  Measured on GB300:
-//     two stages, the next copy issued right after the current head's rows are written back,
-//     beat deeper prefetch -- the state is updated in place, and HBM serves an in-place
-//     stream best when a row's write follows its read closely;
-//   * Dv/16 warps; every warp owns 16 rows of the head; a row is split over L lanes (L = 8
-//     for Dk = 128), each lane holding NV float4 column groups (NV = 4), read from shared
-//     memory without bank conflicts (8 lanes read one 128-byte run);
-//   * row dot products reduce over the L lanes of the row with xor shuffles (log2 L stages);
-//   * q^, k^ are normalised in registers (the same lane layout, so the norm sums also reduce
-//     over L lanes); k^.q^ is one scalar per head, as the page notes;
-//   * the updated rows go straight from registers to global memory (coalesced float4 stores).
-#include <math.h>
-
-#include <algorithm>
-
-#include "gdn_common.cuh"
+// gdn_decode.cu -- entry of the decode step: dispatch on the activation type (one unit per
+// type, gdn_decode_{f32,bf16,f16}.cu, instantiating gdn_decode.cuh for every Dk, Dv), the
+// wait-timeout self-test kernel, and the decode watchdog words.
 #include "gdn_internal.h"
 #include "gdn_tma.cuh"
 
 namespace gdn {
-namespace {
-
-template <int DK> struct DecodeGeom;
-template <> struct DecodeGeom<128> { static constexpr int NV = 4; };
-template <> struct DecodeGeom<64> { static constexpr int NV = 4; };
-template <> struct DecodeGeom<32> { static constexpr int NV = 2; };
-template <> struct DecodeGeom<16> { static constexpr int NV = 1; };
-
-constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// Tuning knobs (defaults are the measured best on GB300):
-//   GDN_DECODE_STAGES_128  pipeline stages for Dk = Dv = 128 (64 KB of state each)
-//   GDN_DECODE_SPLIT       bulk copies a head's state is cut into
-//   GDN_DECODE_LDGSTS      1: per-thread cp.async (LSU path) instead of TMA bulk copies
-#ifndef GDN_DECODE_STAGES_128
-#define GDN_DECODE_STAGES_128 2
-#endif
-#ifndef GDN_DECODE_SPLIT
-#define GDN_DECODE_SPLIT 1
-#endif
-#ifndef GDN_DECODE_LDGSTS
-#define GDN_DECODE_LDGSTS 0
-#endif
-//   GDN_DECODE_LATE_ISSUE  1: issue the next copy into a freed stage after the row updates
-//   GDN_DECODE_MINB        minimum resident CTAs per SM requested from the compiler
-#ifndef GDN_DECODE_LATE_ISSUE
-#define GDN_DECODE_LATE_ISSUE 1
-#endif
-#ifndef GDN_DECODE_MINB
-#define GDN_DECODE_MINB 1
-#endif
-
-template <typename TA, int DK, int DV> struct DecodeCfg {
-    static constexpr int NV = DecodeGeom<DK>::NV;   // float4 per lane per row
-    static constexpr int L = DK / (4 * NV);         // lanes per row
-    static constexpr int RPS = 32 / L;              // rows covered by one warp-wide access
-    static constexpr int R = 16 / RPS;              // row slots per lane (16 rows per warp)
-    static constexpr int NWARPS = DV / 16;
-    static constexpr int NT = NWARPS * 32;
-    static constexpr int STATE = DV * DK;           // floats per head
-    // stages: 2 for 64 KB heads (measured best) and for 32 KB heads (then several CTAs share
-    // an SM: Dk = 128, Dv = 64 ran at 5261 GB/s with 2 stages, 4136 GB/s with 4), else 4
-    static constexpr int NST = (STATE >= 128 * 128) ? GDN_DECODE_STAGES_128 : (STATE >= 64 * 128 ? 2 : 4);
-    // shared-memory layout (every copy destination 16-byte aligned)
-    static constexpr size_t ST_OFF = 0;
-    static constexpr size_t Q_OFF = ST_OFF + size_t(NST) * STATE * 4;
-    static constexpr size_t K_OFF = Q_OFF + size_t(NST) * DK * sizeof(TA);
-    static constexpr size_t V_OFF = K_OFF + size_t(NST) * DK * sizeof(TA);
-    static constexpr size_t Z_OFF = V_OFF + size_t(NST) * DV * sizeof(TA);
-    static constexpr size_t BAR_OFF = align_up(Z_OFF + size_t(NST) * DV * sizeof(TA), 16);
-    static constexpr size_t RED_OFF = BAR_OFF + size_t(NST) * 8;
-    static constexpr size_t BYTES = RED_OFF + size_t(NWARPS) * 4;
-    static_assert(L * 4 * NV == DK && RPS * L == 32 && R * RPS == 16, "geometry");
-    static_assert(DV % 16 == 0 && NWARPS >= 1, "Dv must be a multiple of 16");
-    static_assert(DK * sizeof(TA) % 16 == 0 && DV * sizeof(TA) % 16 == 0, "bulk copy sizes");
-};
-
-template <typename TA, int DK, int DV>
-__global__ void __launch_bounds__(DecodeCfg<TA, DK, DV>::NT, GDN_DECODE_MINB)
-gdn_decode_kernel(const gdn_params p, int64_t nheads) {
-    using C = DecodeCfg<TA, DK, DV>;
-    using A = Act<TA>;
-    constexpr int NV = C::NV, L = C::L, RPS = C::RPS, R = C::R, NST = C::NST;
-    constexpr int STATE = C::STATE;
-
-    extern __shared__ __align__(128) unsigned char smem[];
-    float *st_s = reinterpret_cast<float *>(smem + C::ST_OFF);
-    TA *q_s = reinterpret_cast<TA *>(smem + C::Q_OFF);
-    TA *k_s = reinterpret_cast<TA *>(smem + C::K_OFF);
-    TA *v_s = reinterpret_cast<TA *>(smem + C::V_OFF);
-    TA *z_s = reinterpret_cast<TA *>(smem + C::Z_OFF);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
-
-    const bool gated = p.z != nullptr;
-    const unsigned tx = STATE * 4 + 2 * DK * sizeof(TA) + (gated ? 2 : 1) * DV * sizeof(TA);
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int g = lane / L;                              // row within a warp-wide access
-    const int part = lane % L;                           // column part of the row
-    const int row0 = warp * 16 + g;                      // rows row0 + r * RPS
-    const int group = p.Hv / p.Hk;
-    const int64_t nmine =
-        (blockIdx.x < nheads) ? (nheads - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-
-    if (tid == 0) {
-        for (int s = 0; s < NST; s++) mbar_init(&bar[s], 1);
-        mbar_init_fence();
-    }
-    __syncthreads();
-    // Programmatic dependent launch: the next kernel on the stream may start its set-up now;
-    // this one reads nothing from global memory before the previous kernel (the step that
-    // wrote the state, or whatever produced the inputs) has completed.  Both are no-ops in a
-    // plain launch.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    auto head_of = [&](int64_t i) -> int64_t { return blockIdx.x + i * gridDim.x; };
-#if GDN_DECODE_LDGSTS
-    // every thread copies the state float4s it will read itself; threads 0.. copy the small
-    // vectors; one cp.async group per head (empty groups keep the count uniform)
-    auto issue = [&](int64_t i, int s) {
-        if (i < nmine) {
-            const int64_t h = head_of(i);
-            const int b = static_cast<int>(h / p.Hv);
-            const int hk = static_cast<int>(h - static_cast<int64_t>(b) * p.Hv) / group;
-            const int64_t qo = (static_cast<int64_t>(b) * p.Hk + hk) * DK;
-            const float *src = p.state + h * STATE;
-            float *dst = st_s + s * STATE;
-#pragma unroll
-            for (int r = 0; r < R; r++)
-#pragma unroll
-                for (int c = 0; c < NV; c++) {
-                    const int off = (row0 + r * RPS) * DK + 4 * (c * L + part);
-                    cp_async16(dst + off, src + off);
-                }
-            constexpr int QP = DK * sizeof(TA) / 16, VP = DV * sizeof(TA) / 16;
-            if (tid < QP) {
-                cp_async16(reinterpret_cast<char *>(q_s + s * DK) + 16 * tid,
-                           reinterpret_cast<const char *>(static_cast<const TA *>(p.q) + qo) + 16 * tid);
-                cp_async16(reinterpret_cast<char *>(k_s + s * DK) + 16 * tid,
-                           reinterpret_cast<const char *>(static_cast<const TA *>(p.k) + qo) + 16 * tid);
-            } else if (tid < QP + VP) {
-                const int t = tid - QP;
-                cp_async16(reinterpret_cast<char *>(v_s + s * DV) + 16 * t,
-                           reinterpret_cast<const char *>(static_cast<const TA *>(p.v) + h * DV) + 16 * t);
-                if (gated)
-                    cp_async16(reinterpret_cast<char *>(z_s + s * DV) + 16 * t,
-                               reinterpret_cast<const char *>(static_cast<const TA *>(p.z) + h * DV) + 16 * t);
-            }
-        }
-        cp_async_commit();
-    };
-    for (int64_t i = 0; i < NST; i++) issue(i, static_cast<int>(i));
-#else
-    // thread 0: bulk copies of head i's state and inputs into stage s
-    auto issue = [&](int64_t i, int s) {
-        const int64_t h = head_of(i);
-        const int b = static_cast<int>(h / p.Hv);
-        const int hk = static_cast<int>(h - static_cast<int64_t>(b) * p.Hv) / group;
-        const int64_t qo = (static_cast<int64_t>(b) * p.Hk + hk) * DK;   // S == 1
-        constexpr int SPLIT = (STATE * 4 / GDN_DECODE_SPLIT) % 16 == 0 ? GDN_DECODE_SPLIT : 1;
-        constexpr int PIECE = STATE / SPLIT;
-        mbar_arrive_expect_tx(&bar[s], tx);
-#pragma unroll
-        for (int j = 0; j < SPLIT; j++)
-            bulk_g2s(st_s + s * STATE + j * PIECE, p.state + h * STATE + j * PIECE, PIECE * 4, &bar[s]);
-        bulk_g2s(q_s + s * DK, static_cast<const TA *>(p.q) + qo, DK * sizeof(TA), &bar[s]);
-        bulk_g2s(k_s + s * DK, static_cast<const TA *>(p.k) + qo, DK * sizeof(TA), &bar[s]);
-        bulk_g2s(v_s + s * DV, static_cast<const TA *>(p.v) + h * DV, DV * sizeof(TA), &bar[s]);
-        if (gated)
-            bulk_g2s(z_s + s * DV, static_cast<const TA *>(p.z) + h * DV, DV * sizeof(TA), &bar[s]);
-    };
-    if (tid == 0)
-        for (int64_t i = 0; i < nmine && i < NST; i++) issue(i, static_cast<int>(i));
-#endif
-
-    // gates of the next head are prefetched one head ahead into registers
-    float gl = 0.f, gb = 0.f;
-    if (nmine > 0) {
-        gl = load_gate(p.log_decay, p.gate_dtype, head_of(0));
-        gb = load_gate(p.beta, p.gate_dtype, head_of(0));
-    }
-    const float inv_sqrt_dk = rsqrtf(static_cast<float>(DK));
-
-    for (int64_t i = 0; i < nmine; i++) {
-        const int s = static_cast<int>(i % NST);
-        const int64_t h = head_of(i);
-        const float alpha = expf(gl), beta = gb;
-        if (i + 1 < nmine) {
-            gl = load_gate(p.log_decay, p.gate_dtype, head_of(i + 1));
-            gb = load_gate(p.beta, p.gate_dtype, head_of(i + 1));
-        }
-
-#if GDN_DECODE_LDGSTS
-        cp_async_wait<NST - 1>();
-        __syncthreads();
-#else
-        // wait for stage s; a timed-out wait (watchdog set) ends the whole CTA together
-        const bool ok = mbar_wait_bounded(&bar[s], static_cast<unsigned>((i / NST) & 1));
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0)   // let this CTA's copies still in flight land before leaving
-                for (int64_t j = i; j < nmine && j < i + NST; j++)
-                    mbar_wait_bounded(&bar[j % NST], static_cast<unsigned>((j / NST) & 1));
-            return;
-        }
-#endif
-
-        // 1. this lane's state rows and the head's inputs, from shared memory
-        const float *S = st_s + s * STATE;
-        float4 sr[R][NV];
-#pragma unroll
-        for (int r = 0; r < R; r++)
-#pragma unroll
-            for (int c = 0; c < NV; c++)
-                sr[r][c] = *reinterpret_cast<const float4 *>(
-                    S + (row0 + r * RPS) * DK + 4 * (c * L + part));
-        float4 kh[NV], qh[NV];
-#pragma unroll
-        for (int c = 0; c < NV; c++) {
-            kh[c] = A::four(k_s + s * DK + 4 * (c * L + part));
-            qh[c] = A::four(q_s + s * DK + 4 * (c * L + part));
-        }
-        float vr[R], zr[R];
-#pragma unroll
-        for (int r = 0; r < R; r++) {
-            vr[r] = A::one(v_s + s * DV + row0 + r * RPS);
-            zr[r] = gated ? A::one(z_s + s * DV + row0 + r * RPS) : 0.f;
-        }
-        __syncthreads();                                 // stage s consumed by every thread
-#if !GDN_DECODE_LATE_ISSUE
-#if GDN_DECODE_LDGSTS
-        issue(i + NST, s);
-#else
-        if (tid == 0 && i + NST < nmine) issue(i + NST, s);
-#endif
-#endif
-
-        // 2. q^, k^ and k^.q^
-        float ssk = 0.f, ssq = 0.f, skq = 0.f;
-#pragma unroll
-        for (int c = 0; c < NV; c++) {
-            ssk = dot4(kh[c], kh[c], ssk);
-            ssq = dot4(qh[c], qh[c], ssq);
-            skq = dot4(kh[c], qh[c], skq);
-        }
-        ssk = group_sum<L>(ssk);
-        ssq = group_sum<L>(ssq);
-        skq = group_sum<L>(skq);
-        const float rk = rsqrtf(ssk + p.qk_eps);
-        const float rq = rsqrtf(ssq + p.qk_eps) * inv_sqrt_dk;
-#pragma unroll
-        for (int c = 0; c < NV; c++) {
-            kh[c].x *= rk; kh[c].y *= rk; kh[c].z *= rk; kh[c].w *= rk;
-            qh[c].x *= rq; qh[c].y *= rq; qh[c].z *= rq; qh[c].w *= rq;
-        }
-        const float kq = skq * rk * rq;                  // k^ . q^, one scalar per head
-
-        // 3. fused pass per row: u, w from the registers, updated row straight to HBM
-        float *Sg = p.state + h * STATE;
-        float o[R];
-#pragma unroll
-        for (int r = 0; r < R; r++) {
-            float pu = 0.f, pw = 0.f;
-#pragma unroll
-            for (int c = 0; c < NV; c++) {
-                pu = dot4(sr[r][c], kh[c], pu);
-                pw = dot4(sr[r][c], qh[c], pw);
-            }
-            pu = group_sum<L>(pu);
-            pw = group_sum<L>(pw);
-            const float coef = beta * (vr[r] - alpha * pu);
-            float *row = Sg + (row0 + r * RPS) * DK;
-#pragma unroll
-            for (int c = 0; c < NV; c++) {
-                float4 n;
-                n.x = fmaf(alpha, sr[r][c].x, coef * kh[c].x);
-                n.y = fmaf(alpha, sr[r][c].y, coef * kh[c].y);
-                n.z = fmaf(alpha, sr[r][c].z, coef * kh[c].z);
-                n.w = fmaf(alpha, sr[r][c].w, coef * kh[c].w);
-                *reinterpret_cast<float4 *>(row + 4 * (c * L + part)) = n;
-            }
-            o[r] = fmaf(alpha, pw, coef * kq);
-        }
-
-#if GDN_DECODE_LATE_ISSUE
-#if GDN_DECODE_LDGSTS
-        issue(i + NST, s);
-#else
-        if (tid == 0 && i + NST < nmine) issue(i + NST, s);
-#endif
-#endif
-
-        // 4. output: gated RMSNorm over the head's Dv rows, or the raw o
-        float *yp = p.y + h * DV;
-        if (gated) {
-            float x[R];
-            float ss = 0.f;
-#pragma unroll
-            for (int r = 0; r < R; r++) {
-                x[r] = o[r] * silu(zr[r]);
-                ss = fmaf(x[r], x[r], ss);
-            }
-            // every row's x is replicated over its L lanes: count it once (part == 0)
-            ss = (part == 0) ? ss : 0.f;
-            ss = group_sum<32>(ss);
-            if (lane == 0) red[warp] = ss;
-            __syncthreads();
-            float total = 0.f;
-#pragma unroll
-            for (int w = 0; w < C::NWARPS; w++) total += red[w];
-            const float rr = rsqrtf(total / static_cast<float>(DV) + p.norm_eps);
-            if (part == 0) {
-#pragma unroll
-                for (int r = 0; r < R; r++) {
-                    const int a = row0 + r * RPS;
-                    yp[a] = x[r] * rr * p.gn[a];
-                }
-            }
-        } else if (part == 0) {
-#pragma unroll
-            for (int r = 0; r < R; r++) yp[row0 + r * RPS] = o[r];
-        }
-    }
-}
-
-constexpr int kMaxDevices = 64;
-
-// Per-device launch configuration of one kernel instantiation, computed on first use (the
-// attribute call and the occupancy query cost more than a small decode step's launch).
-struct LaunchSlots {
-    int slots[kMaxDevices] = {};   // resident CTAs on the whole device; 0 = not computed
-};
-
-template <typename TA, int DK, int DV>
-cudaError_t launch_typed(const gdn_params &p, cudaStream_t stream) {
-    using C = DecodeCfg<TA, DK, DV>;
-    static LaunchSlots cache;
-    auto kern = gdn_decode_kernel<TA, DK, DV>;
-    const int bytes = static_cast<int>(C::BYTES);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    int slots = (dev >= 0 && dev < kMaxDevices) ? cache.slots[dev] : 0;
-    if (slots == 0) {
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) !=
-            cudaSuccess)
-            return e;
-        int occ = 0, sms = 0;
-        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::NT, bytes)) !=
-            cudaSuccess)
-            return e;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return e;
-        slots = std::max(1, sms) * std::max(1, occ);
-        if (dev >= 0 && dev < kMaxDevices) cache.slots[dev] = slots;
-    }
-    const int64_t heads = static_cast<int64_t>(p.B) * p.Hv;
-    const int64_t grid = std::min<int64_t>(heads, slots);
-    // launched as a programmatic dependent of the previous kernel on the stream: its CTAs
-    // become resident as that kernel's CTAs retire and wait (griddepcontrol.wait) for its
-    // completion, which hides the launch gap between consecutive decode steps
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(C::NT);
-    cfg.dynamicSmemBytes = bytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p, heads);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
-
-template <typename TA, int DK>
-cudaError_t launch_dv(const gdn_params &p, cudaStream_t stream) {
-    switch (p.Dv) {
-        case 16: return launch_typed<TA, DK, 16>(p, stream);
-        case 32: return launch_typed<TA, DK, 32>(p, stream);
-        case 64: return launch_typed<TA, DK, 64>(p, stream);
-        case 128: return launch_typed<TA, DK, 128>(p, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-template <typename TA>
-cudaError_t launch_dim(const gdn_params &p, cudaStream_t stream) {
-    switch (p.Dk) {
-        case 16: return launch_dv<TA, 16>(p, stream);
-        case 32: return launch_dv<TA, 32>(p, stream);
-        case 64: return launch_dv<TA, 64>(p, stream);
-        case 128: return launch_dv<TA, 128>(p, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-}  // namespace
 
 cudaError_t launch_decode(const gdn_params &p, cudaStream_t stream) {
     switch (p.act_dtype) {
-        case GDN_F32: return launch_dim<float>(p, stream);
-        case GDN_BF16: return launch_dim<__nv_bfloat16>(p, stream);
-        case GDN_F16: return launch_dim<__half>(p, stream);
+        case GDN_F32: return launch_decode_f32(p, stream);
+        case GDN_BF16: return launch_decode_bf16(p, stream);
+        case GDN_F16: return launch_decode_f16(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 namespace {
+// This unit's watchdog word (the wait-timeout self-test below), read and cleared.
+cudaError_t read_own_watchdog(unsigned *flag, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_watchdog, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+    const unsigned zero = 0;
+    if (*flag) e = cudaMemcpyToSymbolAsync(g_watchdog, &zero, sizeof(unsigned), 0,
+                                           cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    return e;
+}
+
 // A wait that cannot complete: the barrier's one arrival comes with 16 expected bytes and no
 // copy ever sends them, so the bounded wait runs out, sets the watchdog word and returns.
 __global__ void gdn_wait_timeout_kernel(uint64_t limit_ns) {
@@ -443,15 +49,17 @@ cudaError_t launch_wait_timeout(cudaStream_t stream, uint64_t limit_ns) {
 }
 
 cudaError_t decode_watchdog(unsigned *flag, cudaStream_t stream) {
-    cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_watchdog, sizeof(unsigned), 0,
-                                              cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) return e;
-    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
-    const unsigned zero = 0;
-    if (*flag) e = cudaMemcpyToSymbolAsync(g_watchdog, &zero, sizeof(unsigned), 0,
-                                           cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    return e;
+    cudaError_t (*const words[])(unsigned *, cudaStream_t) = {
+        read_own_watchdog, decode_watchdog_f32, decode_watchdog_bf16, decode_watchdog_f16};
+    unsigned any = 0;
+    for (auto read : words) {
+        unsigned f = 0;
+        const cudaError_t e = read(&f, stream);
+        if (e != cudaSuccess) return e;
+        any |= f;
+    }
+    *flag = any;
+    return cudaSuccess;
 }
 
 }  // namespace gdn

@@ -11,7 +11,16 @@ namespace gdn {
 // One decode step: one CTA per (b, hv) head, gated norm fused in the CTA tail.
 cudaError_t launch_decode(const gdn_params &p, cudaStream_t stream);
 
-// Reads and clears the decode kernels' watchdog word (synchronises `stream`).
+// The decode step per activation type (gdn_decode_{f32,bf16,f16}.cu) and each unit's watchdog
+// word (read and cleared; synchronises `stream`).
+cudaError_t launch_decode_f32(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_decode_f16(const gdn_params &p, cudaStream_t stream);
+cudaError_t decode_watchdog_f32(unsigned *flag, cudaStream_t stream);
+cudaError_t decode_watchdog_bf16(unsigned *flag, cudaStream_t stream);
+cudaError_t decode_watchdog_f16(unsigned *flag, cudaStream_t stream);
+
+// Reads and clears the decode kernels' watchdog words (synchronises `stream`).
 cudaError_t decode_watchdog(unsigned *flag, cudaStream_t stream);
 
 // One CTA whose mbarrier wait runs out after limit_ns, setting the decode watchdog word.
@@ -24,11 +33,19 @@ cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
 // each unit's watchdog word (read and cleared; synchronises `stream`).
 cudaError_t launch_scan_tc_dk16(const gdn_params &p, cudaStream_t stream);
 cudaError_t launch_scan_tc_dk32(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk48(const gdn_params &p, cudaStream_t stream);
 cudaError_t launch_scan_tc_dk64(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk80(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk96(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk112(const gdn_params &p, cudaStream_t stream);
 cudaError_t launch_scan_tc_dk128(const gdn_params &p, cudaStream_t stream);
 cudaError_t scan_watchdog_dk16(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk32(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_watchdog_dk48(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk64(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_watchdog_dk80(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_watchdog_dk96(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_watchdog_dk112(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk128(unsigned *flag, cudaStream_t stream);
 
 // The chunked scan with the memory in tensor memory (bf16, Dk = Dv = 128, 16-byte aligned

@@ -14,21 +14,35 @@ cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
     switch (p.Dk) {
         case 16: return launch_scan_tc_dk16(p, stream);
         case 32: return launch_scan_tc_dk32(p, stream);
+        case 48: return launch_scan_tc_dk48(p, stream);
         case 64: return launch_scan_tc_dk64(p, stream);
+        case 80: return launch_scan_tc_dk80(p, stream);
+        case 96: return launch_scan_tc_dk96(p, stream);
+        case 112: return launch_scan_tc_dk112(p, stream);
         case 128: return launch_scan_tc_dk128(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {
-    unsigned f[5] = {0, 0, 0, 0, 0};
-    cudaError_t e;
-    if ((e = scan_watchdog_dk16(&f[0], stream)) != cudaSuccess) return e;
-    if ((e = scan_watchdog_dk32(&f[1], stream)) != cudaSuccess) return e;
-    if ((e = scan_watchdog_dk64(&f[2], stream)) != cudaSuccess) return e;
-    if ((e = scan_watchdog_dk128(&f[3], stream)) != cudaSuccess) return e;
-    if ((e = scan_umma_watchdog(&f[4], stream)) != cudaSuccess) return e;
-    *flag = f[0] | f[1] | f[2] | f[3] | f[4];
+    cudaError_t (*const words[])(unsigned *, cudaStream_t) = {
+        scan_watchdog_dk16,
+        scan_watchdog_dk32,
+        scan_watchdog_dk48,
+        scan_watchdog_dk64,
+        scan_watchdog_dk80,
+        scan_watchdog_dk96,
+        scan_watchdog_dk112,
+        scan_watchdog_dk128,
+        scan_umma_watchdog};
+    unsigned any = 0;
+    for (auto read : words) {
+        unsigned f = 0;
+        const cudaError_t e = read(&f, stream);
+        if (e != cudaSuccess) return e;
+        any |= f;
+    }
+    *flag = any;
     return cudaSuccess;
 }
 

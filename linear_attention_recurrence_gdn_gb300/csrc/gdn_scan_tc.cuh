@@ -91,7 +91,8 @@ template <typename TA, int DK, int DV, int NW> struct TcCfg {
     static constexpr bool WHOLE_HEAD = (RB == DV);
     static constexpr int KPIECES = DK * (int)sizeof(TA) / 16;    // 16-byte pieces of a k row
     static constexpr int VPIECES = RB * (int)sizeof(TA) / 16;    // ... of this CTA's v rows
-    static constexpr int TPK = KPIECES < 4 ? KPIECES : 4;        // norm-pass threads per token
+    static constexpr int TPK = KPIECES % 4 == 0 ? 4 : (KPIECES % 2 == 0 ? 2 : 1);  // norm-pass
+                                                                  // threads per token
     static_assert(DV % RB == 0 && DK % 16 == 0 && DV % 16 == 0, "shape");
     static_assert(KPIECES >= 1 && VPIECES >= 1, "16-byte copy granularity");
     static_assert(KPIECES % TPK == 0 && (SPLIT_KQ ? PT / 2 : PT) / TPK >= kT,
@@ -406,7 +407,8 @@ gdn_scan_tc_kernel(const gdn_params p) {
     // groups of this CTA's RB columns interleaved (a quarter-warp reads 128 contiguous bytes);
     // a split head first sends each token's partial sum of squares to the other CTAs of its
     // cluster and waits for theirs.  Without z: this CTA's raw o rows.
-    constexpr int TPT = (RB / 4 < 8) ? RB / 4 : 8;         // threads per token (norm)
+    constexpr int TPT = (RB / 4) % 8 == 0 ? 8 : 4;         // threads per token (norm); RB / 4
+                                                           // is a multiple of 4
     constexpr int FPT = RB / (4 * TPT);                    // float4 groups per thread
     constexpr int NIT = kT * TPT / PT;                     // token passes
     static_assert(PT % TPT == 0 && (kT * TPT) % PT == 0, "norm thread groups");
@@ -780,7 +782,7 @@ cudaError_t launch_tc_dv128(const gdn_params &p, cudaStream_t stream) {
     }
 }
 
-// Dv < 128: one CTA per head, Dv / 16 row warps.
+// Dv < 128 (a multiple of 16): one CTA per head, Dv / 16 row warps.
 template <typename TA, int DK, int DV>
 cudaError_t launch_tc_small(const gdn_params &p, cudaStream_t stream) {
     int occ = 0;
@@ -795,7 +797,11 @@ cudaError_t launch_tc_dv(const gdn_params &p, cudaStream_t stream) {
     switch (p.Dv) {
         case 16: return launch_tc_small<TA, DK, 16>(p, stream);
         case 32: return launch_tc_small<TA, DK, 32>(p, stream);
+        case 48: return launch_tc_small<TA, DK, 48>(p, stream);
         case 64: return launch_tc_small<TA, DK, 64>(p, stream);
+        case 80: return launch_tc_small<TA, DK, 80>(p, stream);
+        case 96: return launch_tc_small<TA, DK, 96>(p, stream);
+        case 112: return launch_tc_small<TA, DK, 112>(p, stream);
         case 128: return launch_tc_dv128<TA, DK>(p, stream);
         default: return cudaErrorInvalidValue;
     }

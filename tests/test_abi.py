@@ -124,9 +124,10 @@ REJECTIONS = [
     (dict(S=-2), 0, gdn.GDN_ERR_BAD_SHAPE, "B and S"),
     (dict(S=3), 1, gdn.GDN_ERR_BAD_SHAPE, "S == 1"),
     (dict(S=0), 1, gdn.GDN_ERR_BAD_SHAPE, "S == 1"),
-    (dict(Dk=48, Dv=48), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "16, 32, 64 or 128"),
-    (dict(Dk=256, Dv=256), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "16, 32, 64 or 128"),
-    (dict(Dk=64, Dv=96), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "16, 32, 64 or 128"),
+    (dict(Dk=40, Dv=40), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
+    (dict(Dk=256, Dv=256), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
+    (dict(Dk=64, Dv=72), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
+    (dict(Dk=144, Dv=64), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
     (dict(act_dtype=7), 0, gdn.GDN_ERR_BAD_DTYPE, "act_dtype"),
     (dict(act_dtype=gdn.GDN_BF16, gate_dtype=gdn.GDN_F16), 0, gdn.GDN_ERR_BAD_DTYPE, "gate_dtype"),
     (dict(qk_eps=-1.0), 0, gdn.GDN_ERR_BAD_ARG, "eps"),

@@ -1,6 +1,7 @@
-"""GPU parity with separate key and value head dims (Dk != Dv), decode and scan, against the
-fp64 oracle.  Tolerances as for the square heads: decode 1e-4, scan 2e-3 (relative to
-1 + |oracle|), on y and the final state.
+"""GPU parity with separate key and value head dims (Dk != Dv) and head dims that are not powers
+of two (any multiple of 16 up to 128), decode and scan, against the fp64 oracle.  Tolerances as
+for the square heads: decode 1e-4, scan 2e-3 (relative to 1 + |oracle|), on y and the final
+state.
 """
 from __future__ import annotations
 
@@ -31,6 +32,13 @@ SCAN_CASES = [
     (1, 50, 1, 1, 128, 64, "bf16", False),
     (2, 20, 1, 2, 32, 128, "f32", False),
     (3, 64, 1, 3, 128, 16, "bf16", True),
+    # head dims that are not powers of two (pruned nested prefixes of a 128-wide head)
+    (2, 45, 1, 2, 48, 80, "bf16", False),
+    (1, 70, 2, 2, 96, 112, "f16", True),
+    (2, 33, 1, 3, 112, 48, "f32", False),
+    (1, 40, 1, 2, 80, 96, "bf16", True),
+    (1, 64, 2, 4, 96, 96, "bf16", False),
+    (1, 37, 1, 1, 112, 128, "f16", False),   # Dv = 128 with an odd Dk: the split-head path
 ]
 
 
@@ -57,6 +65,11 @@ DECODE_CASES = [
     (2, 2, 4, 128, 16, "f16"),
     (4, 1, 1, 32, 64, "f32"),
     (5, 2, 2, 16, 128, "bf16"),
+    (3, 1, 2, 48, 80, "bf16"),
+    (2, 2, 2, 96, 112, "f16"),
+    (4, 1, 3, 112, 48, "f32"),
+    (3, 1, 1, 80, 96, "bf16"),
+    (2, 1, 2, 128, 96, "bf16"),
 ]
 
 

@@ -15,7 +15,7 @@
 //
 // GB300 mapping (bf16, Dk = Dv = 128, one CTA per head):
 //   * the 128 x 128 f32 memory lives in tensor memory (lanes = memory rows); every product is
-//     a tcgen05 MMA with M = 128 issued by one thread, A operands in tensor memory (f32 values
+//     a tcgen05 MMA with M = 128 issued by one elected lane, A operands in tensor memory (f32 values
 //     split into bf16 hi + lo, about 2^-16 relative per product; bf16 k, q exact), B operands in
 //     shared memory (k and q as the tensor-map copies land them: 128-byte swizzle, K-major or
 //     MN-major; the small per-chunk matrices as 8 x 8 core matrices);
@@ -23,14 +23,19 @@
 //     running) plus the correction C_c (K_c [K;Q]_{c+1}^T) once chunk c's update coefficients
 //     C_c are known, so the long K = 128 product stays off the serial path; the serial path per
 //     chunk is r -> d = R T -> C, D -> O = D QX', S' += C K, correction -> o;
-//   * 4 row warps (one per tensor-memory lane quarter, a thread per memory row) do the
-//     element-wise steps; the chunk tables come from one MMA per chunk, A = [K;Q]_{c+1},
-//     B = [K_c | K_{c+1}]: lanes 0-31 hold K_{c+1} K_c^T and K_{c+1} K_{c+1}^T, lanes 32-63 hold
-//     Q_{c+1} K_c^T and Q_{c+1} K_{c+1}^T.  Two table warps (lane quarters 0 and 1) turn them
-//     into the correction operand, N, the unit-triangular inverse T and QX' (one lane per
-//     token column, 16-byte stores of the core-matrix layout); six staging warps issue the
-//     tensor-map copies, form the decay products and the q norms, and apply the gated RMSNorm
-//     to finished chunks (one warp per token, coalesced rows).
+//   * 8 row warps (two per tensor-memory lane quarter, a thread per memory row, each half of
+//     the columns and of the tokens) do the element-wise steps; the chunk tables come from
+//     one MMA group per chunk, A = [K;Q]_{c+1}, B = [K_c | K_{c+1}]: lanes 0-31 hold
+//     K_{c+1} K_c^T and K_{c+1} K_{c+1}^T, lanes 32-63 hold Q_{c+1} K_c^T and Q_{c+1} K_{c+1}^T.
+//     Two table warps (lane quarters 0 and 1) turn them into the correction operand, N, the
+//     unit-triangular inverse T (16 x 16 diagonal blocks by back substitution, the off-diagonal
+//     block as -T11 N12 T22) and QX' (one lane per token column, 16-byte stores of the
+//     core-matrix layout); the second of them issues the next chunk's table MMAs.  Six
+//     staging warps issue the tensor-map copies, form the decay products one chunk ahead, the
+//     q norms, and apply the gated RMSNorm to finished chunks (8 lanes per token).  The
+//     operands of a chunk are buffered by chunk % 3, so the producers may run two chunks
+//     ahead of the row warps.
+//   * MMAs are issued by one elect.sync lane of a converged warp.
 //   Only TMA, tcgen05 (mma, ld, st, alloc, commit, fences), plain shared / global accesses,
 //   mbarriers and named barriers are used.
 #include <cuda.h>
@@ -100,12 +105,13 @@ struct alignas(1024) U3Smem {
     __nv_bfloat16 kq[uSlots][kSlotKQ / 2];        // k / q staging ring (16 KB per slot)
     alignas(16) __nv_bfloat16 v[uSlots][uC][uD];  // v, z rows (unswizzled boxes)
     alignas(16) __nv_bfloat16 z[uSlots][uC][uD];
-    alignas(16) __nv_bfloat16 thi[2][uC * uC], tlo[2][uC * uC];   // T = (I + N)^-1, B [s][t]
-    alignas(16) __nv_bfloat16 phi[2][uC * uC], plo[2][uC * uC];   // QX', B [s][t]
-    alignas(16) __nv_bfloat16 ghi[2][2 * uC * uC], glo[2][2 * uC * uC];   // correction, B [j][n], N = 64
-    alignas(16) float ob[2][uC][uD + 4];          // o of a chunk (row warps -> staging warps)
-    alignas(16) float cb[2][uC], cx[2][uC], cy[2][uC], cw[2][uC];  // per-token row constants
-    alignas(16) float gam[2][4];                  // e^{cum_31} of the chunk
+    // a chunk's operands for the row warps, by chunk % 3 (the producers may run two chunks ahead)
+    alignas(16) __nv_bfloat16 thi[3][uC * uC], tlo[3][uC * uC];   // T = (I + N)^-1, B [s][t]
+    alignas(16) __nv_bfloat16 phi[3][uC * uC], plo[3][uC * uC];   // QX', B [s][t]
+    alignas(16) __nv_bfloat16 ghi[3][2 * uC * uC], glo[3][2 * uC * uC];   // correction, B [j][n], N = 64
+    alignas(16) float ob[2][uC][uD];              // o of a chunk (row warps -> staging warps)
+    alignas(16) float cb[3][uC], cx[3][uC], cy[3][uC], cw[3][uC];  // per-token row constants
+    alignas(16) float gam[3][4];                  // e^{cum_31} of the chunk
     alignas(16) float4 gts[2][uC];                // beta, e^{cum_t}, e^{cum_31 - cum_t} (by chunk parity)
     alignas(16) float cum[2][uC];
     alignas(16) float gamp[2][4];                 // e^{cum_31}, reference m, factored-exp flag
@@ -115,23 +121,24 @@ struct alignas(1024) U3Smem {
     alignas(16) float tR[16][20];                 // T[0:16][0:16] row-major
     alignas(8) uint64_t bar_load[uSlots];         // a slot's copies landed
     alignas(8) uint64_t bar_tab, bar_d, bar_o, bar_pre;   // MMA groups completed
-    alignas(8) uint64_t bar_g[2];                 // correction operand written (64 arrivals)
+    alignas(8) uint64_t bar_g[3];                 // correction operand written (64 arrivals)
     alignas(8) uint64_t bar_gates[2];             // decay products of a chunk written (32)
     uint32_t tmem_base;
 };
 static_assert(sizeof(U3Smem) + 1024 <= 227 * 1024, "shared memory");
 
-// Named barriers.  FULL: row warps sync, table + staging warps arrive (chunk operands ready).
+// Named barriers.  FULL (three, by chunk % 3): row warps sync, table + staging warps arrive
+// (chunk operands ready).
 // EMPTY: row warps arrive, staging warps sync (o rows of a chunk written).  NORMS: staging
-// arrive, table warps sync (the q norms are written, and the row warps are done with chunk
-// ch-2, so its per-chunk buffers may be rewritten).  TDONE: table warps arrive, staging sync
+// arrive, table warps sync (the q norms are written; the staging warps have passed the chunk
+// before, so the row warps are done with chunk ch-3 and its per-chunk buffers may be rewritten).  TDONE: table warps arrive, staging sync
 // (table warps done with the previous chunk's shared buffers).  TBAR: rk and the factored
 // exponentials from table warp 0 to table warp 1; TBAR2: the diagonal blocks of T likewise.
 // TLD: both table warps have read the chunk tables out of tensor memory, so table warp 1 may
 // issue the next chunk's table MMAs into the same columns.
 enum {
-    uBarFull0 = 1, uBarEmpty0 = 3, uBarRow = 5, uBarStg = 6, uBarT2 = 7, uBarNorms = 8,
-    uBarTdone = 9, uBarT = 10, uBarTld = 11
+    uBarFull0 = 1, uBarEmpty0 = 4, uBarRow = 6, uBarStg = 7, uBarT2 = 8, uBarNorms = 9,
+    uBarTdone = 10, uBarT = 11, uBarTld = 12
 };
 
 __global__ void __launch_bounds__(uNT, 1)
@@ -159,8 +166,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         mbar_init(&sm.bar_d, 1);
         mbar_init(&sm.bar_o, 1);
         mbar_init(&sm.bar_pre, 1);
-        mbar_init(&sm.bar_g[0], 64);
-        mbar_init(&sm.bar_g[1], 64);
+        for (int i = 0; i < 3; i++) mbar_init(&sm.bar_g[i], 64);
         mbar_init(&sm.bar_gates[0], 32);
         mbar_init(&sm.bar_gates[1], 32);
         mbar_init_fence();
@@ -265,11 +271,11 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
 
         float lam = 1.0f;                                  // true memory = lam * S'
         for (int ch = 0; ch < nchunks; ch++) {
-            const int hb = ch & 1, slot = ch % uSlots;
+            const int hb = ch & 1, tb = ch % 3, slot = ch % uSlots;
             const int nt = min(uC, S - ch * uC);
             const bool more = ch + 1 < nchunks;
             const uint32_t xy = TM_XY + 64 * hb, xyn = TM_XY + 64 * (hb ^ 1);
-            bar_sync(uBarFull0 + hb, uNT);                 // chunk ch's operands staged
+            bar_sync(uBarFull0 + tb, uNT);                 // chunk ch's operands staged
 
             // ---- r = beta (v - lam e^cum rk x) (0 past the end); y <- lam e^cum rq y in place
             {                                              // tokens t0r .. t0r + 15
@@ -281,9 +287,9 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 float ys[16];
 #pragma unroll
                 for (int t4 = 0; t4 < 4; t4++) {
-                    const float4 b4 = *reinterpret_cast<const float4 *>(&sm.cb[hb][t0r + 4 * t4]);
-                    const float4 x4 = *reinterpret_cast<const float4 *>(&sm.cx[hb][t0r + 4 * t4]);
-                    const float4 y4 = *reinterpret_cast<const float4 *>(&sm.cy[hb][t0r + 4 * t4]);
+                    const float4 b4 = *reinterpret_cast<const float4 *>(&sm.cb[tb][t0r + 4 * t4]);
+                    const float4 x4 = *reinterpret_cast<const float4 *>(&sm.cx[tb][t0r + 4 * t4]);
+                    const float4 y4 = *reinterpret_cast<const float4 *>(&sm.cy[tb][t0r + 4 * t4]);
                     const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
                     const float bx[4] = {x4.x, x4.y, x4.z, x4.w};
                     const float by[4] = {y4.x, y4.y, y4.z, y4.w};
@@ -308,7 +314,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             row_barrier();
             issue(0, [&] {                                 // d = R T into x's columns
                 tc_fence_after();
-                const uint32_t th = smem_u32(&sm.thi[hb][0]), tlw = smem_u32(&sm.tlo[hb][0]);
+                const uint32_t th = smem_u32(&sm.thi[tb][0]), tlw = smem_u32(&sm.tlo[tb][0]);
 #pragma unroll
                 for (int k2 = 0; k2 < 2; k2++) {
                     const uint64_t bh = umma_desc(th + 256 * k2, 128, 512, false);
@@ -334,7 +340,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             wait_mma(&sm.bar_d, static_cast<unsigned>(ch & 1));
 
             // ---- d -> bf16 hi / lo (A of O); C = d W rk / lam' -> hi / lo (A of the update)
-            const float lam_new = lam * sm.gam[hb][0];
+            const float lam_new = lam * sm.gam[tb][0];
             const bool fold = !(lam_new >= 0x1p-40f);      // uniform over the CTA
             const float scale = fold ? 1.0f : 1.0f / lam_new;
             {                                              // tokens 16 hr .. 16 hr + 15
@@ -343,7 +349,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 uint32_t dh[8], dl[8], chh[8], cll[8];
 #pragma unroll
                 for (int t4 = 0; t4 < 4; t4++) {
-                    const float4 w4 = *reinterpret_cast<const float4 *>(&sm.cw[hb][16 * hr + 4 * t4]);
+                    const float4 w4 = *reinterpret_cast<const float4 *>(&sm.cw[tb][16 * hr + 4 * t4]);
                     const float ww[4] = {w4.x * scale, w4.y * scale, w4.z * scale, w4.w * scale};
 #pragma unroll
                     for (int e2 = 0; e2 < 2; e2++) {
@@ -379,7 +385,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             row_barrier();
             issue(0, [&] {
                 tc_fence_after();
-                const uint32_t ph_ = smem_u32(&sm.phi[hb][0]), pl_ = smem_u32(&sm.plo[hb][0]);
+                const uint32_t ph_ = smem_u32(&sm.phi[tb][0]), pl_ = smem_u32(&sm.plo[tb][0]);
 #pragma unroll
                 for (int k2 = 0; k2 < 2; k2++) {           // o += D QX' (onto the scaled y)
                     const uint64_t bh = umma_desc(ph_ + 256 * k2, 128, 512, false);
@@ -396,8 +402,8 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                     umma_ts(tmem + TM_S, tmem + TM_CH + 8 * k2, bk, kIdN128Mn, true);
                 }
                 if (more) {                                // next [x | y] += C (K_ch [K;Q]_{ch+1}^T)
-                    const int gb = (ch + 1) & 1;
-                    mbar_wait_bounded(&sm.bar_g[gb], static_cast<unsigned>((ch >> 1) & 1));
+                    const int gb = (ch + 1) % 3;           // prep ch+1 wrote it, use (ch) / 3 of gb
+                    mbar_wait_bounded(&sm.bar_g[gb], static_cast<unsigned>((ch / 3) & 1));
                     tc_fence_after();
                     const uint32_t gh = smem_u32(&sm.ghi[gb][0]), gl = smem_u32(&sm.glo[gb][0]);
 #pragma unroll
@@ -449,7 +455,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         const int t = lane;
         const uint32_t tabl = tmem + (static_cast<uint32_t>(32 * tq) << 16) + TM_TAB;
         for (int ch = 0; ch < nchunks; ch++) {
-            const int hb = ch & 1;
+            const int hb = ch & 1, tb = ch % 3;
             const int nt = min(uC, S - ch * uC);
             mbar_wait_bounded(&sm.bar_tab, static_cast<unsigned>(ch & 1));
             __syncwarp();
@@ -468,8 +474,8 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             }
             if (ch > 0) {                                  // correction operand, column n
                 const int n = 32 * tq + t;
-                char *gh = reinterpret_cast<char *>(&sm.ghi[hb][0]);
-                char *gl = reinterpret_cast<char *>(&sm.glo[hb][0]);
+                char *gh = reinterpret_cast<char *>(&sm.ghi[tb][0]);
+                char *gl = reinterpret_cast<char *>(&sm.glo[tb][0]);
 #pragma unroll
                 for (int kg = 0; kg < 4; kg++) {
                     uint32_t h4[4], l4[4];
@@ -479,7 +485,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                     *reinterpret_cast<uint4 *>(gl + core_run(n, kg)) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&sm.bar_g[hb]);
+                mbar_arrive(&sm.bar_g[tb]);
             }
             mbar_wait_bounded(&sm.bar_gates[hb], static_cast<unsigned>((ch >> 1) & 1));
             __syncwarp();
@@ -565,11 +571,11 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 }
                 __syncwarp();
                 bar_arrive(uBarT2, 64);                    // diagonal blocks ready
-                bar_sync(uBarNorms, 64 + uST);             // row warps done with chunk ch-2
+                bar_sync(uBarNorms, 64 + uST);             // row warps done with chunk ch-3
                 // column t of T as B [s][t]: rows of the lane's diagonal block; zeros below
                 // the diagonal block for t < 16 (rows 16-31 of T11's columns)
-                char *dh = reinterpret_cast<char *>(&sm.thi[hb][0]);
-                char *dl = reinterpret_cast<char *>(&sm.tlo[hb][0]);
+                char *dh = reinterpret_cast<char *>(&sm.thi[tb][0]);
+                char *dl = reinterpret_cast<char *>(&sm.tlo[tb][0]);
 #pragma unroll
                 for (int kk = 0; kk < 2; kk++) {
                     uint32_t h4[4], l4[4];
@@ -618,13 +624,13 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                         }
                     }
                 }
-                sm.cb[hb][t] = gt.x;
-                sm.cx[hb][t] = gt.y * rk_own;
-                sm.cy[hb][t] = gt.y * rq_t;
-                sm.cw[hb][t] = gt.z * rk_own;
-                if (t == 0) sm.gam[hb][0] = sm.gamp[hb][0];
-                char *ph_ = reinterpret_cast<char *>(&sm.phi[hb][0]);
-                char *pl_ = reinterpret_cast<char *>(&sm.plo[hb][0]);
+                sm.cb[tb][t] = gt.x;
+                sm.cx[tb][t] = gt.y * rk_own;
+                sm.cy[tb][t] = gt.y * rq_t;
+                sm.cw[tb][t] = gt.z * rk_own;
+                if (t == 0) sm.gam[tb][0] = sm.gamp[hb][0];
+                char *ph_ = reinterpret_cast<char *>(&sm.phi[tb][0]);
+                char *pl_ = reinterpret_cast<char *>(&sm.plo[tb][0]);
 #pragma unroll
                 for (int kg = 0; kg < 4; kg++) {           // column t as B [s][t], hi / lo
                     uint32_t h4[4], l4[4];
@@ -681,14 +687,14 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 uint32_t h4[4], l4[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) split2(t12[2 * i], t12[2 * i + 1], h4[i], l4[i]);
-                *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(&sm.thi[hb][0]) + core_run(tc, hf)) =
+                *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(&sm.thi[tb][0]) + core_run(tc, hf)) =
                     make_uint4(h4[0], h4[1], h4[2], h4[3]);
-                *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(&sm.tlo[hb][0]) + core_run(tc, hf)) =
+                *reinterpret_cast<uint4 *>(reinterpret_cast<char *>(&sm.tlo[tb][0]) + core_run(tc, hf)) =
                     make_uint4(l4[0], l4[1], l4[2], l4[3]);
             }
             fence_proxy_async_smem();                      // operands for the tensor core
             if (ch + 1 < nchunks) bar_arrive(uBarTdone, 64 + uST);
-            bar_arrive(uBarFull0 + hb, uNT);
+            bar_arrive(uBarFull0 + tb, uNT);
         }
         return;
     }
@@ -826,9 +832,6 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             decay_products(ch + 1);                        // parity ch+1 was last read in ch-1
             if (ch + 2 < nchunks) load_gates(ch + 2);
         }
-        // the row warps are done with chunk ch-2 (its per-chunk buffers may be rewritten once
-        // NORMS below has been passed)
-        if (ch >= 2) bar_sync(uBarEmpty0 + hb, uRT + uST);
         // q norms of chunk ch (warps 0-3: token 8 w + lane % 8, pieces lane / 8 + 4 i)
         if (sw < 4) {
             mbar_wait_bounded(&sm.bar_load[slot], load_parity(ch));
@@ -846,11 +849,16 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             ss += __shfl_xor_sync(0xffffffffu, ss, 16);
             if (nq == 0) sm.rq[tok] = (tok < nt) ? rsqrtf(ss + p.qk_eps) * inv_sqrt_dk : 0.f;
         }
+        // the table warps may now write chunk ch's operands: this point comes after the EMPTY
+        // wait of the chunk before, so the row warps are done with chunk ch-3
         bar_arrive(uBarNorms, 64 + uST);
-        if (ch >= 2) emit(ch - 2);
+        if (ch >= 2) {                                     // chunk ch-2's o rows are written
+            bar_sync(uBarEmpty0 + hb, uRT + uST);
+            emit(ch - 2);
+        }
         bar_sync(uBarStg, uST);                            // its z slot is read: refill it
         if (stid == 0 && ch + 2 < nchunks) issue_chunk(ch + 2);
-        bar_arrive(uBarFull0 + hb, uNT);
+        bar_arrive(uBarFull0 + ch % 3, uNT);
     }
     for (int ch = max(0, nchunks - 2); ch < nchunks; ch++) {
         bar_sync(uBarEmpty0 + (ch & 1), uRT + uST);

@@ -656,8 +656,11 @@ gdn_scan_tc_kernel(const gdn_params p) {
                     const float2 nt_ = sm.nrm[tb + t];     // rk, rq of token t
                     const float dot = acc[j][e] * sm.nrm[tb + s2].x;   // rk_s (k_s . x_t)
                     // prod_{s<r<t} alpha_r: exp of a non-positive sum (fast exp: a few ulp,
-                    // about 1e-5 relative at the largest arguments that do not underflow)
-                    const float wgt = (s2 < t) ? __expf(sm.cum[tb + t - 1] - sm.cum[tb + s2]) : 0.f;
+                    // about 1e-5 relative at the largest arguments that do not underflow).
+                    // Evaluated for every (s, t) and then masked, so no lane branches around
+                    // the exponential; the clamps keep the unused ones finite and in range.
+                    const float ex = __expf(fminf(sm.cum[tb + max(t - 1, 0)] - sm.cum[tb + s2], 0.f));
+                    const float wgt = (s2 < t) ? ex : 0.f;
                     if (isq) {
                         const float val = (s2 < t) ? gt.x * wgt * nt_.y * dot : (s2 == t ? nt_.y * dot : 0.f);
                         split1(val, sm.phi[hb][blk][s2][t], sm.plo[hb][blk][s2][t]);

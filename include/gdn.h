@@ -68,7 +68,7 @@ typedef enum {
     GDN_OK = 0,
     GDN_ERR_NULL_PTR = -1,        /* a required pointer is NULL, or z/gn only one given     */
     GDN_ERR_BAD_SHAPE = -2,       /* dims < 0 or heads < 1, Hv % Hk != 0, S != 1 on decode   */
-    GDN_ERR_UNSUPPORTED_DIM = -3, /* Dk or Dv not a multiple of 16 in [16, 128] (any pair)    */
+    GDN_ERR_UNSUPPORTED_DIM = -3, /* Dk or Dv neither 256 nor a multiple of 16 in [16, 128]   */
     GDN_ERR_BAD_DTYPE = -4,       /* unknown dtype, or gate dtype neither F32 nor act dtype  */
     GDN_ERR_MISALIGNED = -5,      /* a pointer is not aligned (16 B; gates: element size)    */
     GDN_ERR_ALIASING = -6,        /* y overlaps an operand, or state partially overlaps s0   */

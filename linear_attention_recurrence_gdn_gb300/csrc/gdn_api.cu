@@ -41,7 +41,7 @@ int64_t dtype_bytes(int dt) {
 
 bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-bool supported_dim(int d) { return d >= 16 && d <= 128 && d % 16 == 0; }
+bool supported_dim(int d) { return (d >= 16 && d <= 128 && d % 16 == 0) || d == 256; }
 
 // Returns GDN_OK or a status, and sets *why to a static reason.
 int check(const gdn_params *p, int is_decode, const char **why) {
@@ -65,7 +65,7 @@ int check(const gdn_params *p, int is_decode, const char **why) {
     }
     if (p->Dk < 1 || p->Dv < 1) { *why = "Dk and Dv must be >= 1"; return GDN_ERR_BAD_SHAPE; }
     if (!supported_dim(p->Dk) || !supported_dim(p->Dv)) {
-        *why = "Dk and Dv must be multiples of 16 from 16 to 128";
+        *why = "Dk and Dv must be multiples of 16 from 16 to 128, or 256";
         return GDN_ERR_UNSUPPORTED_DIM;
     }
     const int64_t eact = dtype_bytes(p->act_dtype);
@@ -179,7 +179,7 @@ const char *gdn_status_string(int status) {
         case GDN_OK: return "ok";
         case GDN_ERR_NULL_PTR: return "a required pointer is NULL (or only one of z, gn given)";
         case GDN_ERR_BAD_SHAPE: return "bad shape (dims, Hv % Hk, or S != 1 on decode)";
-        case GDN_ERR_UNSUPPORTED_DIM: return "unsupported head dim (Dk, Dv: multiples of 16 from 16 to 128)";
+        case GDN_ERR_UNSUPPORTED_DIM: return "unsupported head dim (Dk, Dv: multiples of 16 from 16 to 128, or 256)";
         case GDN_ERR_BAD_DTYPE: return "bad dtype";
         case GDN_ERR_MISALIGNED: return "misaligned pointer";
         case GDN_ERR_ALIASING: return "output overlaps an operand";

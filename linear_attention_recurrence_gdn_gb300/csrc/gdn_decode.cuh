@@ -10,15 +10,19 @@
 //
 // GB300 mapping (differs from the page's one-block-per-(head, row) launch):
 //   * persistent CTAs, one per SM for Dk = Dv = 128: CTA c processes heads c, c + grid, ...
-//     A head's whole state (64 KB), its q, k, v and z rows arrive in shared memory by bulk
+//     A unit's state (64 KB), its q, k, v and z rows arrive in shared memory by bulk
 //     asynchronous copies (TMA, cp.async.bulk) that complete on an mbarrier; NST stages keep
 //     the next head's copy in flight while the current head is computed.  Measured on GB300:
 //     two stages, the next copy issued right after the current head's rows are written back,
 //     beat deeper prefetch -- the state is updated in place, and HBM serves an in-place
 //     stream best when a row's write follows its read closely;
-//   * Dv/16 warps; every warp owns 16 rows of the head; a row is split over L lanes (L = 8
-//     for Dk = 128), each lane holding NV float4 column groups (NV = 4), read from shared
-//     memory without bank conflicts (8 lanes read one 128-byte run);
+//   * a unit of work is a head, or for heads of more than 64 KB of state (a head dim of 256)
+//     a block of its rows; a head's units run back to back on one CTA, and the gated RMSNorm
+//     then keeps the head's gated outputs in shared memory until its last unit;
+//   * every warp owns 16 rows of the unit (8 for Dk = 256); a row is split over L lanes (L = 8
+//     for Dk = 128 and 256), each lane holding NV float4 column groups (NV = 4; 8 for
+//     Dk = 256), read from shared memory without bank conflicts (8 lanes read one 128-byte
+//     run);
 //   * row dot products reduce over the L lanes of the row with xor shuffles (log2 L stages);
 //   * q^, k^ are normalised in registers (the same lane layout, so the norm sums also reduce
 //     over L lanes); k^.q^ is one scalar per head, as the page notes;
@@ -37,12 +41,24 @@ namespace gdn {
 namespace {
 
 template <int DK> struct DecodeGeom;
-// float4s per lane per row: Dk = 128 uses 8 lanes per row, every other Dk (a multiple of 16)
-// 4 lanes per row with Dk / 16 float4 each.
-template <int DK> struct DecodeGeom { static constexpr int NV = DK / 16; };
-template <> struct DecodeGeom<128> { static constexpr int NV = 4; };
+// float4s per lane per row (NV) and rows per warp (RW): Dk = 128 uses 8 lanes per row and 16
+// rows per warp; Dk = 256 8 lanes per row with 8 float4 each and 8 rows per warp (the same 64
+// state floats per lane); every other Dk (a multiple of 16) 4 lanes per row with Dk / 16 float4.
+template <int DK> struct DecodeGeom { static constexpr int NV = DK / 16, RW = 16; };
+template <> struct DecodeGeom<128> { static constexpr int NV = 4, RW = 16; };
+template <> struct DecodeGeom<256> { static constexpr int NV = 8, RW = 8; };
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Rows of one unit of work: the whole head when its state is at most 64 KB, else the largest
+// divisor of Dv that is a multiple of 16 with at most 64 KB of state (a head's row blocks then
+// run one after another on the same CTA).
+constexpr int decode_rows(int dk, int dv) {
+    if (dv * dk <= 16384) return dv;
+    for (int r = dv; r >= 16; r -= 16)
+        if (dv % r == 0 && r * dk <= 16384) return r;
+    return 16;
+}
 
 // Tuning knobs (defaults are the measured best on GB300):
 //   GDN_DECODE_STAGES_128  pipeline stages for Dk = Dv = 128 (64 KB of state each)
@@ -68,12 +84,15 @@ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 template <typename TA, int DK, int DV> struct DecodeCfg {
     static constexpr int NV = DecodeGeom<DK>::NV;   // float4 per lane per row
+    static constexpr int RW = DecodeGeom<DK>::RW;   // rows per warp
     static constexpr int L = DK / (4 * NV);         // lanes per row
     static constexpr int RPS = 32 / L;              // rows covered by one warp-wide access
-    static constexpr int R = 16 / RPS;              // row slots per lane (16 rows per warp)
-    static constexpr int NWARPS = DV / 16;
+    static constexpr int R = RW / RPS;              // row slots per lane
+    static constexpr int RBK = decode_rows(DK, DV); // rows per unit (a row block of a head)
+    static constexpr int NRBK = DV / RBK;           // units per head
+    static constexpr int NWARPS = RBK / RW;
     static constexpr int NT = NWARPS * 32;
-    static constexpr int STATE = DV * DK;           // floats per head
+    static constexpr int STATE = RBK * DK;          // state floats per unit
     // stages: 2 for 64 KB heads (measured best) and for 32 KB heads (then several CTAs share
     // an SM: Dk = 128, Dv = 64 ran at 5261 GB/s with 2 stages, 4136 GB/s with 4), else 4
     static constexpr int NST = (STATE >= 128 * 128) ? GDN_DECODE_STAGES_128 : (STATE >= 64 * 128 ? 2 : 4);
@@ -82,13 +101,15 @@ template <typename TA, int DK, int DV> struct DecodeCfg {
     static constexpr size_t Q_OFF = ST_OFF + size_t(NST) * STATE * 4;
     static constexpr size_t K_OFF = Q_OFF + size_t(NST) * DK * sizeof(TA);
     static constexpr size_t V_OFF = K_OFF + size_t(NST) * DK * sizeof(TA);
-    static constexpr size_t Z_OFF = V_OFF + size_t(NST) * DV * sizeof(TA);
-    static constexpr size_t BAR_OFF = align_up(Z_OFF + size_t(NST) * DV * sizeof(TA), 16);
+    static constexpr size_t Z_OFF = V_OFF + size_t(NST) * RBK * sizeof(TA);
+    static constexpr size_t BAR_OFF = align_up(Z_OFF + size_t(NST) * RBK * sizeof(TA), 16);
     static constexpr size_t RED_OFF = BAR_OFF + size_t(NST) * 8;
-    static constexpr size_t BYTES = RED_OFF + size_t(NWARPS) * 4;
-    static_assert(L * 4 * NV == DK && RPS * L == 32 && R * RPS == 16, "geometry");
-    static_assert(DV % 16 == 0 && NWARPS >= 1, "Dv must be a multiple of 16");
-    static_assert(DK * sizeof(TA) % 16 == 0 && DV * sizeof(TA) % 16 == 0, "bulk copy sizes");
+    static constexpr size_t XO_OFF = align_up(RED_OFF + size_t(NWARPS) * 4, 16);
+    // a head of several units keeps its gated outputs here until its last unit
+    static constexpr size_t BYTES = XO_OFF + (NRBK > 1 ? size_t(DV) * 4 : 0);
+    static_assert(L * 4 * NV == DK && RPS * L == 32 && R * RPS == RW, "geometry");
+    static_assert(DV % RBK == 0 && RBK % RW == 0 && NWARPS >= 1, "row blocks");
+    static_assert(DK * sizeof(TA) % 16 == 0 && RBK * sizeof(TA) % 16 == 0, "bulk copy sizes");
 };
 
 template <typename TA, int DK, int DV>
@@ -97,7 +118,7 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
     using C = DecodeCfg<TA, DK, DV>;
     using A = Act<TA>;
     constexpr int NV = C::NV, L = C::L, RPS = C::RPS, R = C::R, NST = C::NST;
-    constexpr int STATE = C::STATE;
+    constexpr int STATE = C::STATE, RBK = C::RBK, NRBK = C::NRBK;
 
     extern __shared__ __align__(128) unsigned char smem[];
     float *st_s = reinterpret_cast<float *>(smem + C::ST_OFF);
@@ -107,17 +128,20 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
     TA *z_s = reinterpret_cast<TA *>(smem + C::Z_OFF);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
     float *red = reinterpret_cast<float *>(smem + C::RED_OFF);
+    float *xo = reinterpret_cast<float *>(smem + C::XO_OFF);
 
     const bool gated = p.z != nullptr;
-    const unsigned tx = STATE * 4 + 2 * DK * sizeof(TA) + (gated ? 2 : 1) * DV * sizeof(TA);
+    const unsigned tx = STATE * 4 + 2 * DK * sizeof(TA) + (gated ? 2 : 1) * RBK * sizeof(TA);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane / L;                              // row within a warp-wide access
     const int part = lane % L;                           // column part of the row
-    const int row0 = warp * 16 + g;                      // rows row0 + r * RPS
+    const int row0 = warp * C::RW + g;                   // unit rows row0 + r * RPS
     const int group = p.Hv / p.Hk;
+    // this CTA's heads blockIdx.x, blockIdx.x + grid, ...; unit u = (head i, row block rb)
     const int64_t nmine =
         (blockIdx.x < nheads) ? (nheads - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t nunits = nmine * NRBK;
 
     if (tid == 0) {
         for (int s = 0; s < NST; s++) mbar_init(&bar[s], 1);
@@ -133,15 +157,17 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
 
     auto head_of = [&](int64_t i) -> int64_t { return blockIdx.x + i * gridDim.x; };
 #if GDN_DECODE_LDGSTS
-    // every thread copies the state float4s it will read itself; threads 0.. copy the small
-    // vectors; one cp.async group per head (empty groups keep the count uniform)
-    auto issue = [&](int64_t i, int s) {
-        if (i < nmine) {
-            const int64_t h = head_of(i);
+    // every thread copies the state float4s it will read itself; the threads copy the small
+    // vectors in turn; one cp.async group per unit (empty groups keep the count uniform)
+    auto issue = [&](int64_t u, int s) {
+        if (u < nunits) {
+            const int64_t h = head_of(u / NRBK);
+            const int rb = static_cast<int>(u % NRBK);
             const int b = static_cast<int>(h / p.Hv);
             const int hk = static_cast<int>(h - static_cast<int64_t>(b) * p.Hv) / group;
             const int64_t qo = (static_cast<int64_t>(b) * p.Hk + hk) * DK;
-            const float *src = p.state + h * STATE;
+            const int64_t vo = h * DV + rb * RBK;
+            const float *src = p.state + h * (static_cast<int64_t>(DV) * DK) + rb * STATE;
             float *dst = st_s + s * STATE;
 #pragma unroll
             for (int r = 0; r < R; r++)
@@ -150,62 +176,71 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
                     const int off = (row0 + r * RPS) * DK + 4 * (c * L + part);
                     cp_async16(dst + off, src + off);
                 }
-            constexpr int QP = DK * sizeof(TA) / 16, VP = DV * sizeof(TA) / 16;
-            if (tid < QP) {
-                cp_async16(reinterpret_cast<char *>(q_s + s * DK) + 16 * tid,
-                           reinterpret_cast<const char *>(static_cast<const TA *>(p.q) + qo) + 16 * tid);
-                cp_async16(reinterpret_cast<char *>(k_s + s * DK) + 16 * tid,
-                           reinterpret_cast<const char *>(static_cast<const TA *>(p.k) + qo) + 16 * tid);
-            } else if (tid < QP + VP) {
-                const int t = tid - QP;
-                cp_async16(reinterpret_cast<char *>(v_s + s * DV) + 16 * t,
-                           reinterpret_cast<const char *>(static_cast<const TA *>(p.v) + h * DV) + 16 * t);
+            constexpr int QP = DK * sizeof(TA) / 16, VP = RBK * sizeof(TA) / 16;
+            for (int t = tid; t < QP; t += C::NT) {
+                cp_async16(reinterpret_cast<char *>(q_s + s * DK) + 16 * t,
+                           reinterpret_cast<const char *>(static_cast<const TA *>(p.q) + qo) + 16 * t);
+                cp_async16(reinterpret_cast<char *>(k_s + s * DK) + 16 * t,
+                           reinterpret_cast<const char *>(static_cast<const TA *>(p.k) + qo) + 16 * t);
+            }
+            for (int t = tid; t < VP; t += C::NT) {
+                cp_async16(reinterpret_cast<char *>(v_s + s * RBK) + 16 * t,
+                           reinterpret_cast<const char *>(static_cast<const TA *>(p.v) + vo) + 16 * t);
                 if (gated)
-                    cp_async16(reinterpret_cast<char *>(z_s + s * DV) + 16 * t,
-                               reinterpret_cast<const char *>(static_cast<const TA *>(p.z) + h * DV) + 16 * t);
+                    cp_async16(reinterpret_cast<char *>(z_s + s * RBK) + 16 * t,
+                               reinterpret_cast<const char *>(static_cast<const TA *>(p.z) + vo) + 16 * t);
             }
         }
         cp_async_commit();
     };
-    for (int64_t i = 0; i < NST; i++) issue(i, static_cast<int>(i));
+    for (int64_t u = 0; u < NST; u++) issue(u, static_cast<int>(u));
 #else
-    // thread 0: bulk copies of head i's state and inputs into stage s
-    auto issue = [&](int64_t i, int s) {
-        const int64_t h = head_of(i);
+    // thread 0: bulk copies of unit u's state rows and inputs into stage s
+    auto issue = [&](int64_t u, int s) {
+        const int64_t h = head_of(u / NRBK);
+        const int rb = static_cast<int>(u % NRBK);
         const int b = static_cast<int>(h / p.Hv);
         const int hk = static_cast<int>(h - static_cast<int64_t>(b) * p.Hv) / group;
         const int64_t qo = (static_cast<int64_t>(b) * p.Hk + hk) * DK;   // S == 1
+        const int64_t vo = h * DV + rb * RBK;
+        const float *src = p.state + h * (static_cast<int64_t>(DV) * DK) + rb * STATE;
         constexpr int SPLIT = (STATE * 4 / GDN_DECODE_SPLIT) % 16 == 0 ? GDN_DECODE_SPLIT : 1;
         constexpr int PIECE = STATE / SPLIT;
         mbar_arrive_expect_tx(&bar[s], tx);
 #pragma unroll
         for (int j = 0; j < SPLIT; j++)
-            bulk_g2s(st_s + s * STATE + j * PIECE, p.state + h * STATE + j * PIECE, PIECE * 4, &bar[s]);
+            bulk_g2s(st_s + s * STATE + j * PIECE, src + j * PIECE, PIECE * 4, &bar[s]);
         bulk_g2s(q_s + s * DK, static_cast<const TA *>(p.q) + qo, DK * sizeof(TA), &bar[s]);
         bulk_g2s(k_s + s * DK, static_cast<const TA *>(p.k) + qo, DK * sizeof(TA), &bar[s]);
-        bulk_g2s(v_s + s * DV, static_cast<const TA *>(p.v) + h * DV, DV * sizeof(TA), &bar[s]);
+        bulk_g2s(v_s + s * RBK, static_cast<const TA *>(p.v) + vo, RBK * sizeof(TA), &bar[s]);
         if (gated)
-            bulk_g2s(z_s + s * DV, static_cast<const TA *>(p.z) + h * DV, DV * sizeof(TA), &bar[s]);
+            bulk_g2s(z_s + s * RBK, static_cast<const TA *>(p.z) + vo, RBK * sizeof(TA), &bar[s]);
     };
     if (tid == 0)
-        for (int64_t i = 0; i < nmine && i < NST; i++) issue(i, static_cast<int>(i));
+        for (int64_t u = 0; u < nunits && u < NST; u++) issue(u, static_cast<int>(u));
 #endif
 
     // gates of the next head are prefetched one head ahead into registers
-    float gl = 0.f, gb = 0.f;
+    float gl = 0.f, gb = 0.f, alpha = 0.f, beta = 0.f;
     if (nmine > 0) {
         gl = load_gate(p.log_decay, p.gate_dtype, head_of(0));
         gb = load_gate(p.beta, p.gate_dtype, head_of(0));
     }
     const float inv_sqrt_dk = rsqrtf(static_cast<float>(DK));
+    float head_ss = 0.f;                                 // sum of squares over a head's units
 
-    for (int64_t i = 0; i < nmine; i++) {
-        const int s = static_cast<int>(i % NST);
+    for (int64_t u = 0; u < nunits; u++) {
+        const int s = static_cast<int>(u % NST);
+        const int64_t i = u / NRBK;
+        const int rb = static_cast<int>(u % NRBK);
         const int64_t h = head_of(i);
-        const float alpha = expf(gl), beta = gb;
-        if (i + 1 < nmine) {
-            gl = load_gate(p.log_decay, p.gate_dtype, head_of(i + 1));
-            gb = load_gate(p.beta, p.gate_dtype, head_of(i + 1));
+        if (rb == 0) {
+            alpha = expf(gl);
+            beta = gb;
+            if (i + 1 < nmine) {
+                gl = load_gate(p.log_decay, p.gate_dtype, head_of(i + 1));
+                gb = load_gate(p.beta, p.gate_dtype, head_of(i + 1));
+            }
         }
 
 #if GDN_DECODE_LDGSTS
@@ -213,10 +248,10 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
         __syncthreads();
 #else
         // wait for stage s; a timed-out wait (watchdog set) ends the whole CTA together
-        const bool ok = mbar_wait_bounded(&bar[s], static_cast<unsigned>((i / NST) & 1));
+        const bool ok = mbar_wait_bounded(&bar[s], static_cast<unsigned>((u / NST) & 1));
         if (__syncthreads_or(!ok)) {
             if (tid == 0)   // let this CTA's copies still in flight land before leaving
-                for (int64_t j = i; j < nmine && j < i + NST; j++)
+                for (int64_t j = u; j < nunits && j < u + NST; j++)
                     mbar_wait_bounded(&bar[j % NST], static_cast<unsigned>((j / NST) & 1));
             return;
         }
@@ -240,15 +275,15 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
         float vr[R], zr[R];
 #pragma unroll
         for (int r = 0; r < R; r++) {
-            vr[r] = A::one(v_s + s * DV + row0 + r * RPS);
-            zr[r] = gated ? A::one(z_s + s * DV + row0 + r * RPS) : 0.f;
+            vr[r] = A::one(v_s + s * RBK + row0 + r * RPS);
+            zr[r] = gated ? A::one(z_s + s * RBK + row0 + r * RPS) : 0.f;
         }
         __syncthreads();                                 // stage s consumed by every thread
 #if !GDN_DECODE_LATE_ISSUE
 #if GDN_DECODE_LDGSTS
-        issue(i + NST, s);
+        issue(u + NST, s);
 #else
-        if (tid == 0 && i + NST < nmine) issue(i + NST, s);
+        if (tid == 0 && u + NST < nunits) issue(u + NST, s);
 #endif
 #endif
 
@@ -273,7 +308,7 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
         const float kq = skq * rk * rq;                  // k^ . q^, one scalar per head
 
         // 3. fused pass per row: u, w from the registers, updated row straight to HBM
-        float *Sg = p.state + h * STATE;
+        float *Sg = p.state + h * (static_cast<int64_t>(DV) * DK) + rb * STATE;
         float o[R];
 #pragma unroll
         for (int r = 0; r < R; r++) {
@@ -301,14 +336,14 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
 
 #if GDN_DECODE_LATE_ISSUE
 #if GDN_DECODE_LDGSTS
-        issue(i + NST, s);
+        issue(u + NST, s);
 #else
-        if (tid == 0 && i + NST < nmine) issue(i + NST, s);
+        if (tid == 0 && u + NST < nunits) issue(u + NST, s);
 #endif
 #endif
 
         // 4. output: gated RMSNorm over the head's Dv rows, or the raw o
-        float *yp = p.y + h * DV;
+        float *yp = p.y + h * DV + rb * RBK;
         if (gated) {
             float x[R];
             float ss = 0.f;
@@ -317,20 +352,35 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads) {
                 x[r] = o[r] * silu(zr[r]);
                 ss = fmaf(x[r], x[r], ss);
             }
+            if constexpr (NRBK > 1) {
+                if (part == 0) {
+#pragma unroll
+                    for (int r = 0; r < R; r++) xo[rb * RBK + row0 + r * RPS] = x[r];
+                }
+            }
             // every row's x is replicated over its L lanes: count it once (part == 0)
             ss = (part == 0) ? ss : 0.f;
             ss = group_sum<32>(ss);
             if (lane == 0) red[warp] = ss;
-            __syncthreads();
+            __syncthreads();                             // red (and this unit's xo) complete
             float total = 0.f;
 #pragma unroll
             for (int w = 0; w < C::NWARPS; w++) total += red[w];
-            const float rr = rsqrtf(total / static_cast<float>(DV) + p.norm_eps);
-            if (part == 0) {
+            if constexpr (NRBK == 1) {
+                const float rr = rsqrtf(total / static_cast<float>(DV) + p.norm_eps);
+                if (part == 0) {
 #pragma unroll
-                for (int r = 0; r < R; r++) {
-                    const int a = row0 + r * RPS;
-                    yp[a] = x[r] * rr * p.gn[a];
+                    for (int r = 0; r < R; r++) {
+                        const int a = row0 + r * RPS;
+                        yp[a] = x[r] * rr * p.gn[a];
+                    }
+                }
+            } else {
+                head_ss += total;
+                if (rb == NRBK - 1) {                    // the head's last unit: all of y
+                    const float rr = rsqrtf(head_ss / static_cast<float>(DV) + p.norm_eps);
+                    for (int a = tid; a < DV; a += C::NT) p.y[h * DV + a] = xo[a] * rr * p.gn[a];
+                    head_ss = 0.f;
                 }
             }
         } else if (part == 0) {
@@ -402,6 +452,7 @@ cudaError_t launch_dv(const gdn_params &p, cudaStream_t stream) {
         case 96: return launch_typed<TA, DK, 96>(p, stream);
         case 112: return launch_typed<TA, DK, 112>(p, stream);
         case 128: return launch_typed<TA, DK, 128>(p, stream);
+        case 256: return launch_typed<TA, DK, 256>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -417,6 +468,7 @@ cudaError_t launch_dim(const gdn_params &p, cudaStream_t stream) {
         case 96: return launch_dv<TA, 96>(p, stream);
         case 112: return launch_dv<TA, 112>(p, stream);
         case 128: return launch_dv<TA, 128>(p, stream);
+        case 256: return launch_dv<TA, 256>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -39,6 +39,7 @@ cudaError_t launch_scan_tc_dk80(const gdn_params &p, cudaStream_t stream);
 cudaError_t launch_scan_tc_dk96(const gdn_params &p, cudaStream_t stream);
 cudaError_t launch_scan_tc_dk112(const gdn_params &p, cudaStream_t stream);
 cudaError_t launch_scan_tc_dk128(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk256(const gdn_params &p, cudaStream_t stream);
 cudaError_t scan_watchdog_dk16(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk32(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk48(unsigned *flag, cudaStream_t stream);
@@ -47,6 +48,7 @@ cudaError_t scan_watchdog_dk80(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk96(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk112(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk128(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_watchdog_dk256(unsigned *flag, cudaStream_t stream);
 
 // The chunked scan with the memory in tensor memory (bf16, Dk = Dv = 128, 16-byte aligned
 // operands; chosen by GDN_FLAG_SCAN_TMEM), and its watchdog word.

@@ -20,6 +20,7 @@ cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
         case 96: return launch_scan_tc_dk96(p, stream);
         case 112: return launch_scan_tc_dk112(p, stream);
         case 128: return launch_scan_tc_dk128(p, stream);
+        case 256: return launch_scan_tc_dk256(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -34,6 +35,7 @@ cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {
         scan_watchdog_dk96,
         scan_watchdog_dk112,
         scan_watchdog_dk128,
+        scan_watchdog_dk256,
         scan_umma_watchdog};
     unsigned any = 0;
     for (auto read : words) {

@@ -80,6 +80,12 @@ template <typename TA, int DK, int DV, int NW> struct TcCfg {
                                  NW % 4 == 0 && NP % 4 == 0),
                   "register split within the launch's registers, whole warpgroups");
     static constexpr bool SPLIT_KQ = (NP == 8);      // norm pass: k on 4 warps, q on the others
+    // f32 rows of 256: the norm pass reads the raw k, q rows from global memory (no staging
+    // slot; the two f32 rows and the hi / lo rings would not fit in shared memory together)
+    static constexpr bool DIRECT_KQ = !EXACT && sizeof(TA) == 4 && DK > 128;
+    // a warp's 16 x 256 memory block takes about 250 registers: no register split, whole
+    // register file for at most 8 warps
+    static_assert(DK <= 128 || NT <= 256, "Dk > 128 runs at most 4 row warps");
     static constexpr int NTILE = DK / 8;             // n-tiles of a warp's 16 x Dk memory block
     static constexpr int KST = DK / 16;              // k-steps over Dk
     static constexpr int NBLK = kT / kB;
@@ -102,12 +108,17 @@ template <typename TA, int DK, int DV, int NW> struct TcCfg {
 // k and q operands, rows padded by 16 bytes (conflict-free ldmatrix and 16-byte accesses).
 // bf16: the raw rows, copied in place into a ring of three slots.  Other types: a staging
 // slot for the raw rows and a ring of two slots of bf16 hi / lo parts.
-template <typename TA, int D, bool EXACT> struct TcOps;
-template <typename TA, int D> struct TcOps<TA, D, true> {
+// f32 rows of 256 have no staging slot (read from global memory by the norm pass).
+template <typename TA, int D, bool EXACT, bool DIRECT> struct TcOps;
+template <typename TA, int D> struct TcOps<TA, D, true, false> {
     __nv_bfloat16 k[3][kT][D + 8], q[3][kT][D + 8];
 };
-template <typename TA, int D> struct TcOps<TA, D, false> {
+template <typename TA, int D> struct TcOps<TA, D, false, false> {
     TA kraw[kT][D + 16 / sizeof(TA)], qraw[kT][D + 16 / sizeof(TA)];
+    __nv_bfloat16 khi[2][kT][D + 8], klo[2][kT][D + 8];
+    __nv_bfloat16 qhi[2][kT][D + 8], qlo[2][kT][D + 8];
+};
+template <typename TA, int D> struct TcOps<TA, D, false, true> {
     __nv_bfloat16 khi[2][kT][D + 8], klo[2][kT][D + 8];
     __nv_bfloat16 qhi[2][kT][D + 8], qlo[2][kT][D + 8];
 };
@@ -117,7 +128,7 @@ template <typename TA, int D> struct TcOps<TA, D, false> {
 // read (o, per-token scalars, tables) c % 2.
 template <typename TA, int DK, int DV, int NW> struct TcSmem {
     using C = TcCfg<TA, DK, DV, NW>;
-    alignas(16) TcOps<TA, DK, C::EXACT> op;
+    alignas(16) TcOps<TA, DK, C::EXACT, C::DIRECT_KQ> op;
     alignas(16) TA vr[C::NVZ][kT][C::LDV];       // raw v rows of this CTA
     alignas(16) TA zr[C::NVZ][kT][C::LDV];       // raw z (whole-head CTAs with z)
     alignas(16) float ob[2][kT][C::LDO];         // o of the chunk, written by the row warps
@@ -373,6 +384,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
 
     // copies of chunk c: raw k, q rows (into the operand ring for bf16, else the staging slot)
     auto issue_kq = [&](int c) {
+        if constexpr (C::DIRECT_KQ) return;
         const int t0 = c * kT, nt = min(kT, S - t0);
         for (int i = ptid; i < nt * C::KPIECES; i += PT) {
             const int tt = i / C::KPIECES, pc = i % C::KPIECES;
@@ -381,6 +393,8 @@ gdn_scan_tc_kernel(const gdn_params p) {
             if constexpr (EXACT) {
                 dk = reinterpret_cast<char *>(&sm.op.k[c % 3][tt][0]);
                 dq = reinterpret_cast<char *>(&sm.op.q[c % 3][tt][0]);
+            } else if constexpr (C::DIRECT_KQ) {
+                return;
             } else {
                 dk = reinterpret_cast<char *>(&sm.op.kraw[tt][0]);
                 dq = reinterpret_cast<char *>(&sm.op.qraw[tt][0]);
@@ -562,11 +576,20 @@ gdn_scan_tc_kernel(const gdn_params p) {
                 } else {
                     constexpr int E = Piece<TA>::E;
                     if (valid) {
+                        const TA *ksrc, *qsrc;
+                        if constexpr (C::DIRECT_KQ) {
+                            const int64_t off = static_cast<int64_t>(t0 + n_tok) * k_ts + E * pc;
+                            ksrc = kg + off;
+                            qsrc = qg + off;
+                        } else {
+                            ksrc = &sm.op.kraw[n_tok][E * pc];
+                            qsrc = &sm.op.qraw[n_tok][E * pc];
+                        }
                         if (do_k)
-                            Piece<TA>::split(&sm.op.kraw[n_tok][E * pc], &sm.op.khi[os][n_tok][E * pc],
+                            Piece<TA>::split(ksrc, &sm.op.khi[os][n_tok][E * pc],
                                              &sm.op.klo[os][n_tok][E * pc], ssk);
                         if (do_q)
-                            Piece<TA>::split(&sm.op.qraw[n_tok][E * pc], &sm.op.qhi[os][n_tok][E * pc],
+                            Piece<TA>::split(qsrc, &sm.op.qhi[os][n_tok][E * pc],
                                              &sm.op.qlo[os][n_tok][E * pc], ssq);
                     } else {
 #pragma unroll
@@ -755,58 +778,66 @@ inline int device_sms() {
     return n;
 }
 
-// Rows per CTA for Dv = 128: the fewest warps on the busiest SM with every CTA resident at
-// once (a sequential scan must not run in waves); ties go to the larger CTA.
-template <typename TA, int DK>
-cudaError_t launch_tc_dv128(const gdn_params &p, cudaStream_t stream) {
+// Rows per CTA among the candidates NWS (row warps, largest first): the fewest warps on the
+// busiest SM with every CTA resident at once (a sequential scan must not run in waves); ties go
+// to the larger CTA.  A candidate whose shared memory exceeds this device's limit is skipped.
+template <typename TA, int DK, int DV, int... NWS>
+cudaError_t launch_tc_best(const gdn_params &p, cudaStream_t stream) {
+    constexpr int n = sizeof...(NWS);
+    constexpr int nws[n] = {NWS...};
+    cudaError_t (*const prep[n])(int *) = {prepare_tc<TA, DK, DV, NWS>...};
+    cudaError_t (*const launch[n])(const gdn_params &, cudaStream_t) = {
+        launch_tc_cfg<TA, DK, DV, NWS>...};
     const int sms = std::max(1, device_sms());
     const int64_t heads = static_cast<int64_t>(p.B) * p.Hv;
-    int occ[3] = {0, 0, 0};
-    cudaError_t e;
-    if ((e = prepare_tc<TA, DK, 128, 8>(&occ[0])) != cudaSuccess) return e;
-    if ((e = prepare_tc<TA, DK, 128, 4>(&occ[1])) != cudaSuccess) return e;
-    if ((e = prepare_tc<TA, DK, 128, 2>(&occ[2])) != cudaSuccess) return e;
-    const int nws[3] = {8, 4, 2};
     int best = -1;
     int64_t best_cost = INT64_MAX;
-    for (int i = 0; i < 3; i++) {
-        if (occ[i] < 1) continue;
-        const int64_t ctas = heads * (8 / nws[i]);
+    for (int i = 0; i < n; i++) {
+        int occ = 0;
+        const cudaError_t e = prep[i](&occ);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) continue;
+        const int64_t ctas = heads * (DV / (16 * nws[i]));
         const int64_t per_sm = (ctas + sms - 1) / sms;
-        const int64_t waves = (per_sm + occ[i] - 1) / occ[i];
-        const int64_t cost = waves * std::min<int64_t>(per_sm, occ[i]) * nws[i];
+        const int64_t waves = (per_sm + occ - 1) / occ;
+        const int64_t cost = waves * std::min<int64_t>(per_sm, occ) * nws[i];
         if (cost < best_cost) { best_cost = cost; best = i; }
     }
     if (best < 0) return cudaErrorInvalidConfiguration;
-    switch (nws[best]) {
-        case 8: return launch_tc_cfg<TA, DK, 128, 8>(p, stream);
-        case 4: return launch_tc_cfg<TA, DK, 128, 4>(p, stream);
-        default: return launch_tc_cfg<TA, DK, 128, 2>(p, stream);
-    }
+    return launch[best](p, stream);
 }
 
-// Dv < 128 (a multiple of 16): one CTA per head, Dv / 16 row warps.
-template <typename TA, int DK, int DV>
-cudaError_t launch_tc_small(const gdn_params &p, cudaStream_t stream) {
-    int occ = 0;
-    cudaError_t e = prepare_tc<TA, DK, DV, DV / 16>(&occ);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    return launch_tc_cfg<TA, DK, DV, DV / 16>(p, stream);
-}
-
+// Value head dims: multiples of 16 up to 128, and 256.  Up to Dk = 128 a CTA takes a whole head
+// of Dv <= 112 (Dv / 16 row warps); Dv = 128 and 256 choose their rows per CTA.  Dk = 256 runs
+// at most 4 row warps per CTA, so a head of more rows is split over a cluster of CTAs.
 template <typename TA, int DK>
 cudaError_t launch_tc_dv(const gdn_params &p, cudaStream_t stream) {
-    switch (p.Dv) {
-        case 16: return launch_tc_small<TA, DK, 16>(p, stream);
-        case 32: return launch_tc_small<TA, DK, 32>(p, stream);
-        case 48: return launch_tc_small<TA, DK, 48>(p, stream);
-        case 64: return launch_tc_small<TA, DK, 64>(p, stream);
-        case 80: return launch_tc_small<TA, DK, 80>(p, stream);
-        case 96: return launch_tc_small<TA, DK, 96>(p, stream);
-        case 112: return launch_tc_small<TA, DK, 112>(p, stream);
-        case 128: return launch_tc_dv128<TA, DK>(p, stream);
-        default: return cudaErrorInvalidValue;
+    if constexpr (DK <= 128) {
+        switch (p.Dv) {
+            case 16: return launch_tc_best<TA, DK, 16, 1>(p, stream);
+            case 32: return launch_tc_best<TA, DK, 32, 2>(p, stream);
+            case 48: return launch_tc_best<TA, DK, 48, 3>(p, stream);
+            case 64: return launch_tc_best<TA, DK, 64, 4>(p, stream);
+            case 80: return launch_tc_best<TA, DK, 80, 5>(p, stream);
+            case 96: return launch_tc_best<TA, DK, 96, 6>(p, stream);
+            case 112: return launch_tc_best<TA, DK, 112, 7>(p, stream);
+            case 128: return launch_tc_best<TA, DK, 128, 8, 4, 2>(p, stream);
+            case 256: return launch_tc_best<TA, DK, 256, 8, 4>(p, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (p.Dv) {
+            case 16: return launch_tc_best<TA, DK, 16, 1>(p, stream);
+            case 32: return launch_tc_best<TA, DK, 32, 2>(p, stream);
+            case 48: return launch_tc_best<TA, DK, 48, 3>(p, stream);
+            case 64: return launch_tc_best<TA, DK, 64, 4>(p, stream);
+            case 80: return launch_tc_best<TA, DK, 80, 1>(p, stream);
+            case 96: return launch_tc_best<TA, DK, 96, 3>(p, stream);
+            case 112: return launch_tc_best<TA, DK, 112, 1>(p, stream);
+            case 128: return launch_tc_best<TA, DK, 128, 4, 2>(p, stream);
+            case 256: return launch_tc_best<TA, DK, 256, 4, 2>(p, stream);
+            default: return cudaErrorInvalidValue;
+        }
     }
 }
 

@@ -108,10 +108,10 @@ def test_valid_params_have_no_reject_reason(lib):
     # empty sequence: empty tensors may come as NULL pointers, nothing is read or written
     assert reject(lib, fake_params(S=0, y=None, q=None, k=None, v=None, z=None, log_decay=None,
                                    beta=None), 0) is None
-    for d in (16, 32, 128):
+    for d in (16, 32, 128, 256):
         assert reject(lib, fake_params(Dk=d, Dv=d), 0) is None
     # separate key and value head dims
-    for dk, dv in ((64, 128), (128, 32), (16, 64)):
+    for dk, dv in ((64, 128), (128, 32), (16, 64), (256, 128), (128, 256), (256, 48)):
         assert reject(lib, fake_params(Dk=dk, Dv=dv), 0) is None
         assert reject(lib, fake_params(Dk=dk, Dv=dv, S=1), 1) is None
 
@@ -125,7 +125,8 @@ REJECTIONS = [
     (dict(S=3), 1, gdn.GDN_ERR_BAD_SHAPE, "S == 1"),
     (dict(S=0), 1, gdn.GDN_ERR_BAD_SHAPE, "S == 1"),
     (dict(Dk=40, Dv=40), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
-    (dict(Dk=256, Dv=256), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
+    (dict(Dk=240, Dv=256), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
+    (dict(Dk=256, Dv=512), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
     (dict(Dk=64, Dv=72), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
     (dict(Dk=144, Dv=64), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
     (dict(act_dtype=7), 0, gdn.GDN_ERR_BAD_DTYPE, "act_dtype"),

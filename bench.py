@@ -68,7 +68,7 @@ def scan_mma_flops(w: Workload) -> int:
     is 2 * 16 * 8 * 16 FLOP.  The per-chunk KK / QX tables (under 4% more) are not counted.
     """
     terms = 2 if w.act == "bf16" else 3
-    kst, ntile = w.Dk // 16, w.Dv // 8
+    kst, ntile = w.Dk // 16, w.Dk // 8       # the update runs over the Dk / 8 n-tiles of a row
     per_warp_block = 4 * kst * terms + 12 + ntile * terms
     warps_per_head = w.Dv // 16
     return (w.B * w.Hv * warps_per_head * per_warp_block * 2 * 16 * 8 * 16 * w.S) // 16
@@ -533,18 +533,28 @@ def main(argv=None):
             print(json.dumps({"scan": out}), flush=True)
         return 0
     if args.only == "rect":
-        # the headline workloads with Dk != Dv (same heads, same token counts)
-        rd = DECODE_B64.replace(name="decode_bf16_b64_hk16_hv32_dk128_dv64", Dv=64)
-        dec = bench_decode(gdn, rd, dev, args.steps, args.warmup, world, None)
-        gbs = decode_bytes(rd) / (dec["ms_per_step"] * 1e-3) / 1e9
-        rs = PREFILL_B4.replace(name="prefill_bf16_b4_s4096_hk16_hv32_dk64_dv128", Dk=64)
-        scan = bench_scan(gdn, rs, dev, args.scan_reps, props.multi_processor_count,
-                          peaks["sm_max_mhz"], peaks)
+        # the headline workloads with Dk != Dv (same heads, same token counts), and with head
+        # dims of 256 (half the heads, so twice the state per token)
+        decs = [DECODE_B64.replace(name="decode_bf16_b64_hk16_hv32_dk128_dv64", Dv=64),
+                DECODE_B64.replace(name="decode_bf16_b64_hk8_hv16_d256", Hk=8, Hv=16, Dk=256,
+                                   Dv=256)]
+        scans = [PREFILL_B4.replace(name="prefill_bf16_b4_s4096_hk16_hv32_dk64_dv128", Dk=64),
+                 PREFILL_B4.replace(name="prefill_bf16_b4_s4096_hk8_hv16_d256", Hk=8, Hv=16,
+                                    Dk=256, Dv=256)]
+        lines = []
+        for rd in decs:
+            dec = bench_decode(gdn, rd, dev, args.steps, args.warmup, world, None)
+            gbs = decode_bytes(rd) / (dec["ms_per_step"] * 1e-3) / 1e9
+            lines.append({"config": rd.as_config(), "metric": "decode state HBM GB/s",
+                          "value": gbs, "ms_per_step": dec["ms_per_step"],
+                          "frac_of_measured_hbm": gbs / peaks["hbm_gbs"]})
+            del dec
+            torch.cuda.empty_cache()
+        for rs in scans:
+            lines.append(bench_scan(gdn, rs, dev, args.scan_reps, props.multi_processor_count,
+                                    peaks["sm_max_mhz"], peaks))
         if rank == 0:
-            print(json.dumps({"rect": [
-                {"config": rd.as_config(), "metric": "decode state HBM GB/s", "value": gbs,
-                 "ms_per_step": dec["ms_per_step"], "frac_of_measured_hbm": gbs / peaks["hbm_gbs"]},
-                scan]}), flush=True)
+            print(json.dumps({"rect": lines}), flush=True)
         return 0
 
     sampler = ClockSampler(device_uuid(dev)) if rank == 0 else None

@@ -68,6 +68,12 @@ def test_roofline_byte_and_flop_models():
     assert bench.scan_flops(PREFILL_B4) == 6 * 128 * 128 * 4 * 4096 * 32
     # bf16 block form: per warp and 16-token block 64 (X, Y) + 12 (d, O) + 32 (update) MMAs
     assert bench.scan_mma_flops(PREFILL_B4) == 4 * 32 * 8 * 108 * 4096 * 4096 // 16
+    # Dk != Dv: X, Y run over Dk / 16 k-steps and the update over Dk / 8 n-tiles, on Dv / 16
+    # warps: Dk = 64, Dv = 128 bf16 -> 32 + 12 + 16 MMAs on 8 warps; Dk = 128, Dv = 64 f16
+    # (3 operand terms) -> 96 + 12 + 48 on 4 warps
+    assert bench.scan_mma_flops(PREFILL_B4.replace(Dk=64)) == 4 * 32 * 8 * 60 * 4096 * 4096 // 16
+    assert (bench.scan_mma_flops(PREFILL_B4.replace(Dv=64, act="f16"))
+            == 4 * 32 * 4 * 156 * 4096 * 4096 // 16)
     # tensor-memory chunked kernel: per head and steady chunk 16x32 (tables) + 16x64 ([x|y])
     # + 12x32 (d, O) + 4x128 (update) + 6x64 (correction) = 2816 columns of 128x16 MMAs;
     # the first chunk has no cross table (8x32 fewer), the last no correction (6x64 fewer)

@@ -297,57 +297,31 @@ def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
     """Same metric end to end: every step copies its inputs from pinned host memory, runs the
     C-ABI decode step on the resident state, and reads y back to the host.
 
-    The per-step inputs (q, k, v, z, log_decay, beta) sit in one pinned host buffer and one
-    device buffer (each input 256-byte aligned inside it), so a step is one host-to-device
-    copy, the C-ABI call and one device-to-host copy of y, then a stream synchronize.
+    Through the binding's HostDecodeStep: the per-step inputs (q, k, v, z, log_decay, beta)
+    sit in one pinned host buffer, and a step is one CUDA graph (host-to-device copy of that
+    buffer, the C-ABI decode step, device-to-host copy of y) followed by a stream synchronize.
     """
-    lib = gdn.library()
     inp = make_inputs(w)
     names = ["q", "k", "v", "z", "log_decay", "beta"]
-    offs, off = {}, 0
-    for k in names:
-        offs[k] = off
-        off += (inp[k].numel() * inp[k].element_size() + 255) // 256 * 256
-    h_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
-    d_buf = torch.empty(off, dtype=torch.uint8, device=dev)
-
-    def view(buf, k):
-        n = inp[k].numel() * inp[k].element_size()
-        return buf[offs[k]:offs[k] + n].view(inp[k].dtype).view(inp[k].shape)
-
-    for k in names:
-        view(h_buf, k).copy_(inp[k])
-    d = {k: view(d_buf, k) for k in names}
-    gn = inp["gn"].to(dev)
     state = inp["s0"].to(dev)
-    y = torch.empty(inp["v"].shape, dtype=torch.float32, device=dev)
-    y_host = torch.empty(y.shape, dtype=torch.float32).pin_memory()
-    prm = gdn.make_params(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], state, y,
-                          z=d["z"], gn=gn, head_major=w.head_major)
-    stream = torch.cuda.current_stream(dev)
-    h2d = sum(inp[k].numel() * inp[k].element_size() for k in names)
-    d2h = y_host.numel() * 4
-
-    def step():
-        d_buf.copy_(h_buf, non_blocking=True)
-        st = lib.gdn_decode_step(ctypes.byref(prm), stream.cuda_stream)
-        if st != 0:
-            raise RuntimeError(f"gdn_decode_step failed with status {st}")
-        y_host.copy_(y, non_blocking=True)
-        stream.synchronize()
-
+    gn = inp["gn"].to(dev)
+    stepper = gdn.HostDecodeStep({k: inp[k] for k in names}, state, gn,
+                                 head_major=w.head_major)
+    for k in names:
+        stepper.host[k].copy_(inp[k])
     for _ in range(5):
-        step()
+        stepper.run()
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(steps):
-        step()
+        stepper.run()
     sec = allreduce_max(time.perf_counter() - t0, world, dev)
     return {"value": aggregate_rate(decode_bytes(w), world, sec / steps) / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": 1e3 * sec / steps,
-            "note": "state resident in HBM; per-step inputs from one pinned host buffer (one "
-                    "copy), y read back"}
+            "h2d_bytes_per_step": stepper.h2d_bytes, "d2h_bytes_per_step": stepper.d2h_bytes,
+            "steps": steps, "ms_per_step": 1e3 * sec / steps,
+            "note": "state resident in HBM; per step one CUDA graph (inputs from one pinned "
+                    "host buffer, the decode step, y back to pinned host memory), then a "
+                    "stream synchronize"}
 
 
 # ------------------------------------------------------------------------------ scan

@@ -246,3 +246,86 @@ def gdn_selftest_wait_timeout(limit_ms: float = 1.0, stream=None, device=None) -
 
 def gdn_version() -> int:
     return library().gdn_version()
+
+
+class HostDecodeStep:
+    """A decode step fed from pinned host memory, replayed as one CUDA graph.
+
+    Every :meth:`run` copies the step's inputs (q, k, v, z, log_decay, beta) from one pinned
+    host buffer to one device buffer, runs ``gdn_decode_step`` on the device-resident
+    ``state`` (updated in place) and copies ``y`` back to pinned host memory: three graph
+    nodes, so a step costs one graph launch and one synchronisation instead of three separate
+    launches issued from Python.  Write a step's inputs into the views of :attr:`host` before
+    calling :meth:`run`; the graph reads them at replay time.
+
+    ``like`` holds CPU tensors with the step's shapes and dtypes (S == 1, per ``head_major``);
+    ``z`` and ``gn`` are both given or both omitted (raw o).  Each input starts 256-byte
+    aligned inside the staging buffers.  The object keeps ``state`` and ``gn`` alive (the graph
+    holds their device addresses).
+    """
+
+    NAMES = ("q", "k", "v", "z", "log_decay", "beta")
+
+    def __init__(self, like: dict, state, gn=None, *, head_major=False, qk_eps=1e-6,
+                 norm_eps=1e-6):
+        _require_cuda(state, gn)
+        dev = state.device
+        # the graph holds raw pointers: keep every tensor it reads or writes alive with it
+        self.state, self.gn = state, gn
+        names = [n for n in self.NAMES if like.get(n) is not None]
+        offs, off = {}, 0
+        for n in names:
+            offs[n] = off
+            off += (like[n].numel() * like[n].element_size() + 255) // 256 * 256
+        self._h_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self._d_buf = torch.empty(off, dtype=torch.uint8, device=dev)
+
+        def view(buf, n):
+            nbytes = like[n].numel() * like[n].element_size()
+            return buf[offs[n]:offs[n] + nbytes].view(like[n].dtype).view(like[n].shape)
+
+        self.host = {n: view(self._h_buf, n) for n in names}
+        d = {n: view(self._d_buf, n) for n in names}
+        self.y = torch.empty(like["v"].shape, dtype=torch.float32, device=dev)
+        self.y_host = torch.empty(self.y.shape, dtype=torch.float32).pin_memory()
+        self.h2d_bytes = sum(like[n].numel() * like[n].element_size() for n in names)
+        self.d2h_bytes = self.y_host.numel() * 4
+        self._params = make_params(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], state,
+                                   self.y, z=d.get("z"), gn=gn, head_major=head_major,
+                                   qk_eps=qk_eps, norm_eps=norm_eps)
+        self._lib = library()
+        self._device = dev
+        self._stream = torch.cuda.Stream(dev)
+        self._stream.wait_stream(torch.cuda.current_stream(dev))
+        # One call outside the capture sets the kernel's launch attributes (first use per
+        # device), which must not happen inside it.  It runs the first sequence of zeroed
+        # inputs on a scratch state, so neither ``state`` nor ``y`` changes.
+        with torch.cuda.stream(self._stream):
+            self._d_buf.zero_()
+            one = {n: t[:1] for n, t in d.items()}
+            scratch = torch.zeros((1,) + tuple(state.shape[1:]), dtype=torch.float32, device=dev)
+            y1 = torch.empty((1,) + tuple(self.y.shape[1:]), dtype=torch.float32, device=dev)
+            warm = make_params(one["q"], one["k"], one["v"], one["log_decay"], one["beta"],
+                               scratch, y1, z=one.get("z"), gn=gn, head_major=head_major,
+                               qk_eps=qk_eps, norm_eps=norm_eps)
+            _raise(self._lib, self._lib.gdn_decode_step(ctypes.byref(warm), self._stream.cuda_stream),
+                   warm, 1)
+        self._stream.synchronize()
+        self._graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self._graph, stream=self._stream):
+            self._body()
+
+    def _body(self):
+        self._d_buf.copy_(self._h_buf, non_blocking=True)
+        st = self._lib.gdn_decode_step(ctypes.byref(self._params),
+                                       torch.cuda.current_stream(self._device).cuda_stream)
+        _raise(self._lib, st, self._params, 1)
+        self.y_host.copy_(self.y, non_blocking=True)
+
+    def run(self, sync: bool = True):
+        """Replay the step on the current stream; returns the pinned host ``y`` (valid after
+        the synchronisation, which ``sync=False`` leaves to the caller)."""
+        self._graph.replay()
+        if sync:
+            torch.cuda.current_stream(self._device).synchronize()
+        return self.y_host

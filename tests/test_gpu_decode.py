@@ -79,6 +79,38 @@ def test_tiny_workload_as_eight_decode_steps():
     assert rel_err(state, sr) <= DECODE_TOL
 
 
+@pytest.mark.parametrize("head_major,gated,act", [(False, True, "bf16"), (True, True, "f16"),
+                                                   (False, False, "f32")])
+def test_host_decode_step_graph_over_several_steps(head_major, gated, act):
+    # HostDecodeStep: the step's inputs go from pinned host memory to the device, the decode
+    # step runs on the resident state and y comes back, replayed as one CUDA graph; every step
+    # writes new inputs into the host views, which the graph must read at replay time
+    steps = 5
+    w = small_workload(B=3, S=steps, Hk=2, Hv=4, D=128, act=act, head_major=head_major,
+                       seed=640, s0_std=0.05)
+    inp = make_inputs(w)
+    names = ["q", "k", "v", "log_decay", "beta"] + (["z"] if gated else [])
+    tdim = 2 if head_major else 1                          # the token axis
+    step_in = lambda t: {n: inp[n].narrow(tdim, t, 1).contiguous() for n in names}
+    s0 = inp["s0"].to("cuda")
+    state = s0.clone()
+    gn = inp["gn"].to("cuda") if gated else None
+    stepper = gdn.HostDecodeStep(step_in(0), state, gn, head_major=head_major)
+    torch.cuda.synchronize()
+    assert torch.equal(state, s0)                          # building the graph ran no step
+    assert stepper.h2d_bytes == sum(t.numel() * t.element_size() for t in step_in(0).values())
+    ys = []
+    for t in range(steps):
+        for n, x in step_in(t).items():
+            stepper.host[n].copy_(x)
+        ys.append(stepper.run().clone())
+    yr, sr = oracle_ref(inp, gated=gated, head_major=head_major)
+    # the stepper keeps the tensors its graph points at alive
+    assert stepper.state is state and stepper.gn is gn
+    assert rel_err(torch.cat(ys, tdim), yr) <= DECODE_TOL
+    assert rel_err(state, sr) <= DECODE_TOL
+
+
 SHAPES = [(D, Hk, Hv) for D in (16, 32, 64, 128) for (Hk, Hv) in ((2, 2), (2, 4), (1, 4))]
 
 

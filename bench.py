@@ -294,12 +294,13 @@ def bench_decode(gdn, w: Workload, dev, steps: int, warmup: int, world: int, sam
 
 
 def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
-    """Same metric end to end: every step copies its inputs from pinned host memory, runs the
-    C-ABI decode step on the resident state, and reads y back to the host.
+    """Same metric end to end: every step moves its inputs from pinned host memory to the
+    GPU, runs the C-ABI decode step on the resident state, and brings y back to the host.
 
     Through the binding's HostDecodeStep: the per-step inputs (q, k, v, z, log_decay, beta)
-    sit in one pinned host buffer, and a step is one CUDA graph (host-to-device copy of that
-    buffer, the C-ABI decode step, device-to-host copy of y) followed by a stream synchronize.
+    sit in one pinned host buffer and y in pinned host memory; a step is one C-ABI call with
+    GDN_FLAG_HOST_IO, whose kernel reads the inputs from host memory and writes y there over
+    the chip-to-chip link, then a stream synchronize.
     """
     inp = make_inputs(w)
     names = ["q", "k", "v", "z", "log_decay", "beta"]
@@ -319,9 +320,9 @@ def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
     return {"value": aggregate_rate(decode_bytes(w), world, sec / steps) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": stepper.h2d_bytes, "d2h_bytes_per_step": stepper.d2h_bytes,
             "steps": steps, "ms_per_step": 1e3 * sec / steps,
-            "note": "state resident in HBM; per step one CUDA graph (inputs from one pinned "
-                    "host buffer, the decode step, y back to pinned host memory), then a "
-                    "stream synchronize"}
+            "note": "state resident in HBM; per step one C-ABI call reading the inputs from "
+                    "pinned host memory and writing y to pinned host memory "
+                    "(GDN_FLAG_HOST_IO), then a stream synchronize"}
 
 
 # ------------------------------------------------------------------------------ scan

@@ -29,9 +29,9 @@
  *   f32 even for a 16-bit model).
  *
  * OWNERSHIP
- *   The caller owns every buffer and every pointer is a DEVICE pointer (the stream's device).
- *   The library allocates nothing, keeps no state between calls and never copies to the
- *   host.  Work is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *   The caller owns every buffer and every pointer is a DEVICE pointer (the stream's device),
+ *   except under GDN_FLAG_HOST_IO below.  The library allocates nothing, keeps no state
+ *   between calls and never copies to the host.  Work is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
  *   default stream) and is asynchronous: results are ready when the stream is.
  *
  * ERRORS
@@ -84,6 +84,16 @@ typedef enum {
  *                       other shapes run the default kernel.  Same results within the scan
  *                       tolerance; the default kernel is faster on the reference workloads. */
 #define GDN_FLAG_SCAN_TMEM 1
+/*   GDN_FLAG_HOST_IO    gdn_decode_step only (gdn_scan rejects it): q, k, v, z, log_decay,
+ *                       beta and y may live in pinned host memory that is mapped into the
+ *                       device's address space (cudaHostAlloc, or cudaHostRegister with
+ *                       cudaHostRegisterMapped, under unified addressing: the host address is
+ *                       the device address).  The kernel then reads each head's inputs with
+ *                       plain loads one head ahead and writes y with plain stores, so a step
+ *                       fed from the host needs no separate copies.  state and gn stay in
+ *                       device memory.  Device pointers remain valid with the flag.  Passing
+ *                       memory the device cannot address is a fault, as with any bad pointer. */
+#define GDN_FLAG_HOST_IO 2
 
 /* Operands of one call.  Shape fields follow GDNShape (num_key_heads = Hk, num_value_heads
  * = Hv, key_head_dim = Dk, value_head_dim = Dv) plus batch B and sequence length S. */

@@ -25,6 +25,7 @@ LIBRARY = _build.LIBRARY
 
 GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 GDN_FLAG_SCAN_TMEM = 1          # gdn_params.flags: tensor-memory chunked scan where it applies
+GDN_FLAG_HOST_IO = 2            # gdn_params.flags: decode inputs and y in pinned host memory
 _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
 
 GDN_OK = 0
@@ -177,19 +178,36 @@ def _require_cuda(*tensors):
             raise GdnError(GDN_ERR_BAD_ARG, "all tensors must be CUDA tensors (no CPU path)")
 
 
+def _require_device_addressable(*tensors):
+    # GDN_FLAG_HOST_IO operands: CUDA tensors, or pinned host tensors (mapped into the
+    # device's address space); the kernel reads and writes them, nothing runs on the CPU
+    for t in tensors:
+        if t is not None and not t.is_cuda and not t.is_pinned():
+            raise GdnError(GDN_ERR_BAD_ARG,
+                           "host_io operands must be CUDA tensors or pinned host tensors")
+
+
 def gdn_decode_step(q, k, v, log_decay, beta, state, y=None, *, z=None, gn=None,
-                    head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None):
+                    head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None, host_io=False):
     """One decode token (S == 1); ``state`` [B,Hv,Dv,Dk] f32 is updated in place.
 
-    Returns ``y`` (allocated with v's shape in f32 if not given).
+    Returns ``y`` (allocated with v's shape in f32 if not given: on v's device, or pinned
+    host memory when v is a host tensor).  ``host_io=True`` sets GDN_FLAG_HOST_IO: q, k, v,
+    z, the gates and y may then be pinned host tensors, which the kernel reads and writes
+    directly (state and gn stay CUDA tensors).  The result is ready when the stream is.
     """
-    _require_cuda(q, k, v, log_decay, beta, state, y, z, gn)
+    if host_io:
+        _require_device_addressable(q, k, v, log_decay, beta, y, z)
+        _require_cuda(state, gn)
+    else:
+        _require_cuda(q, k, v, log_decay, beta, state, y, z, gn)
     if y is None:
-        y = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+        y = (torch.empty(v.shape, dtype=torch.float32, device=v.device) if v.is_cuda
+             else torch.empty(v.shape, dtype=torch.float32).pin_memory())
     prm = make_params(q, k, v, log_decay, beta, state, y, z=z, gn=gn, head_major=head_major,
-                      qk_eps=qk_eps, norm_eps=norm_eps)
+                      qk_eps=qk_eps, norm_eps=norm_eps, flags=GDN_FLAG_HOST_IO if host_io else 0)
     lib = library()
-    st = lib.gdn_decode_step(ctypes.byref(prm), _stream_handle(stream, v.device))
+    st = lib.gdn_decode_step(ctypes.byref(prm), _stream_handle(stream, state.device))
     _raise(lib, st, prm, 1)
     return y
 
@@ -249,19 +267,18 @@ def gdn_version() -> int:
 
 
 class HostDecodeStep:
-    """A decode step fed from pinned host memory, replayed as one CUDA graph.
+    """A decode step fed from pinned host memory and returning y to it, with no copies.
 
-    Every :meth:`run` copies the step's inputs (q, k, v, z, log_decay, beta) from one pinned
-    host buffer to one device buffer, runs ``gdn_decode_step`` on the device-resident
-    ``state`` (updated in place) and copies ``y`` back to pinned host memory: three graph
-    nodes, so a step costs one graph launch and one synchronisation instead of three separate
-    launches issued from Python.  Write a step's inputs into the views of :attr:`host` before
-    calling :meth:`run`; the graph reads them at replay time.
+    The step's inputs (q, k, v, z, log_decay, beta) sit in one pinned host buffer (views in
+    :attr:`host`, each input 256-byte aligned) and y in pinned :attr:`y_host`.  :meth:`run`
+    is one C-ABI call with GDN_FLAG_HOST_IO, whose kernel reads each head's inputs from host
+    memory and writes y there, and one stream synchronisation.  Write a step's inputs into
+    :attr:`host` before calling :meth:`run`.
 
-    ``like`` holds CPU tensors with the step's shapes and dtypes (S == 1, per ``head_major``);
-    ``z`` and ``gn`` are both given or both omitted (raw o).  Each input starts 256-byte
-    aligned inside the staging buffers.  The object keeps ``state`` and ``gn`` alive (the graph
-    holds their device addresses).
+    ``like`` holds tensors with the step's shapes and dtypes (S == 1, per ``head_major``);
+    ``z`` and ``gn`` are both given or both omitted (raw o).  ``state`` (updated in place) and
+    ``gn`` are CUDA tensors; the object keeps them alive (its parameter block holds their
+    device addresses).
     """
 
     NAMES = ("q", "k", "v", "z", "log_decay", "beta")
@@ -269,8 +286,6 @@ class HostDecodeStep:
     def __init__(self, like: dict, state, gn=None, *, head_major=False, qk_eps=1e-6,
                  norm_eps=1e-6):
         _require_cuda(state, gn)
-        dev = state.device
-        # the graph holds raw pointers: keep every tensor it reads or writes alive with it
         self.state, self.gn = state, gn
         names = [n for n in self.NAMES if like.get(n) is not None]
         offs, off = {}, 0
@@ -278,54 +293,28 @@ class HostDecodeStep:
             offs[n] = off
             off += (like[n].numel() * like[n].element_size() + 255) // 256 * 256
         self._h_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
-        self._d_buf = torch.empty(off, dtype=torch.uint8, device=dev)
 
-        def view(buf, n):
+        def view(n):
             nbytes = like[n].numel() * like[n].element_size()
-            return buf[offs[n]:offs[n] + nbytes].view(like[n].dtype).view(like[n].shape)
+            return self._h_buf[offs[n]:offs[n] + nbytes].view(like[n].dtype).view(like[n].shape)
 
-        self.host = {n: view(self._h_buf, n) for n in names}
-        d = {n: view(self._d_buf, n) for n in names}
-        self.y = torch.empty(like["v"].shape, dtype=torch.float32, device=dev)
-        self.y_host = torch.empty(self.y.shape, dtype=torch.float32).pin_memory()
+        self.host = {n: view(n) for n in names}
+        self.y_host = torch.empty(like["v"].shape, dtype=torch.float32).pin_memory()
         self.h2d_bytes = sum(like[n].numel() * like[n].element_size() for n in names)
         self.d2h_bytes = self.y_host.numel() * 4
-        self._params = make_params(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], state,
-                                   self.y, z=d.get("z"), gn=gn, head_major=head_major,
-                                   qk_eps=qk_eps, norm_eps=norm_eps)
+        h = self.host
+        self._params = make_params(h["q"], h["k"], h["v"], h["log_decay"], h["beta"], state,
+                                   self.y_host, z=h.get("z"), gn=gn, head_major=head_major,
+                                   qk_eps=qk_eps, norm_eps=norm_eps, flags=GDN_FLAG_HOST_IO)
         self._lib = library()
-        self._device = dev
-        self._stream = torch.cuda.Stream(dev)
-        self._stream.wait_stream(torch.cuda.current_stream(dev))
-        # One call outside the capture sets the kernel's launch attributes (first use per
-        # device), which must not happen inside it.  It runs the first sequence of zeroed
-        # inputs on a scratch state, so neither ``state`` nor ``y`` changes.
-        with torch.cuda.stream(self._stream):
-            self._d_buf.zero_()
-            one = {n: t[:1] for n, t in d.items()}
-            scratch = torch.zeros((1,) + tuple(state.shape[1:]), dtype=torch.float32, device=dev)
-            y1 = torch.empty((1,) + tuple(self.y.shape[1:]), dtype=torch.float32, device=dev)
-            warm = make_params(one["q"], one["k"], one["v"], one["log_decay"], one["beta"],
-                               scratch, y1, z=one.get("z"), gn=gn, head_major=head_major,
-                               qk_eps=qk_eps, norm_eps=norm_eps)
-            _raise(self._lib, self._lib.gdn_decode_step(ctypes.byref(warm), self._stream.cuda_stream),
-                   warm, 1)
-        self._stream.synchronize()
-        self._graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self._graph, stream=self._stream):
-            self._body()
+        self._device = state.device
 
-    def _body(self):
-        self._d_buf.copy_(self._h_buf, non_blocking=True)
-        st = self._lib.gdn_decode_step(ctypes.byref(self._params),
-                                       torch.cuda.current_stream(self._device).cuda_stream)
+    def run(self, sync: bool = True, stream=None):
+        """One step on ``stream`` (default: the current stream); returns :attr:`y_host`, valid
+        once the stream has completed (``sync=True`` waits for it here)."""
+        handle = _stream_handle(stream, self._device)
+        st = self._lib.gdn_decode_step(ctypes.byref(self._params), handle)
         _raise(self._lib, st, self._params, 1)
-        self.y_host.copy_(self.y, non_blocking=True)
-
-    def run(self, sync: bool = True):
-        """Replay the step on the current stream; returns the pinned host ``y`` (valid after
-        the synchronisation, which ``sync=False`` leaves to the caller)."""
-        self._graph.replay()
         if sync:
-            torch.cuda.current_stream(self._device).synchronize()
+            (stream or torch.cuda.current_stream(self._device)).synchronize()
         return self.y_host

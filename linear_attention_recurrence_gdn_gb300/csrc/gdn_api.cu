@@ -47,9 +47,16 @@ bool supported_dim(int d) { return (d >= 16 && d <= 128 && d % 16 == 0) || d == 
 int check(const gdn_params *p, int is_decode, const char **why) {
     *why = nullptr;
     if (p == nullptr) { *why = "params pointer is NULL"; return GDN_ERR_NULL_PTR; }
-    if ((p->flags & ~GDN_FLAG_SCAN_TMEM) != 0) { *why = "unknown flags bit"; return GDN_ERR_BAD_ARG; }
-    if (is_decode && p->flags != 0) {
+    if ((p->flags & ~(GDN_FLAG_SCAN_TMEM | GDN_FLAG_HOST_IO)) != 0) {
+        *why = "unknown flags bit";
+        return GDN_ERR_BAD_ARG;
+    }
+    if (is_decode && (p->flags & GDN_FLAG_SCAN_TMEM)) {
         *why = "flags: GDN_FLAG_SCAN_TMEM applies to gdn_scan only";
+        return GDN_ERR_BAD_ARG;
+    }
+    if (!is_decode && (p->flags & GDN_FLAG_HOST_IO)) {
+        *why = "flags: GDN_FLAG_HOST_IO applies to gdn_decode_step only";
         return GDN_ERR_BAD_ARG;
     }
     if (p->B < 0 || p->S < 0) { *why = "B and S must be >= 0"; return GDN_ERR_BAD_SHAPE; }

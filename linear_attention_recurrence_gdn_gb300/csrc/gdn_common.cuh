@@ -14,36 +14,56 @@ namespace gdn {
 
 template <typename T> struct Act;
 
+// one(p), four(p): one element / four consecutive elements (4*sizeof(T)-byte aligned) as f32.
+// raw1 / raw4 load the same elements as their stored bits and cvt1 / cvt4 widen them, so a
+// load can be issued well before the value is needed.
 template <> struct Act<float> {
-    __device__ __forceinline__ static float one(const float *p) { return *p; }
-    // four consecutive elements, 4*sizeof(T)-byte aligned
-    __device__ __forceinline__ static float4 four(const float *p) {
+    using R1 = float;
+    using R4 = float4;
+    __device__ __forceinline__ static R1 raw1(const float *p) { return *p; }
+    __device__ __forceinline__ static R4 raw4(const float *p) {
         return *reinterpret_cast<const float4 *>(p);
     }
+    __device__ __forceinline__ static float cvt1(R1 r) { return r; }
+    __device__ __forceinline__ static float4 cvt4(R4 r) { return r; }
+    __device__ __forceinline__ static float one(const float *p) { return *p; }
+    __device__ __forceinline__ static float4 four(const float *p) { return raw4(p); }
 };
 
 template <> struct Act<__nv_bfloat16> {
-    __device__ __forceinline__ static float one(const __nv_bfloat16 *p) {
-        return __bfloat162float(*p);
+    using R1 = __nv_bfloat16;
+    using R4 = uint2;
+    __device__ __forceinline__ static R1 raw1(const __nv_bfloat16 *p) { return *p; }
+    __device__ __forceinline__ static R4 raw4(const __nv_bfloat16 *p) {
+        return *reinterpret_cast<const uint2 *>(p);
     }
-    __device__ __forceinline__ static float4 four(const __nv_bfloat16 *p) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    __device__ __forceinline__ static float cvt1(R1 r) { return __bfloat162float(r); }
+    __device__ __forceinline__ static float4 cvt4(R4 raw) {
         const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
         const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
         const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
         return make_float4(a.x, a.y, b.x, b.y);
     }
+    __device__ __forceinline__ static float one(const __nv_bfloat16 *p) { return cvt1(*p); }
+    __device__ __forceinline__ static float4 four(const __nv_bfloat16 *p) { return cvt4(raw4(p)); }
 };
 
 template <> struct Act<__half> {
-    __device__ __forceinline__ static float one(const __half *p) { return __half2float(*p); }
-    __device__ __forceinline__ static float4 four(const __half *p) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    using R1 = __half;
+    using R4 = uint2;
+    __device__ __forceinline__ static R1 raw1(const __half *p) { return *p; }
+    __device__ __forceinline__ static R4 raw4(const __half *p) {
+        return *reinterpret_cast<const uint2 *>(p);
+    }
+    __device__ __forceinline__ static float cvt1(R1 r) { return __half2float(r); }
+    __device__ __forceinline__ static float4 cvt4(R4 raw) {
         const __half2 lo = *reinterpret_cast<const __half2 *>(&raw.x);
         const __half2 hi = *reinterpret_cast<const __half2 *>(&raw.y);
         const float2 a = __half22float2(lo), b = __half22float2(hi);
         return make_float4(a.x, a.y, b.x, b.y);
     }
+    __device__ __forceinline__ static float one(const __half *p) { return cvt1(*p); }
+    __device__ __forceinline__ static float4 four(const __half *p) { return cvt4(raw4(p)); }
 };
 
 // Gate scalars (log_decay, beta) are either f32 or the activation dtype: a runtime switch

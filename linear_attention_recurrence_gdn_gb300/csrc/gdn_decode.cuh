@@ -136,7 +136,11 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
     float *xo = reinterpret_cast<float *>(smem + C::XO_OFF);
 
     const bool gated = p.z != nullptr;
-    const unsigned tx = STATE * 4 + 2 * DK * sizeof(TA) + (gated ? 2 : 1) * RBK * sizeof(TA);
+    // host_io: q, k, v, z (and the gates, y) may be in mapped host memory; the threads stage
+    // the inputs with plain loads (below) and the stage copies carry the state only
+    const bool host_io = (p.flags & GDN_FLAG_HOST_IO) != 0;
+    const unsigned tx =
+        STATE * 4 + (host_io ? 0u : 2 * DK * sizeof(TA) + (gated ? 2 : 1) * RBK * sizeof(TA));
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane / L;                              // row within a warp-wide access
@@ -187,13 +191,13 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
                     cp_async16(dst + off, src + off);
                 }
             constexpr int QP = DK * sizeof(TA) / 16, VP = RBK * sizeof(TA) / 16;
-            for (int t = tid; t < QP; t += C::NT) {
+            for (int t = tid; t < (host_io ? 0 : QP); t += C::NT) {
                 cp_async16(reinterpret_cast<char *>(q_s + s * DK) + 16 * t,
                            reinterpret_cast<const char *>(static_cast<const TA *>(p.q) + qo) + 16 * t);
                 cp_async16(reinterpret_cast<char *>(k_s + s * DK) + 16 * t,
                            reinterpret_cast<const char *>(static_cast<const TA *>(p.k) + qo) + 16 * t);
             }
-            for (int t = tid; t < VP; t += C::NT) {
+            for (int t = tid; t < (host_io ? 0 : VP); t += C::NT) {
                 cp_async16(reinterpret_cast<char *>(v_s + s * RBK) + 16 * t,
                            reinterpret_cast<const char *>(static_cast<const TA *>(p.v) + vo) + 16 * t);
                 if (gated)
@@ -220,6 +224,7 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
 #pragma unroll
         for (int j = 0; j < SPLIT; j++)
             bulk_g2s(st_s + s * STATE + j * PIECE, src + j * PIECE, PIECE * 4, &bar[s]);
+        if (host_io) return;
         bulk_g2s(q_s + s * DK, static_cast<const TA *>(p.q) + qo, DK * sizeof(TA), &bar[s]);
         bulk_g2s(k_s + s * DK, static_cast<const TA *>(p.k) + qo, DK * sizeof(TA), &bar[s]);
         bulk_g2s(v_s + s * RBK, static_cast<const TA *>(p.v) + vo, RBK * sizeof(TA), &bar[s]);
@@ -229,6 +234,64 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
     if (tid == 0)
         for (int64_t u = 0; u < nunits && u < NST; u++) issue(u, static_cast<int>(u));
 #endif
+
+    // host_io: the q, k, v, z rows of a unit travel as 16-byte pieces, loaded by the threads in
+    // turn two units ahead and stored into the unit's stage one unit ahead (its previous unit
+    // has consumed that stage by then); the loop-top barrier orders the stores before the reads
+    constexpr int QP = DK * sizeof(TA) / 16, VP = RBK * sizeof(TA) / 16;
+    constexpr int PPT = (2 * QP + 2 * VP + C::NT - 1) / C::NT;   // pieces per thread, at most
+    const int npieces = 2 * QP + (gated ? 2 : 1) * VP;
+    uint4 held[PPT];
+    auto piece = [&](int64_t u, int i, int s, const uint4 *&src, uint4 *&dst) {
+        const int64_t h = head_of(u / NRBK);
+        const int rb = static_cast<int>(u % NRBK);
+        const int b = static_cast<int>(h / p.Hv);
+        const int hk = static_cast<int>(h - static_cast<int64_t>(b) * p.Hv) / group;
+        const int64_t qo = (static_cast<int64_t>(b) * p.Hk + hk) * DK;
+        const int64_t vo = h * DV + rb * RBK;
+        if (i < QP) {
+            src = reinterpret_cast<const uint4 *>(static_cast<const TA *>(p.q) + qo) + i;
+            dst = reinterpret_cast<uint4 *>(q_s + s * DK) + i;
+        } else if (i < 2 * QP) {
+            src = reinterpret_cast<const uint4 *>(static_cast<const TA *>(p.k) + qo) + (i - QP);
+            dst = reinterpret_cast<uint4 *>(k_s + s * DK) + (i - QP);
+        } else if (i < 2 * QP + VP) {
+            src = reinterpret_cast<const uint4 *>(static_cast<const TA *>(p.v) + vo) + (i - 2 * QP);
+            dst = reinterpret_cast<uint4 *>(v_s + s * RBK) + (i - 2 * QP);
+        } else {
+            src = reinterpret_cast<const uint4 *>(static_cast<const TA *>(p.z) + vo) + (i - 2 * QP - VP);
+            dst = reinterpret_cast<uint4 *>(z_s + s * RBK) + (i - 2 * QP - VP);
+        }
+    };
+    auto load_pieces = [&](int64_t u) {
+#pragma unroll
+        for (int j = 0; j < PPT; j++) {
+            const int i = tid + j * C::NT;
+            if (i < npieces) {
+                const uint4 *src;
+                uint4 *dst;
+                piece(u, i, 0, src, dst);
+                held[j] = *src;
+            }
+        }
+    };
+    auto store_pieces = [&](int64_t u) {
+#pragma unroll
+        for (int j = 0; j < PPT; j++) {
+            const int i = tid + j * C::NT;
+            if (i < npieces) {
+                const uint4 *src;
+                uint4 *dst;
+                piece(u, i, static_cast<int>(u % NST), src, dst);
+                *dst = held[j];
+            }
+        }
+    };
+    if (host_io && nunits > 0) {
+        load_pieces(0);
+        store_pieces(0);
+        if (nunits > 1) load_pieces(1);
+    }
 
     // gates of the next head are prefetched one head ahead into registers
     float gl = 0.f, gb = 0.f, alpha = 0.f, beta = 0.f;
@@ -289,6 +352,10 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
             zr[r] = gated ? A::one(z_s + s * RBK + row0 + r * RPS) : 0.f;
         }
         __syncthreads();                                 // stage s consumed by every thread
+        if (host_io) {                                   // next unit's inputs into its stage
+            if (u + 1 < nunits) store_pieces(u + 1);
+            if (u + 2 < nunits) load_pieces(u + 2);
+        }
 #if !GDN_DECODE_LATE_ISSUE
 #if GDN_DECODE_LDGSTS
         issue(u + NST, s);

@@ -105,6 +105,8 @@ def test_valid_params_have_no_reject_reason(lib):
     st = BASE + 8 * GAP
     assert reject(lib, fake_params(s0=st, state=st), 0) is None         # in-place resume
     assert reject(lib, fake_params(gate_dtype=gdn.GDN_BF16), 0) is None
+    assert reject(lib, fake_params(S=1, flags=gdn.GDN_FLAG_HOST_IO), 1) is None
+    assert reject(lib, fake_params(flags=gdn.GDN_FLAG_SCAN_TMEM), 0) is None
     # empty sequence: empty tensors may come as NULL pointers, nothing is read or written
     assert reject(lib, fake_params(S=0, y=None, q=None, k=None, v=None, z=None, log_decay=None,
                                    beta=None), 0) is None
@@ -135,8 +137,10 @@ REJECTIONS = [
     (dict(norm_eps=float("nan")), 0, gdn.GDN_ERR_BAD_ARG, "eps"),
     (dict(norm_eps=float("inf")), 0, gdn.GDN_ERR_BAD_ARG, "eps"),
     (dict(head_major=2), 0, gdn.GDN_ERR_BAD_ARG, "head_major"),
-    (dict(flags=2), 0, gdn.GDN_ERR_BAD_ARG, "unknown flags"),
+    (dict(flags=4), 0, gdn.GDN_ERR_BAD_ARG, "unknown flags"),
+    (dict(S=1, flags=8), 1, gdn.GDN_ERR_BAD_ARG, "unknown flags"),
     (dict(S=1, flags=gdn.GDN_FLAG_SCAN_TMEM), 1, gdn.GDN_ERR_BAD_ARG, "gdn_scan only"),
+    (dict(flags=gdn.GDN_FLAG_HOST_IO), 0, gdn.GDN_ERR_BAD_ARG, "gdn_decode_step only"),
     (dict(B=1 << 20, S=1 << 20), 0, gdn.GDN_ERR_BAD_ARG, "too large"),
     (dict(state=None), 0, gdn.GDN_ERR_NULL_PTR, "state and y"),
     (dict(S=1, y=None), 1, gdn.GDN_ERR_NULL_PTR, "state and y"),
@@ -193,6 +197,15 @@ def test_binding_rejects_cpu_tensors_and_noncontiguous():
     with pytest.raises(gdn.GdnError, match="contiguous"):
         gdn.make_params(t, t, t, torch.zeros(1, 2, 1), torch.zeros(1, 2, 1),
                         torch.zeros(1, 1, 16, 16), torch.zeros(1, 1, 1, 16))
+
+
+def test_binding_host_io_refuses_unpinned_host_tensors():
+    # GDN_FLAG_HOST_IO operands must be device-addressable: CUDA tensors or pinned host
+    # memory; ordinary (pageable) CPU tensors are refused before any CUDA call
+    q = torch.zeros(1, 1, 1, 16)
+    with pytest.raises(gdn.GdnError, match="pinned"):
+        gdn.gdn_decode_step(q, q, q, torch.zeros(1, 1, 1), torch.zeros(1, 1, 1),
+                            torch.zeros(1, 1, 16, 16), host_io=True)
 
 
 def test_binding_shape_and_dtype_checks():

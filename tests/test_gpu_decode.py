@@ -81,10 +81,10 @@ def test_tiny_workload_as_eight_decode_steps():
 
 @pytest.mark.parametrize("head_major,gated,act", [(False, True, "bf16"), (True, True, "f16"),
                                                    (False, False, "f32")])
-def test_host_decode_step_graph_over_several_steps(head_major, gated, act):
-    # HostDecodeStep: the step's inputs go from pinned host memory to the device, the decode
-    # step runs on the resident state and y comes back, replayed as one CUDA graph; every step
-    # writes new inputs into the host views, which the graph must read at replay time
+def test_host_decode_step_over_several_steps(head_major, gated, act):
+    # HostDecodeStep: the kernel reads the step's inputs from pinned host memory and writes y
+    # to pinned host memory (GDN_FLAG_HOST_IO) on the device-resident state; every step writes
+    # new inputs into the host views, which the next call must read
     steps = 5
     w = small_workload(B=3, S=steps, Hk=2, Hv=4, D=128, act=act, head_major=head_major,
                        seed=640, s0_std=0.05)
@@ -97,7 +97,7 @@ def test_host_decode_step_graph_over_several_steps(head_major, gated, act):
     gn = inp["gn"].to("cuda") if gated else None
     stepper = gdn.HostDecodeStep(step_in(0), state, gn, head_major=head_major)
     torch.cuda.synchronize()
-    assert torch.equal(state, s0)                          # building the graph ran no step
+    assert torch.equal(state, s0)                          # construction runs no step
     assert stepper.h2d_bytes == sum(t.numel() * t.element_size() for t in step_in(0).values())
     ys = []
     for t in range(steps):
@@ -109,6 +109,54 @@ def test_host_decode_step_graph_over_several_steps(head_major, gated, act):
     assert stepper.state is state and stepper.gn is gn
     assert rel_err(torch.cat(ys, tdim), yr) <= DECODE_TOL
     assert rel_err(state, sr) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("placement", ["inputs_host", "y_host", "all_host"])
+@pytest.mark.parametrize("dims", [(128, 128), (64, 256), (256, 80)], ids=lambda d: f"{d[0]}x{d[1]}")
+def test_decode_host_io_placements(placement, dims):
+    # GDN_FLAG_HOST_IO accepts pinned host memory and device memory in any mix; several steps,
+    # including heads cut into row blocks (Dv = 256 with Dk = 64 is one 64 KB unit; Dk = 256,
+    # Dv = 80 five units of 16 rows)
+    Dk, Dv = dims
+    steps = 3
+    w = small_workload(B=5, S=steps, Hk=2, Hv=4, Dk=Dk, Dv=Dv, act="bf16", seed=650 + Dv,
+                       s0_std=0.05)
+    inp = make_inputs(w)
+    state = inp["s0"].to("cuda")
+    gn = inp["gn"].to("cuda")
+    host_in = placement in ("inputs_host", "all_host")
+    host_y = placement in ("y_host", "all_host")
+    ys = []
+    for t in range(steps):
+        sl = {n: inp[n][:, t:t + 1].contiguous() for n in ("q", "k", "v", "z", "log_decay", "beta")}
+        sl = {n: (x.pin_memory() if host_in else x.to("cuda")) for n, x in sl.items()}
+        y = (torch.empty(sl["v"].shape, dtype=torch.float32).pin_memory() if host_y
+             else torch.empty(sl["v"].shape, dtype=torch.float32, device="cuda"))
+        gdn.gdn_decode_step(sl["q"], sl["k"], sl["v"], sl["log_decay"], sl["beta"], state, y,
+                            z=sl["z"], gn=gn, host_io=True)
+        torch.cuda.synchronize()
+        ys.append(y.cpu().clone())
+    yr, sr = oracle_ref(inp)
+    assert rel_err(torch.cat(ys, 1), yr) <= DECODE_TOL
+    assert rel_err(state, sr) <= DECODE_TOL
+
+
+def test_decode_host_io_many_heads_matches_device_path():
+    # every CTA runs several heads: the pieces staged one unit ahead must follow the heads of
+    # a CTA's range; bit-identical to the device-memory path (same kernel arithmetic)
+    w = DECODE_B64.replace(B=20)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    st_dev = d["s0"].clone()
+    y_dev = gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st_dev,
+                                z=d["z"], gn=d["gn"])
+    h = {n: inp[n].contiguous().pin_memory() for n in ("q", "k", "v", "z", "log_decay", "beta")}
+    st_host = d["s0"].clone()
+    y_host = gdn.gdn_decode_step(h["q"], h["k"], h["v"], h["log_decay"], h["beta"], st_host,
+                                 z=h["z"], gn=d["gn"], host_io=True)
+    torch.cuda.synchronize()
+    assert not y_host.is_cuda and y_host.is_pinned()
+    assert torch.equal(y_host, y_dev.cpu()) and torch.equal(st_host, st_dev)
 
 
 SHAPES = [(D, Hk, Hv) for D in (16, 32, 64, 128) for (Hk, Hv) in ((2, 2), (2, 4), (1, 4))]

@@ -820,7 +820,9 @@ cudaError_t launch_tc_dv(const gdn_params &p, cudaStream_t stream) {
             case 64: return launch_tc_best<TA, DK, 64, 4>(p, stream);
             case 80: return launch_tc_best<TA, DK, 80, 5>(p, stream);
             case 96: return launch_tc_best<TA, DK, 96, 6>(p, stream);
-            case 112: return launch_tc_best<TA, DK, 112, 7>(p, stream);
+            case 112:   // f32 rows of 128 with 7 row warps exceed the shared-memory limit
+                if constexpr (sizeof(TA) == 4) return launch_tc_best<TA, DK, 112, 7, 1>(p, stream);
+                else return launch_tc_best<TA, DK, 112, 7>(p, stream);
             case 128: return launch_tc_best<TA, DK, 128, 8, 4, 2>(p, stream);
             case 256: return launch_tc_best<TA, DK, 256, 8, 4>(p, stream);
             default: return cudaErrorInvalidValue;

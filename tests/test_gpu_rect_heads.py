@@ -44,6 +44,7 @@ SCAN_CASES = [
     (1, 40, 1, 2, 80, 96, "bf16", True),
     (1, 64, 2, 4, 96, 96, "bf16", False),
     (1, 37, 1, 1, 112, 128, "f16", False),   # Dv = 128 with an odd Dk: the split-head path
+    (1, 40, 1, 2, 128, 112, "f32", False),   # 7 row warps of f32 rows do not fit: 7 CTAs
     # head dims of 256
     (1, 40, 1, 2, 256, 256, "bf16", False),   # 4 row warps, a cluster of 4 CTAs per head
     (2, 33, 1, 2, 256, 128, "f16", True),

@@ -309,12 +309,12 @@ class HostDecodeStep:
         self._lib = library()
         self._device = state.device
 
-    def run(self, sync: bool = True, stream=None):
-        """One step on ``stream`` (default: the current stream); returns :attr:`y_host`, valid
-        once the stream has completed (``sync=True`` waits for it here)."""
-        handle = _stream_handle(stream, self._device)
-        st = self._lib.gdn_decode_step(ctypes.byref(self._params), handle)
+    def run(self, sync: bool = True, stream: torch.cuda.Stream | None = None):
+        """One step on ``stream`` (a torch CUDA stream; default: the current stream); returns
+        :attr:`y_host`, valid once the stream has completed (``sync=True`` waits here)."""
+        s = stream if stream is not None else torch.cuda.current_stream(self._device)
+        st = self._lib.gdn_decode_step(ctypes.byref(self._params), s.cuda_stream)
         _raise(self._lib, st, self._params, 1)
         if sync:
-            (stream or torch.cuda.current_stream(self._device)).synchronize()
+            s.synchronize()
         return self.y_host

@@ -27,7 +27,9 @@
 //   * row dot products reduce over the L lanes of the row with xor shuffles (log2 L stages);
 //   * q^, k^ are normalised in registers (the same lane layout, so the norm sums also reduce
 //     over L lanes); k^.q^ is one scalar per head, as the page notes;
-//   * the updated rows go straight from registers to global memory (coalesced float4 stores).
+//   * the updated rows go from the registers back into their stage in shared memory and out to
+//     HBM as one bulk copy per unit (TMA), which leaves the load/store units to the
+//     shared-memory traffic; the stage is refilled once that copy has read it.
 #pragma once
 
 #include <math.h>
@@ -81,6 +83,16 @@ constexpr int decode_rows(int dk, int dv) {
 #endif
 #ifndef GDN_DECODE_MINB
 #define GDN_DECODE_MINB 1
+#endif
+//   GDN_DECODE_BULK_STORE  1: updated rows go back into the stage and out by one bulk copy per
+//                          unit, the stage refilled at the next unit's start; 0: float4 stores
+//                          from the registers.  Measured on GB300 (B = 32 / 64 / 256): 5351 /
+//                          5877 / 6591 GB/s against 5340 / 5860 / 6584
+#ifndef GDN_DECODE_BULK_STORE
+#define GDN_DECODE_BULK_STORE 1
+#endif
+#if GDN_DECODE_BULK_STORE && (GDN_DECODE_LDGSTS || !GDN_DECODE_LATE_ISSUE)
+#error "GDN_DECODE_BULK_STORE needs the TMA copies and the late reissue"
 #endif
 //   GDN_DECODE_CONTIG_MAX  most heads per CTA for which a CTA takes a contiguous range of heads
 #ifndef GDN_DECODE_CONTIG_MAX
@@ -307,6 +319,12 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
         const int64_t i = u / NRBK;
         const int rb = static_cast<int>(u % NRBK);
         const int64_t h = head_of(i);
+#if GDN_DECODE_BULK_STORE
+        if (tid == 0 && u >= 1) {          // the previous unit's store has read its stage
+            bulk_wait_read_all();
+            if (u - 1 + NST < nunits) issue(u - 1 + NST, static_cast<int>((u - 1) % NST));
+        }
+#endif
         if (rb == 0) {
             alpha = expf(gl);
             beta = gb;
@@ -323,9 +341,13 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
         // wait for stage s; a timed-out wait (watchdog set) ends the whole CTA together
         const bool ok = mbar_wait_bounded(&bar[s], static_cast<unsigned>((u / NST) & 1));
         if (__syncthreads_or(!ok)) {
-            if (tid == 0)   // let this CTA's copies still in flight land before leaving
+            if (tid == 0) { // let this CTA's copies still in flight land before leaving
                 for (int64_t j = u; j < nunits && j < u + NST; j++)
                     mbar_wait_bounded(&bar[j % NST], static_cast<unsigned>((j / NST) & 1));
+#if GDN_DECODE_BULK_STORE
+                bulk_wait_all();
+#endif
+            }
             return;
         }
 #endif
@@ -351,7 +373,9 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
             vr[r] = A::one(v_s + s * RBK + row0 + r * RPS);
             zr[r] = gated ? A::one(z_s + s * RBK + row0 + r * RPS) : 0.f;
         }
+#if !GDN_DECODE_BULK_STORE
         __syncthreads();                                 // stage s consumed by every thread
+#endif
         if (host_io) {                                   // next unit's inputs into its stage
             if (u + 1 < nunits) store_pieces(u + 1);
             if (u + 2 < nunits) load_pieces(u + 2);
@@ -384,8 +408,14 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
         }
         const float kq = skq * rk * rq;                  // k^ . q^, one scalar per head
 
-        // 3. fused pass per row: u, w from the registers, updated row straight to HBM
+        // 3. fused pass per row: u, w from the registers, updated row straight to HBM (or back
+        //    into the stage, for one bulk copy of the unit)
         float *Sg = p.state + h * (static_cast<int64_t>(DV) * DK) + rb * STATE;
+#if GDN_DECODE_BULK_STORE
+        float *Sw = st_s + s * STATE;
+#else
+        float *Sw = Sg;
+#endif
         float o[R];
 #pragma unroll
         for (int r = 0; r < R; r++) {
@@ -398,7 +428,7 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
             pu = group_sum<L>(pu);
             pw = group_sum<L>(pw);
             const float coef = beta * (vr[r] - alpha * pu);
-            float *row = Sg + (row0 + r * RPS) * DK;
+            float *row = Sw + (row0 + r * RPS) * DK;
 #pragma unroll
             for (int c = 0; c < NV; c++) {
                 float4 n;
@@ -411,7 +441,14 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
             o[r] = fmaf(alpha, pw, coef * kq);
         }
 
-#if GDN_DECODE_LATE_ISSUE
+#if GDN_DECODE_BULK_STORE
+        fence_async_smem_writes();
+        __syncthreads();                                 // the unit's rows are in stage s
+        if (tid == 0) {
+            bulk_s2g(Sg, st_s + s * STATE, STATE * 4);
+            bulk_commit();
+        }
+#elif GDN_DECODE_LATE_ISSUE
 #if GDN_DECODE_LDGSTS
         issue(u + NST, s);
 #else
@@ -465,6 +502,9 @@ gdn_decode_kernel(const gdn_params p, int64_t nheads, int64_t per) {
             for (int r = 0; r < R; r++) yp[row0 + r * RPS] = o[r];
         }
     }
+#if GDN_DECODE_BULK_STORE
+    if (tid == 0) bulk_wait_all();                       // shared memory outlives the stores
+#endif
 }
 
 constexpr int kMaxDevices = 64;

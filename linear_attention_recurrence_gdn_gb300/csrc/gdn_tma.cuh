@@ -80,6 +80,29 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
         : "memory");
 }
 
+// One contiguous shared -> global bulk copy, tracked by the issuing thread's bulk groups;
+// `bytes` a multiple of 16, both addresses 16-byte aligned.  The writes to the shared source
+// must be made visible to the async proxy first (fence_async_smem_writes, then a barrier).
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, unsigned bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Every committed bulk store of this thread has finished reading its shared source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed bulk store of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem_writes() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 16-byte global -> shared copy through the LSU (cp.async), grouped by commit/wait.
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem)

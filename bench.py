@@ -113,20 +113,45 @@ def load_peaks() -> dict:
                 "bf16_tflops": FALLBACK_BF16_TFLOPS, "sm_max_mhz": MAX_SM_MHZ_FALLBACK}
 
 
-def profiled_traffic(kernel_file: str, summary: str):
-    """DRAM bytes per launch recorded by an ncu capture, if the kernel source is unchanged.
+def code_hash(source: str) -> str:
+    """sha256 of C/C++/CUDA source with its comments and all whitespace removed: the hash
+    changes with the code, not with its comments or layout."""
+    out, i, n = [], 0, len(source)
+    while i < n:
+        if source.startswith("//", i):
+            j = source.find("\n", i)
+            i = n if j < 0 else j
+        elif source.startswith("/*", i):
+            j = source.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif source[i] == '"':                     # string literal, kept verbatim
+            j = i + 1
+            while j < n and source[j] != '"':
+                j += 2 if source[j] == "\\" else 1
+            out.append(source[i:j + 1])
+            i = j + 1
+        else:
+            if not source[i].isspace():
+                out.append(source[i])
+            i += 1
+    return hashlib.sha256("".join(out).encode()).hexdigest()
 
-    ``summary`` (under profiles/) holds lines ``source_sha256: <hex>`` and
-    ``dram_bytes_per_launch: <int>``; a hash mismatch means the counters are stale -> None.
+
+def profiled_traffic(kernel_file: str, summary: str):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel code is unchanged.
+
+    ``summary`` (under profiles/) holds lines ``code_sha256: <hex>`` (``code_hash`` of the
+    kernel source) and ``dram_bytes_per_launch: <int>``; a mismatch means the counters are
+    stale -> None.
     """
     try:
         text = open(os.path.join(ROOT, "profiles", summary)).read()
         src = open(os.path.join(ROOT, "linear_attention_recurrence_gdn_gb300", "csrc",
-                                kernel_file), "rb").read()
+                                kernel_file)).read()
     except OSError:
         return None
     fields = dict(line.split(":", 1) for line in text.splitlines() if ":" in line)
-    if fields.get("source_sha256", "").strip() != hashlib.sha256(src).hexdigest():
+    if fields.get("code_sha256", "").strip() != code_hash(src):
         return None
     try:
         return int(fields["dram_bytes_per_launch"].strip())

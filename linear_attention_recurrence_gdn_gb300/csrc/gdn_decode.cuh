@@ -3,9 +3,9 @@
 // Algorithm: logicaffeine_compile::codegen_cuda::gdn, "The fusion": because the update is
 // affine in S, o[a] = alpha (S_old q^)[a] + coef[a] (k^ . q^) with coef[a] = beta (v[a] -
 // alpha u[a]), so one pass over a state row gives u[a] = S_old[a,:] k^ and w[a] = S_old[a,:] q^,
-// and the updated row alpha S_old[a,:] + coef[a] k^ is written back from the registers that
-// already hold it.  The gated RMSNorm (GDN_KERNELS: "needs the whole head") runs in the same
-// CTA because one CTA owns a whole head at a time, so there is no second kernel and o never
+// and the updated row alpha S_old[a,:] + coef[a] k^ is formed in the registers that already
+// hold it.  The gated RMSNorm (GDN_KERNELS: "needs the whole head") runs in the same CTA
+// because one CTA owns a whole head at a time, so there is no second kernel and o never
 // round-trips through memory.
 //
 // GB300 mapping (differs from the page's one-block-per-(head, row) launch):
@@ -13,9 +13,8 @@
 //     heads (up to 32 heads per CTA; measured faster there) or heads c, c + grid, ...
 //     A unit's state (64 KB), its q, k, v and z rows arrive in shared memory by bulk
 //     asynchronous copies (TMA, cp.async.bulk) that complete on an mbarrier; NST stages keep
-//     the next head's copy in flight while the current head is computed.  Measured on GB300:
-//     two stages, the next copy issued right after the current head's rows are written back,
-//     beat deeper prefetch -- the state is updated in place, and HBM serves an in-place
+//     the next unit's copy in flight while the current one is computed.  Measured on GB300:
+//     two stages beat three -- the state is updated in place, and HBM serves an in-place
 //     stream best when a row's write follows its read closely;
 //   * a unit of work is a head, or for heads of more than 64 KB of state (a head dim of 256)
 //     a block of its rows; a head's units run back to back on one CTA, and the gated RMSNorm

@@ -61,6 +61,15 @@ def test_single_rank_helpers_are_identity():
     bench.barrier(1)
 
 
+def test_code_hash_ignores_comments_and_layout_not_code():
+    # the traffic record of profiles/ stays valid across comment edits, not code edits
+    a = 'int x = 1; // note\n/* block\n comment */ int  y=2;\nconst char *s = "a // b";'
+    b = 'int x=1;\nint y = 2; // other note\nconst char *s = "a // b";'
+    assert bench.code_hash(a) == bench.code_hash(b)
+    assert bench.code_hash(a) != bench.code_hash(a.replace("y=2", "y=3"))
+    assert bench.code_hash(a) != bench.code_hash(a.replace('"a // b"', '"a "'))
+
+
 def test_roofline_byte_and_flop_models():
     from linear_attention_recurrence_gdn_gb300.workloads import DECODE_B64, PREFILL_B4
     # 8 B per state element (read + write) dominates; the closed form of the bench's docstring

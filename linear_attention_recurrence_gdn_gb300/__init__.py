@@ -40,8 +40,9 @@ GDN_ERR_CUDA = -8
 GDN_ERR_TIMEOUT = -9
 
 # Symbols declared in include/gdn.h (checked by the tests against the header).
-EXPORTED = ("gdn_decode_step", "gdn_scan", "gdn_reject_reason", "gdn_status_string",
-            "gdn_last_error", "gdn_device_status", "gdn_selftest_wait_timeout", "gdn_version")
+EXPORTED = ("gdn_decode_step", "gdn_scan", "gdn_scan_split", "gdn_scan_split_workspace",
+            "gdn_reject_reason", "gdn_status_string", "gdn_last_error", "gdn_device_status",
+            "gdn_selftest_wait_timeout", "gdn_version")
 
 
 class GdnParams(ctypes.Structure):
@@ -83,6 +84,11 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.gdn_decode_step.restype = ctypes.c_int
     lib.gdn_scan.argtypes = [P, ctypes.c_void_p]
     lib.gdn_scan.restype = ctypes.c_int
+    lib.gdn_scan_split.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                   ctypes.c_void_p]
+    lib.gdn_scan_split.restype = ctypes.c_int
+    lib.gdn_scan_split_workspace.argtypes = [P, ctypes.c_int]
+    lib.gdn_scan_split_workspace.restype = ctypes.c_size_t
     lib.gdn_reject_reason.argtypes = [P, ctypes.c_int]
     lib.gdn_reject_reason.restype = ctypes.c_char_p
     lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -237,6 +243,41 @@ def gdn_scan(q, k, v, log_decay, beta, state=None, y=None, *, s0=None, z=None, g
     st = lib.gdn_scan(ctypes.byref(prm), _stream_handle(stream, v.device))
     _raise(lib, st, prm, 0)
     return y, state
+
+
+def gdn_scan_split(q, k, v, log_decay, beta, state=None, y=None, *, segments, s0=None, z=None,
+                   gn=None, head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None,
+                   workspace=None):
+    """``gdn_scan`` with the sequence cut into ``segments`` ranges run in parallel (for batches
+    with few heads).  Returns ``(y, state)`` like ``gdn_scan``.  ``workspace``: a CUDA tensor of
+    at least ``gdn_scan_split_workspace`` bytes (allocated here when None).
+    """
+    _require_cuda(q, k, v, log_decay, beta, state, y, z, gn, s0, workspace)
+    if head_major:
+        B, Hk, S, Dk = q.shape
+        Hv, Dv = v.shape[1], v.shape[3]
+    else:
+        B, S, Hk, Dk = q.shape
+        Hv, Dv = v.shape[2], v.shape[3]
+    if y is None:
+        y = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+    if state is None:
+        state = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=v.device)
+    prm = make_params(q, k, v, log_decay, beta, state, y, z=z, gn=gn, s0=s0,
+                      head_major=head_major, qk_eps=qk_eps, norm_eps=norm_eps)
+    lib = library()
+    need = lib.gdn_scan_split_workspace(ctypes.byref(prm), int(segments))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=v.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.gdn_scan_split(ctypes.byref(prm), int(segments), _ptr(workspace), nbytes,
+                            _stream_handle(stream, v.device))
+    _raise(lib, st, prm, 0)
+    return y, state
+
+
+def gdn_scan_split_workspace(params: GdnParams, segments: int) -> int:
+    return library().gdn_scan_split_workspace(ctypes.byref(params), int(segments))
 
 
 def gdn_reject_reason(params: GdnParams, is_decode: bool) -> str | None:

@@ -143,6 +143,35 @@ int check(const gdn_params *p, int is_decode, const char **why) {
     return GDN_OK;
 }
 
+// gdn_scan_split's own arguments (after check(p, 0) passed).
+int check_split(const gdn_params *p, int segments, const void *ws, size_t ws_bytes,
+                const char **why) {
+    *why = nullptr;
+    if (segments < 1) { *why = "segments must be >= 1"; return GDN_ERR_BAD_ARG; }
+    if (p->flags & GDN_FLAG_SCAN_TMEM) {
+        *why = "flags: GDN_FLAG_SCAN_TMEM applies to gdn_scan only";
+        return GDN_ERR_BAD_ARG;
+    }
+    const size_t need = gdn::scan_split_workspace_floats(*p, segments) * sizeof(float);
+    if (p->B == 0 || need == 0) return GDN_OK;             // one segment: no workspace used
+    if (ws == nullptr) { *why = "workspace is required"; return GDN_ERR_NULL_PTR; }
+    if (!aligned(ws, 16)) { *why = "workspace must be 16-byte aligned"; return GDN_ERR_MISALIGNED; }
+    if (ws_bytes < need) { *why = "workspace too small (see gdn_scan_split_workspace)"; return GDN_ERR_BAD_ARG; }
+    const int64_t B = p->B, S = p->S, Hk = p->Hk, Hv = p->Hv, Dk = p->Dk, Dv = p->Dv;
+    const int64_t eact = dtype_bytes(p->act_dtype), egate = dtype_bytes(p->gate_dtype);
+    const int64_t n_qk = B * S * Hk * Dk, n_v = B * S * Hv * Dv, n_g = B * S * Hv;
+    const int64_t n_state = B * Hv * Dv * Dk;
+    const Range rw{reinterpret_cast<uintptr_t>(ws), reinterpret_cast<uintptr_t>(ws) + need};
+    const Range all[] = {span(p->q, n_qk, eact),         span(p->k, n_qk, eact),
+                         span(p->v, n_v, eact),          span(p->z, n_v, eact),
+                         span(p->log_decay, n_g, egate), span(p->beta, n_g, egate),
+                         span(p->gn, Dv, 4),             span(p->s0, n_state, 4),
+                         span(p->state, n_state, 4),     span(p->y, n_v, 4)};
+    for (const Range &r : all)
+        if (overlaps(rw, r)) { *why = "workspace overlaps an operand"; return GDN_ERR_ALIASING; }
+    return GDN_OK;
+}
+
 int cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return GDN_OK;
     snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
@@ -174,6 +203,27 @@ int gdn_scan(const gdn_params *p, void *stream) {
         return cuda_status(cudaMemsetAsync(p->state, 0, bytes, s));
     }
     return cuda_status(gdn::launch_scan(*p, s));
+}
+
+size_t gdn_scan_split_workspace(const gdn_params *p, int segments) {
+    const char *why;
+    if (check(p, 0, &why) != GDN_OK || segments < 1 || p->B == 0) return 0;
+    return gdn::scan_split_workspace_floats(*p, segments) * sizeof(float);
+}
+
+int gdn_scan_split(const gdn_params *p, int segments, void *workspace, size_t workspace_bytes,
+                   void *stream) {
+    const char *why;
+    int st = check(p, 0, &why);
+    if (st != GDN_OK) return st;
+    st = check_split(p, segments, workspace, workspace_bytes, &why);
+    if (st != GDN_OK) {
+        snprintf(g_last_error, sizeof g_last_error, "%s", why);
+        return st;
+    }
+    if (p->B == 0 || p->S == 0) return gdn_scan(p, stream);
+    return cuda_status(gdn::launch_scan_split(*p, segments, static_cast<float *>(workspace),
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 const char *gdn_reject_reason(const gdn_params *p, int is_decode) {

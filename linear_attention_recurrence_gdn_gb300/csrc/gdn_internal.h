@@ -29,17 +29,40 @@ cudaError_t launch_wait_timeout(cudaStream_t stream, uint64_t limit_ns);
 // Multi-token scan (S >= 1): state resident on chip across the time axis.
 cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
 
+// A scan launch over segments of the sequence.  The plain scan is one segment of S tokens in
+// mode 0 with no per-segment buffers.  Segment g covers tokens [g * seg_len, min(S, (g + 1) *
+// seg_len)); its CTAs are blocks [g * B*Hv*CTAs-per-head, ...) of the grid.
+//   mode 0: each segment from its start memory (s0_seg[g], or p.s0 when s0_seg is NULL),
+//           writing y; the last segment writes the final memory to p.state;
+//   mode 1: each segment's transition M = prod_t alpha_t (I - beta_t k^_t k^_t^T): the rows of
+//           the identity carried through the update with v = 0 (p.Dv == p.Dk), into
+//           state_seg[g]; no y;
+//   mode 2: each segment's offset N (its end memory from zeros), into state_seg[g]; no y.
+struct ScanSplit {
+    int nseg;              // segments in this launch
+    int seg_len;           // tokens per segment (the last one may be shorter)
+    int mode;
+    const float *s0_seg;   // mode 0: [nseg][B*Hv][Dv][Dk] start memories, or NULL
+    float *state_seg;      // modes 1, 2: [nseg][B*Hv][Dv][Dk] end memories
+};
+
+// The sequence-split scan: transitions and offsets of segments 0 .. nseg-2 in parallel, their
+// composition into every segment's start memory, then every segment's outputs in parallel.
+// `ws` holds gdn_scan_split_workspace() bytes.
+cudaError_t launch_scan_split(const gdn_params &p, int nseg, float *ws, cudaStream_t stream);
+size_t scan_split_workspace_floats(const gdn_params &p, int nseg);
+
 // The scan on tensor cores, one translation unit per key head dim (gdn_scan_tc_dk*.cu), and
 // each unit's watchdog word (read and cleared; synchronises `stream`).
-cudaError_t launch_scan_tc_dk16(const gdn_params &p, cudaStream_t stream);
-cudaError_t launch_scan_tc_dk32(const gdn_params &p, cudaStream_t stream);
-cudaError_t launch_scan_tc_dk48(const gdn_params &p, cudaStream_t stream);
-cudaError_t launch_scan_tc_dk64(const gdn_params &p, cudaStream_t stream);
-cudaError_t launch_scan_tc_dk80(const gdn_params &p, cudaStream_t stream);
-cudaError_t launch_scan_tc_dk96(const gdn_params &p, cudaStream_t stream);
-cudaError_t launch_scan_tc_dk112(const gdn_params &p, cudaStream_t stream);
-cudaError_t launch_scan_tc_dk128(const gdn_params &p, cudaStream_t stream);
-cudaError_t launch_scan_tc_dk256(const gdn_params &p, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk16(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk32(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk48(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk64(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk80(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk96(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk112(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk128(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
+cudaError_t launch_scan_tc_dk256(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
 cudaError_t scan_watchdog_dk16(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk32(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk48(unsigned *flag, cudaStream_t stream);

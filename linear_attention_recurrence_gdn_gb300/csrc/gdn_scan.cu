@@ -1,28 +1,142 @@
-// gdn_scan.cu -- the scan entry behind gdn_scan().
+// gdn_scan.cu -- the scan entries behind gdn_scan() and gdn_scan_split().
 //
 // The recurrence and the gated RMSNorm run in the tensor-core kernel of gdn_scan_tc.cuh,
 // instantiated per key head dim in gdn_scan_tc_dk*.cu: the norm, which couples all Dv rows of a
 // head (logicaffeine_compile::codegen_cuda::gdn, GDN_KERNELS: "needs the whole head"), is
 // applied by the CTA that owns the head, or by the cluster of CTAs a head's rows are split
 // over.
+//
+// Sequence split.  The page's update is affine in the memory (codegen_cuda::gdn, "The fusion"):
+// S_t = S_{t-1} A_t + B_t with A_t = alpha_t (I - beta_t k^_t k^_t^T) and B_t = beta_t v_t k^_t^T.
+// Over a segment of tokens, then, S_end = S_start M + N with M = A_1 ... A_T (the memory that
+// the identity becomes with v = 0) and N = sum_t B_t A_{t+1} ... A_T (the memory reached from
+// zeros).  Segments run in parallel twice: once for M and N, once for the outputs from each
+// segment's start, which a short sequential composition provides in between.
+#include <algorithm>
+
 #include "gdn_internal.h"
 
 namespace gdn {
 
-cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
-    if ((p.flags & GDN_FLAG_SCAN_TMEM) && scan_umma_supported(p)) return launch_scan_umma(p, stream);
+namespace {
+
+cudaError_t launch_scan_dk(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
     switch (p.Dk) {
-        case 16: return launch_scan_tc_dk16(p, stream);
-        case 32: return launch_scan_tc_dk32(p, stream);
-        case 48: return launch_scan_tc_dk48(p, stream);
-        case 64: return launch_scan_tc_dk64(p, stream);
-        case 80: return launch_scan_tc_dk80(p, stream);
-        case 96: return launch_scan_tc_dk96(p, stream);
-        case 112: return launch_scan_tc_dk112(p, stream);
-        case 128: return launch_scan_tc_dk128(p, stream);
-        case 256: return launch_scan_tc_dk256(p, stream);
+        case 16: return launch_scan_tc_dk16(p, sp, stream);
+        case 32: return launch_scan_tc_dk32(p, sp, stream);
+        case 48: return launch_scan_tc_dk48(p, sp, stream);
+        case 64: return launch_scan_tc_dk64(p, sp, stream);
+        case 80: return launch_scan_tc_dk80(p, sp, stream);
+        case 96: return launch_scan_tc_dk96(p, sp, stream);
+        case 112: return launch_scan_tc_dk112(p, sp, stream);
+        case 128: return launch_scan_tc_dk128(p, sp, stream);
+        case 256: return launch_scan_tc_dk256(p, sp, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// Start memories of every segment: St[0] = s0 (zeros when NULL), St[g+1] = St[g] M_g + N_g.
+// The rows of a memory are independent, so CTA (head, 16-row block) composes its own rows
+// through all segments; its rows of St[g] stay in shared memory between steps.
+__global__ void __launch_bounds__(256)
+gdn_scan_compose_kernel(const float *s0, const float *M, const float *N, float *St, int64_t bh,
+                        int dv, int dk, int nseg) {
+    extern __shared__ float cur[];                         // [16][dk]
+    const int64_t head = blockIdx.x;
+    const int r0 = blockIdx.y * 16;
+    const int tid = threadIdx.x;
+    const int n = 16 * dk;                                 // outputs of this CTA per step
+    const int64_t mem = static_cast<int64_t>(dv) * dk;
+    for (int o = tid; o < n; o += blockDim.x) {
+        const float v0 = s0 ? s0[head * mem + static_cast<int64_t>(r0) * dk + o] : 0.f;
+        cur[o] = v0;
+        St[head * mem + static_cast<int64_t>(r0) * dk + o] = v0;
+    }
+    for (int g = 0; g + 1 < nseg; g++) {
+        const float *Mg = M + (static_cast<int64_t>(g) * bh + head) * dk * dk;
+        const float *Ng = N + (static_cast<int64_t>(g) * bh + head) * mem + static_cast<int64_t>(r0) * dk;
+        float *Sn = St + (static_cast<int64_t>(g + 1) * bh + head) * mem + static_cast<int64_t>(r0) * dk;
+        __syncthreads();                                   // cur holds St[g]
+        float acc[16];                                     // n / blockDim.x <= 16 (dk <= 256)
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const int o = tid + j * 256;
+            if (o >= n) break;
+            const int r = o / dk, c = o - r * dk;
+            float a = Ng[o];
+            for (int i = 0; i < dk; i++) a = fmaf(cur[r * dk + i], Mg[static_cast<int64_t>(i) * dk + c], a);
+            acc[j] = a;
+        }
+        __syncthreads();                                   // every read of St[g] done
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const int o = tid + j * 256;
+            if (o >= n) break;
+            cur[o] = acc[j];
+            Sn[o] = acc[j];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
+    if ((p.flags & GDN_FLAG_SCAN_TMEM) && scan_umma_supported(p)) return launch_scan_umma(p, stream);
+    const ScanSplit whole{1, p.S, 0, nullptr, nullptr};
+    return launch_scan_dk(p, whole, stream);
+}
+
+// Segments of ceil(S / nseg) tokens (no empty segment).
+static int seg_len_of(int S, int nseg) { return (S + nseg - 1) / nseg; }
+static int nseg_of(int S, int nseg) {
+    const int len = seg_len_of(S, nseg);
+    return (S + len - 1) / len;
+}
+
+size_t scan_split_workspace_floats(const gdn_params &p, int nseg) {
+    if (p.S < 1 || nseg < 1) return 0;
+    const int g = nseg_of(p.S, nseg);
+    if (g < 2) return 0;
+    const size_t bh = static_cast<size_t>(p.B) * p.Hv;
+    const size_t m = bh * p.Dk * p.Dk, nn = bh * p.Dv * p.Dk;
+    return (g - 1) * m + (g - 1) * nn + g * nn;            // M, N of all but the last; all starts
+}
+
+cudaError_t launch_scan_split(const gdn_params &p, int nseg, float *ws, cudaStream_t stream) {
+    const int len = seg_len_of(p.S, nseg);
+    const int g = nseg_of(p.S, nseg);
+    if (g < 2) return launch_scan(p, stream);
+    const int64_t bh = static_cast<int64_t>(p.B) * p.Hv;
+    float *M = ws;                                         // [g-1][bh][Dk][Dk]
+    float *N = M + (g - 1) * bh * p.Dk * p.Dk;             // [g-1][bh][Dv][Dk]
+    float *St = N + (g - 1) * bh * p.Dv * p.Dk;            // [g][bh][Dv][Dk]
+    cudaError_t e;
+    // 1. transitions of segments 0 .. g-2: the identity (Dk rows) through the update, v = 0
+    gdn_params pm = p;
+    pm.Dv = p.Dk;
+    pm.z = nullptr;
+    pm.gn = nullptr;
+    pm.y = nullptr;
+    pm.s0 = nullptr;
+    pm.flags = 0;
+    if ((e = launch_scan_dk(pm, ScanSplit{g - 1, len, 1, nullptr, M}, stream)) != cudaSuccess) return e;
+    // 2. offsets of segments 0 .. g-2: from zeros with the real v
+    gdn_params pn = p;
+    pn.z = nullptr;
+    pn.gn = nullptr;
+    pn.y = nullptr;
+    pn.s0 = nullptr;
+    pn.flags = 0;
+    if ((e = launch_scan_dk(pn, ScanSplit{g - 1, len, 2, nullptr, N}, stream)) != cudaSuccess) return e;
+    // 3. every segment's start memory
+    const int smem = 16 * p.Dk * static_cast<int>(sizeof(float));
+    gdn_scan_compose_kernel<<<dim3(static_cast<unsigned>(bh), p.Dv / 16), 256, smem, stream>>>(
+        p.s0, M, N, St, bh, p.Dv, p.Dk, g);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 4. outputs of every segment; the last writes the final memory
+    gdn_params po = p;
+    po.flags = 0;
+    return launch_scan_dk(po, ScanSplit{g, len, 0, St, nullptr}, stream);
 }
 
 cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {

@@ -154,7 +154,7 @@ enum { kBarFull0 = 1, kBarEmpty0 = 3, kBarProd = 5 };
 
 template <typename TA, int DK, int DV, int NW>
 __global__ void __launch_bounds__(TcCfg<TA, DK, DV, NW>::NT, 1)
-gdn_scan_tc_kernel(const gdn_params p) {
+gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
     using C = TcCfg<TA, DK, DV, NW>;
     using A = Act<TA>;
     using Sm = TcSmem<TA, DK, DV, NW>;
@@ -164,27 +164,41 @@ gdn_scan_tc_kernel(const gdn_params p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Sm &sm = *reinterpret_cast<Sm *>(smem_raw);
 
-    const int64_t head = blockIdx.x / C::NRB;              // b * Hv + hv
-    const int rblk = blockIdx.x % C::NRB;
+    // segment seg of the sequence (one segment for the plain scan), then head and row block
+    const int64_t per_seg = static_cast<int64_t>(p.B) * p.Hv * C::NRB;
+    const int seg = static_cast<int>(blockIdx.x / per_seg);
+    const int64_t local = blockIdx.x - seg * per_seg;
+    const int64_t head = local / C::NRB;                   // b * Hv + hv
+    const int rblk = static_cast<int>(local % C::NRB);
     const int b = static_cast<int>(head / p.Hv);
     const int hv = static_cast<int>(head - static_cast<int64_t>(b) * p.Hv);
     const int hk = hv / (p.Hv / p.Hk);
     const int r0 = rblk * RB;                              // first memory row of this CTA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tq = lane & 3;                // MMA fragment coordinates
-    const int S = p.S;
+    const int S_full = p.S;                                // strides follow the whole sequence
+    const int t_begin = seg * sp.seg_len;                  // this segment's first token
+    const int S = min(sp.seg_len, S_full - t_begin);       // and its length (>= 1)
     const int nchunks = (S + kT - 1) / kT;
+    const bool v_zero = sp.mode == 1;                      // transition: v = 0, start = identity
 
     int64_t k_base, k_ts, v_base, v_ts, g_base, g_ts;
     if (p.head_major) {
-        k_base = (static_cast<int64_t>(b) * p.Hk + hk) * S * DK;  k_ts = DK;
-        v_base = head * S * DV;                                   v_ts = DV;
-        g_base = head * S;                                       g_ts = 1;
+        k_base = (static_cast<int64_t>(b) * p.Hk + hk) * S_full * DK;  k_ts = DK;
+        v_base = head * S_full * DV;                                   v_ts = DV;
+        g_base = head * S_full;                                       g_ts = 1;
     } else {
-        k_base = (static_cast<int64_t>(b) * S * p.Hk + hk) * DK;  k_ts = static_cast<int64_t>(p.Hk) * DK;
-        v_base = (static_cast<int64_t>(b) * S * p.Hv + hv) * DV;  v_ts = static_cast<int64_t>(p.Hv) * DV;
-        g_base = static_cast<int64_t>(b) * S * p.Hv + hv;        g_ts = p.Hv;
+        k_base = (static_cast<int64_t>(b) * S_full * p.Hk + hk) * DK;  k_ts = static_cast<int64_t>(p.Hk) * DK;
+        v_base = (static_cast<int64_t>(b) * S_full * p.Hv + hv) * DV;  v_ts = static_cast<int64_t>(p.Hv) * DV;
+        g_base = static_cast<int64_t>(b) * S_full * p.Hv + hv;        g_ts = p.Hv;
     }
+    k_base += t_begin * k_ts;
+    v_base += t_begin * v_ts;
+    g_base += t_begin * g_ts;
+    // offset of this (segment, head) in the per-segment memories of a split scan
+    auto seg_head = [&]() {
+        return (static_cast<int64_t>(seg) * p.B * p.Hv + head) * (DV * DK);
+    };
     // gated RMSNorm in this kernel: over the CTA when it owns the whole head, else over the
     // cluster of the head's NRB CTAs (partial sums exchanged through distributed shared memory)
     const bool fused_norm = p.z != nullptr;
@@ -209,13 +223,22 @@ gdn_scan_tc_kernel(const gdn_params p) {
         // sacc[j] = S[wrow+g][8j+2tq], S[wrow+g][8j+2tq+1], S[wrow+g+8][8j+2tq], S[..+8][..+1]
         float sacc[NTILE][4];
         {
-            const float *s0 = p.s0 ? p.s0 + head * (DV * DK) + static_cast<int64_t>(r0 + wrow) * DK : nullptr;
+            // start memory: the caller's s0 (plain scan), the segment's start, zeros or the
+            // identity (transition)
+            const float *s0_src = sp.mode != 0 ? nullptr
+                                  : sp.s0_seg ? sp.s0_seg + seg_head()
+                                  : p.s0 ? p.s0 + head * (DV * DK) : nullptr;
+            const float *s0 = s0_src ? s0_src + static_cast<int64_t>(r0 + wrow) * DK : nullptr;
 #pragma unroll
             for (int j = 0; j < NTILE; j++) {
                 float2 lo = make_float2(0.f, 0.f), hi = lo;
                 if (s0) {
                     lo = *reinterpret_cast<const float2 *>(s0 + g * DK + 8 * j + 2 * tq);
                     hi = *reinterpret_cast<const float2 *>(s0 + (g + 8) * DK + 8 * j + 2 * tq);
+                } else if (v_zero) {                       // the identity (rows = key dims)
+                    const int row = r0 + wrow + g, col = 8 * j + 2 * tq;
+                    lo = make_float2(row == col ? 1.f : 0.f, row == col + 1 ? 1.f : 0.f);
+                    hi = make_float2(row + 8 == col ? 1.f : 0.f, row + 8 == col + 1 ? 1.f : 0.f);
                 }
                 sacc[j][0] = lo.x; sacc[j][1] = lo.y; sacc[j][2] = hi.x; sacc[j][3] = hi.y;
             }
@@ -271,7 +294,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
                         const int rr = g + ((e & 2) ? 8 : 0);
                         const int t = 8 * nt8 + 2 * tq + (e & 1);
                         const float4 cs = sm.cst[hb][tb + t];
-                        const float vv = A::one(&sm.vr[vs][tb + t][wrow + rr]);
+                        const float vv = v_zero ? 0.f : A::one(&sm.vr[vs][tb + t][wrow + rr]);
                         ra[nt8][e] = (t < nb) ? cs.x * (vv - lam * cs.y * xa[nt8][e]) : 0.f;
                         oa[nt8][e] = lam * cs.z * ya[nt8][e];
                     }
@@ -362,8 +385,11 @@ gdn_scan_tc_kernel(const gdn_params p) {
             }
             bar_arrive(kBarEmpty0 + hb, NT);               // slots of chunk ch handed back
         }
-        // final memory rows (undo the deferred decay)
-        float *so = p.state + head * (DV * DK) + static_cast<int64_t>(r0 + wrow) * DK;
+        // final memory rows (undo the deferred decay): the caller's state for the plain scan
+        // and the last segment, the per-segment end memory for transitions and offsets
+        if (sp.mode == 0 && seg != sp.nseg - 1) return;    // a segment before the last
+        float *state_dst = sp.mode != 0 ? sp.state_seg + seg_head() : p.state + head * (DV * DK);
+        float *so = state_dst + static_cast<int64_t>(r0 + wrow) * DK;
 #pragma unroll
         for (int j = 0; j < NTILE; j++) {
             *reinterpret_cast<float2 *>(so + g * DK + 8 * j + 2 * tq) =
@@ -404,6 +430,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
         }
     };
     auto issue_vz = [&](int c) {
+        if (v_zero && !fused_norm) return;                 // a transition reads neither v nor z
         const int t0 = c * kT, nt = min(kT, S - t0);
         const int vs = c % C::NVZ;
         for (int i = ptid; i < nt * C::VPIECES; i += PT) {
@@ -433,6 +460,7 @@ gdn_scan_tc_kernel(const gdn_params p) {
                             : make_float4(0.f, 0.f, 0.f, 0.f);
     const float inv_d = 1.0f / static_cast<float>(DV);
     auto emit = [&](int c) {
+        if (p.y == nullptr) return;                        // transitions and offsets: no y
         const int hb = c & 1, vs = c % C::NVZ;
         const int t0 = c * kT, nt = min(kT, S - t0);
         if (fused_norm) {
@@ -748,10 +776,10 @@ cudaError_t prepare_tc(int *occupancy) {
 }
 
 template <typename TA, int DK, int DV, int NW>
-cudaError_t launch_tc_cfg(const gdn_params &p, cudaStream_t stream) {
+cudaError_t launch_tc_cfg(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
     using C = TcCfg<TA, DK, DV, NW>;
     const int bytes = static_cast<int>(sizeof(TcSmem<TA, DK, DV, NW>));
-    const int64_t ctas = static_cast<int64_t>(p.B) * p.Hv * C::NRB;
+    const int64_t ctas = static_cast<int64_t>(p.B) * p.Hv * C::NRB * sp.nseg;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(C::NT);
@@ -766,7 +794,7 @@ cudaError_t launch_tc_cfg(const gdn_params &p, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gdn_scan_tc_kernel<TA, DK, DV, NW>, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gdn_scan_tc_kernel<TA, DK, DV, NW>, p, sp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -782,14 +810,14 @@ inline int device_sms() {
 // busiest SM with every CTA resident at once (a sequential scan must not run in waves); ties go
 // to the larger CTA.  A candidate whose shared memory exceeds this device's limit is skipped.
 template <typename TA, int DK, int DV, int... NWS>
-cudaError_t launch_tc_best(const gdn_params &p, cudaStream_t stream) {
+cudaError_t launch_tc_best(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
     constexpr int n = sizeof...(NWS);
     constexpr int nws[n] = {NWS...};
     cudaError_t (*const prep[n])(int *) = {prepare_tc<TA, DK, DV, NWS>...};
-    cudaError_t (*const launch[n])(const gdn_params &, cudaStream_t) = {
+    cudaError_t (*const launch[n])(const gdn_params &, const ScanSplit &, cudaStream_t) = {
         launch_tc_cfg<TA, DK, DV, NWS>...};
     const int sms = std::max(1, device_sms());
-    const int64_t heads = static_cast<int64_t>(p.B) * p.Hv;
+    const int64_t heads = static_cast<int64_t>(p.B) * p.Hv * sp.nseg;   // (segment, head) pairs
     int best = -1;
     int64_t best_cost = INT64_MAX;
     for (int i = 0; i < n; i++) {
@@ -804,40 +832,40 @@ cudaError_t launch_tc_best(const gdn_params &p, cudaStream_t stream) {
         if (cost < best_cost) { best_cost = cost; best = i; }
     }
     if (best < 0) return cudaErrorInvalidConfiguration;
-    return launch[best](p, stream);
+    return launch[best](p, sp, stream);
 }
 
 // Value head dims: multiples of 16 up to 128, and 256.  Up to Dk = 128 a CTA takes a whole head
 // of Dv <= 112 (Dv / 16 row warps); Dv = 128 and 256 choose their rows per CTA.  Dk = 256 runs
 // at most 4 row warps per CTA, so a head of more rows is split over a cluster of CTAs.
 template <typename TA, int DK>
-cudaError_t launch_tc_dv(const gdn_params &p, cudaStream_t stream) {
+cudaError_t launch_tc_dv(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
     if constexpr (DK <= 128) {
         switch (p.Dv) {
-            case 16: return launch_tc_best<TA, DK, 16, 1>(p, stream);
-            case 32: return launch_tc_best<TA, DK, 32, 2>(p, stream);
-            case 48: return launch_tc_best<TA, DK, 48, 3>(p, stream);
-            case 64: return launch_tc_best<TA, DK, 64, 4>(p, stream);
-            case 80: return launch_tc_best<TA, DK, 80, 5>(p, stream);
-            case 96: return launch_tc_best<TA, DK, 96, 6>(p, stream);
+            case 16: return launch_tc_best<TA, DK, 16, 1>(p, sp, stream);
+            case 32: return launch_tc_best<TA, DK, 32, 2>(p, sp, stream);
+            case 48: return launch_tc_best<TA, DK, 48, 3>(p, sp, stream);
+            case 64: return launch_tc_best<TA, DK, 64, 4>(p, sp, stream);
+            case 80: return launch_tc_best<TA, DK, 80, 5>(p, sp, stream);
+            case 96: return launch_tc_best<TA, DK, 96, 6>(p, sp, stream);
             case 112:   // f32 rows of 128 with 7 row warps exceed the shared-memory limit
-                if constexpr (sizeof(TA) == 4) return launch_tc_best<TA, DK, 112, 7, 1>(p, stream);
-                else return launch_tc_best<TA, DK, 112, 7>(p, stream);
-            case 128: return launch_tc_best<TA, DK, 128, 8, 4, 2>(p, stream);
-            case 256: return launch_tc_best<TA, DK, 256, 8, 4>(p, stream);
+                if constexpr (sizeof(TA) == 4) return launch_tc_best<TA, DK, 112, 7, 1>(p, sp, stream);
+                else return launch_tc_best<TA, DK, 112, 7>(p, sp, stream);
+            case 128: return launch_tc_best<TA, DK, 128, 8, 4, 2>(p, sp, stream);
+            case 256: return launch_tc_best<TA, DK, 256, 8, 4>(p, sp, stream);
             default: return cudaErrorInvalidValue;
         }
     } else {
         switch (p.Dv) {
-            case 16: return launch_tc_best<TA, DK, 16, 1>(p, stream);
-            case 32: return launch_tc_best<TA, DK, 32, 2>(p, stream);
-            case 48: return launch_tc_best<TA, DK, 48, 3>(p, stream);
-            case 64: return launch_tc_best<TA, DK, 64, 4>(p, stream);
-            case 80: return launch_tc_best<TA, DK, 80, 1>(p, stream);
-            case 96: return launch_tc_best<TA, DK, 96, 3>(p, stream);
-            case 112: return launch_tc_best<TA, DK, 112, 1>(p, stream);
-            case 128: return launch_tc_best<TA, DK, 128, 4, 2>(p, stream);
-            case 256: return launch_tc_best<TA, DK, 256, 4, 2>(p, stream);
+            case 16: return launch_tc_best<TA, DK, 16, 1>(p, sp, stream);
+            case 32: return launch_tc_best<TA, DK, 32, 2>(p, sp, stream);
+            case 48: return launch_tc_best<TA, DK, 48, 3>(p, sp, stream);
+            case 64: return launch_tc_best<TA, DK, 64, 4>(p, sp, stream);
+            case 80: return launch_tc_best<TA, DK, 80, 1>(p, sp, stream);
+            case 96: return launch_tc_best<TA, DK, 96, 3>(p, sp, stream);
+            case 112: return launch_tc_best<TA, DK, 112, 1>(p, sp, stream);
+            case 128: return launch_tc_best<TA, DK, 128, 4, 2>(p, sp, stream);
+            case 256: return launch_tc_best<TA, DK, 256, 4, 2>(p, sp, stream);
             default: return cudaErrorInvalidValue;
         }
     }
@@ -845,11 +873,11 @@ cudaError_t launch_tc_dv(const gdn_params &p, cudaStream_t stream) {
 
 // Every activation type and value head dim for one key head dim.
 template <int DK>
-cudaError_t launch_tc_dk(const gdn_params &p, cudaStream_t stream) {
+cudaError_t launch_tc_dk(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
     switch (p.act_dtype) {
-        case GDN_F32: return launch_tc_dv<float, DK>(p, stream);
-        case GDN_BF16: return launch_tc_dv<__nv_bfloat16, DK>(p, stream);
-        case GDN_F16: return launch_tc_dv<__half, DK>(p, stream);
+        case GDN_F32: return launch_tc_dv<float, DK>(p, sp, stream);
+        case GDN_BF16: return launch_tc_dv<__nv_bfloat16, DK>(p, sp, stream);
+        case GDN_F16: return launch_tc_dv<__half, DK>(p, sp, stream);
         default: return cudaErrorInvalidValue;
     }
 }

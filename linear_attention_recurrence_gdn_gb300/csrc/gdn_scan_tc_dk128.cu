@@ -3,8 +3,8 @@
 
 namespace gdn {
 
-cudaError_t launch_scan_tc_dk128(const gdn_params &p, cudaStream_t stream) {
-    return launch_tc_dk<128>(p, stream);
+cudaError_t launch_scan_tc_dk128(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
+    return launch_tc_dk<128>(p, sp, stream);
 }
 
 cudaError_t scan_watchdog_dk128(unsigned *flag, cudaStream_t stream) {

@@ -3,8 +3,8 @@
 
 namespace gdn {
 
-cudaError_t launch_scan_tc_dk64(const gdn_params &p, cudaStream_t stream) {
-    return launch_tc_dk<64>(p, stream);
+cudaError_t launch_scan_tc_dk64(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
+    return launch_tc_dk<64>(p, sp, stream);
 }
 
 cudaError_t scan_watchdog_dk64(unsigned *flag, cudaStream_t stream) {

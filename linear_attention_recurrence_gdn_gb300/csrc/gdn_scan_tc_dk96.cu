@@ -3,8 +3,8 @@
 
 namespace gdn {
 
-cudaError_t launch_scan_tc_dk96(const gdn_params &p, cudaStream_t stream) {
-    return launch_tc_dk<96>(p, stream);
+cudaError_t launch_scan_tc_dk96(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
+    return launch_tc_dk<96>(p, sp, stream);
 }
 
 cudaError_t scan_watchdog_dk96(unsigned *flag, cudaStream_t stream) {

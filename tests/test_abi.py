@@ -167,6 +167,31 @@ def test_rejections_return_before_any_launch(lib, case):
     assert call(lib, prm, is_decode) == status
 
 
+def test_split_scan_rejections_return_before_any_launch(lib):
+    # fake_params: B 2, S 3, Hk 2, Hv 4, D 64 -> 2 segments of 2 and 1 tokens; workspace of
+    # M, N for one segment and starts for two: (8*64*64 * (1 + 1 + 2)) floats
+    prm = fake_params()
+    need = lib.gdn_scan_split_workspace(ctypes.byref(prm), 2)
+    assert need == 4 * 8 * 64 * 64 * 4
+    assert lib.gdn_scan_split_workspace(ctypes.byref(prm), 1) == 0
+    assert lib.gdn_scan_split_workspace(ctypes.byref(fake_params(Hv=3)), 2) == 0   # rejected p
+    ws = BASE + 16 * GAP
+    cases = [
+        (dict(), 0, ws, need, gdn.GDN_ERR_BAD_ARG, "segments"),
+        (dict(flags=gdn.GDN_FLAG_SCAN_TMEM), 2, ws, need, gdn.GDN_ERR_BAD_ARG, "gdn_scan only"),
+        (dict(), 2, None, need, gdn.GDN_ERR_NULL_PTR, "workspace is required"),
+        (dict(), 2, ws + 8, need, gdn.GDN_ERR_MISALIGNED, "16-byte"),
+        (dict(), 2, ws, need - 16, gdn.GDN_ERR_BAD_ARG, "too small"),
+        (dict(), 2, BASE + 9 * GAP - 64, need, gdn.GDN_ERR_ALIASING, "overlaps"),   # into y
+        (dict(Hv=3), 2, ws, need, gdn.GDN_ERR_BAD_SHAPE, ""),        # gdn_scan's own checks
+    ]
+    for kw, nseg, w, nbytes, status, fragment in cases:
+        p = fake_params(**kw)
+        assert lib.gdn_scan_split(ctypes.byref(p), nseg, w, nbytes, None) == status, kw
+        if fragment:
+            assert fragment in lib.gdn_last_error().decode()
+
+
 def test_null_params_pointer(lib):
     assert lib.gdn_scan(None, None) == gdn.GDN_ERR_NULL_PTR
     assert lib.gdn_decode_step(None, None) == gdn.GDN_ERR_NULL_PTR

@@ -352,6 +352,44 @@ def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
 
 # ------------------------------------------------------------------------------ scan
 
+def bench_split(gdn, w: Workload, dev, reps: int):
+    """gdn_scan against gdn_scan_split at several segment counts on one workload (tokens/s,
+    median of `reps` CUDA-event-timed calls each; the workspace allocated once)."""
+    inp = make_inputs(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    y = torch.empty(d["v"].shape, dtype=torch.float32, device=dev)
+    st = torch.empty((w.B, w.Hv, w.Dv, w.Dk), dtype=torch.float32, device=dev)
+    args = (d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, y)
+    kw = dict(s0=d["s0"], z=d["z"], gn=d["gn"], head_major=w.head_major)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(max(3, reps)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    tokens = w.B * w.S
+    out = {"config": w.as_config(), "metric": "tokens/s", "lines": []}
+    ms = timed(lambda: gdn.gdn_scan(*args, **kw))
+    out["lines"].append({"segments": 1, "ms": ms, "value": tokens / (ms * 1e-3)})
+    for nseg in (2, 4, 8):
+        prm = gdn.make_params(*args, z=d["z"], gn=d["gn"], s0=d["s0"], head_major=w.head_major)
+        wsb = torch.empty(max(16, gdn.gdn_scan_split_workspace(prm, nseg)), dtype=torch.uint8,
+                          device=dev)
+        ms_s = timed(lambda: gdn.gdn_scan_split(*args, segments=nseg, workspace=wsb, **kw))
+        out["lines"].append({"segments": nseg, "ms": ms_s, "value": tokens / (ms_s * 1e-3),
+                             "speedup": ms / ms_s})
+    return out
+
+
 def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks: dict,
                tmem: bool = False):
     inp = make_inputs(w)
@@ -496,9 +534,10 @@ def main(argv=None):
     ap.add_argument("--no-scan", action="store_true", help="skip the supplementary scans")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "decode", "scan", "rect"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "scan", "rect", "split"], default="all",
                     help="decode: skip the scans; scan: time only the scans (profiling runs); "
-                         "rect: time the separate-key/value-head-dim workloads")
+                         "rect: time the separate-key/value-head-dim workloads; split: the "
+                         "sequence-split scan against the scan on a long sequence with few heads")
     ap.add_argument("--scan-S", type=int, default=0,
                     help="override the scan workloads' sequence length (profiling runs)")
     args = ap.parse_args(argv)
@@ -531,6 +570,13 @@ def main(argv=None):
                               props.multi_processor_count, peaks["sm_max_mhz"], peaks, tmem=True))
         if rank == 0:
             print(json.dumps({"scan": out}), flush=True)
+        return 0
+    if args.only == "split":
+        # the long-context workload with a quarter of its value heads (8 heads of one
+        # sequence): too few heads to fill the GPU, the case the sequence split is for
+        ws = LONG_B2.replace(name="long_f16_b1_s16384_hk2_hv8_d128", B=1, Hk=2, Hv=8)
+        if rank == 0:
+            print(json.dumps({"split": bench_split(gdn, ws, dev, args.scan_reps)}), flush=True)
         return 0
     if args.only == "rect":
         # the headline workloads with Dk != Dv (same heads, same token counts), and with head

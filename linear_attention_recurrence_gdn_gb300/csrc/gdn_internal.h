@@ -37,13 +37,17 @@ cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream);
 //   mode 1: each segment's transition M = prod_t alpha_t (I - beta_t k^_t k^_t^T): the rows of
 //           the identity carried through the update with v = 0 (p.Dv == p.Dk), into
 //           state_seg[g]; no y;
-//   mode 2: each segment's offset N (its end memory from zeros), into state_seg[g]; no y.
+//   mode 2: each segment's offset N (its end memory from zeros), into state_seg[g]; no y;
+//   mode 3: both at once when Dk == Dv: grid segments g < nseg / 2 are the transitions of
+//           segments g (into state_seg), the others the offsets of segments g - nseg / 2
+//           (into state_seg2).
 struct ScanSplit {
     int nseg;              // segments in this launch
     int seg_len;           // tokens per segment (the last one may be shorter)
     int mode;
     const float *s0_seg;   // mode 0: [nseg][B*Hv][Dv][Dk] start memories, or NULL
-    float *state_seg;      // modes 1, 2: [nseg][B*Hv][Dv][Dk] end memories
+    float *state_seg;      // modes 1, 2, 3: [nseg][B*Hv][Dv][Dk] end memories
+    float *state_seg2;     // mode 3: the offsets' end memories
 };
 
 // The sequence-split scan: transitions and offsets of segments 0 .. nseg-2 in parallel, their

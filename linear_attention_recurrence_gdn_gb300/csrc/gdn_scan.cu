@@ -82,7 +82,7 @@ gdn_scan_compose_kernel(const float *s0, const float *M, const float *N, float *
 
 cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
     if ((p.flags & GDN_FLAG_SCAN_TMEM) && scan_umma_supported(p)) return launch_scan_umma(p, stream);
-    const ScanSplit whole{1, p.S, 0, nullptr, nullptr};
+    const ScanSplit whole{1, p.S, 0, nullptr, nullptr, nullptr};
     return launch_scan_dk(p, whole, stream);
 }
 
@@ -111,23 +111,32 @@ cudaError_t launch_scan_split(const gdn_params &p, int nseg, float *ws, cudaStre
     float *N = M + (g - 1) * bh * p.Dk * p.Dk;             // [g-1][bh][Dv][Dk]
     float *St = N + (g - 1) * bh * p.Dv * p.Dk;            // [g][bh][Dv][Dk]
     cudaError_t e;
-    // 1. transitions of segments 0 .. g-2: the identity (Dk rows) through the update, v = 0
-    gdn_params pm = p;
-    pm.Dv = p.Dk;
-    pm.z = nullptr;
-    pm.gn = nullptr;
-    pm.y = nullptr;
-    pm.s0 = nullptr;
-    pm.flags = 0;
-    if ((e = launch_scan_dk(pm, ScanSplit{g - 1, len, 1, nullptr, M}, stream)) != cudaSuccess) return e;
-    // 2. offsets of segments 0 .. g-2: from zeros with the real v
+    // 1. transitions of segments 0 .. g-2 (the identity's Dk rows through the update, v = 0)
+    //    and 2. their offsets (from zeros with the real v).  One grid for both when Dk == Dv and
+    //    their (segment, head) pairs fit in half the SMs; else two launches (the transitions
+    //    have Dk rows).  Measured on GB300 (8 heads, f16, S 16384; one grid / two launches):
+    //    2 segments 2.26 / 3.26 ms, 4 segments 1.24 / 1.75 ms, 8 segments 1.33 / 1.08 ms --
+    //    beyond half the SMs the one grid is cut into CTAs of 8 row warps, slower here.
     gdn_params pn = p;
     pn.z = nullptr;
     pn.gn = nullptr;
     pn.y = nullptr;
     pn.s0 = nullptr;
     pn.flags = 0;
-    if ((e = launch_scan_dk(pn, ScanSplit{g - 1, len, 2, nullptr, N}, stream)) != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (p.Dk == p.Dv && 2 * (g - 1) * bh <= sms / 2) {
+        if ((e = launch_scan_dk(pn, ScanSplit{2 * (g - 1), len, 3, nullptr, M, N}, stream)) != cudaSuccess)
+            return e;
+    } else {
+        gdn_params pm = pn;
+        pm.Dv = p.Dk;
+        if ((e = launch_scan_dk(pm, ScanSplit{g - 1, len, 1, nullptr, M, nullptr}, stream)) != cudaSuccess)
+            return e;
+        if ((e = launch_scan_dk(pn, ScanSplit{g - 1, len, 2, nullptr, N, nullptr}, stream)) != cudaSuccess)
+            return e;
+    }
     // 3. every segment's start memory
     const int smem = 16 * p.Dk * static_cast<int>(sizeof(float));
     gdn_scan_compose_kernel<<<dim3(static_cast<unsigned>(bh), p.Dv / 16), 256, smem, stream>>>(
@@ -136,7 +145,7 @@ cudaError_t launch_scan_split(const gdn_params &p, int nseg, float *ws, cudaStre
     // 4. outputs of every segment; the last writes the final memory
     gdn_params po = p;
     po.flags = 0;
-    return launch_scan_dk(po, ScanSplit{g, len, 0, St, nullptr}, stream);
+    return launch_scan_dk(po, ScanSplit{g, len, 0, St, nullptr, nullptr}, stream);
 }
 
 cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {

@@ -166,8 +166,12 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
 
     // segment seg of the sequence (one segment for the plain scan), then head and row block
     const int64_t per_seg = static_cast<int64_t>(p.B) * p.Hv * C::NRB;
-    const int seg = static_cast<int>(blockIdx.x / per_seg);
-    const int64_t local = blockIdx.x - seg * per_seg;
+    const int gseg = static_cast<int>(blockIdx.x / per_seg);   // segment slot in the grid
+    const int64_t local = blockIdx.x - gseg * per_seg;
+    // mode 3 runs transitions (first half of the grid) beside offsets (second half)
+    const int half = sp.nseg / 2;
+    const int mode = sp.mode != 3 ? sp.mode : (gseg < half ? 1 : 2);
+    const int seg = (sp.mode == 3 && gseg >= half) ? gseg - half : gseg;
     const int64_t head = local / C::NRB;                   // b * Hv + hv
     const int rblk = static_cast<int>(local % C::NRB);
     const int b = static_cast<int>(head / p.Hv);
@@ -180,7 +184,7 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
     const int t_begin = seg * sp.seg_len;                  // this segment's first token
     const int S = min(sp.seg_len, S_full - t_begin);       // and its length (>= 1)
     const int nchunks = (S + kT - 1) / kT;
-    const bool v_zero = sp.mode == 1;                      // transition: v = 0, start = identity
+    const bool v_zero = mode == 1;                         // transition: v = 0, start = identity
 
     int64_t k_base, k_ts, v_base, v_ts, g_base, g_ts;
     if (p.head_major) {
@@ -225,7 +229,7 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
         {
             // start memory: the caller's s0 (plain scan), the segment's start, zeros or the
             // identity (transition)
-            const float *s0_src = sp.mode != 0 ? nullptr
+            const float *s0_src = mode != 0 ? nullptr
                                   : sp.s0_seg ? sp.s0_seg + seg_head()
                                   : p.s0 ? p.s0 + head * (DV * DK) : nullptr;
             const float *s0 = s0_src ? s0_src + static_cast<int64_t>(r0 + wrow) * DK : nullptr;
@@ -387,8 +391,9 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
         }
         // final memory rows (undo the deferred decay): the caller's state for the plain scan
         // and the last segment, the per-segment end memory for transitions and offsets
-        if (sp.mode == 0 && seg != sp.nseg - 1) return;    // a segment before the last
-        float *state_dst = sp.mode != 0 ? sp.state_seg + seg_head() : p.state + head * (DV * DK);
+        if (mode == 0 && seg != sp.nseg - 1) return;       // a segment before the last
+        float *state_dst = mode == 0 ? p.state + head * (DV * DK)
+                         : (mode == 2 && sp.mode == 3 ? sp.state_seg2 : sp.state_seg) + seg_head();
         float *so = state_dst + static_cast<int64_t>(r0 + wrow) * DK;
 #pragma unroll
         for (int j = 0; j < NTILE; j++) {

@@ -361,6 +361,38 @@ def test_split_scan_equals_single_scan():
     assert np.array_equal(st2, st)
 
 
+def _transition_and_offset(inp, lo, hi):
+    """M (Dk x Dk, the memory the identity becomes with v = 0) and N (the end memory from
+    zeros) of tokens [lo, hi), both from the oracle."""
+    seg = {k: (v[:, lo:hi].contiguous() if k in ("q", "k", "v", "z", "log_decay", "beta") else v)
+           for k, v in inp.items()}
+    B, S, _, Dk = seg["q"].shape
+    Hv = seg["v"].shape[2]
+    _, N = orun(dict(seg, s0=None), gated=False)
+    ident = dict(seg, v=torch.zeros(B, S, Hv, Dk, dtype=torch.float64),
+                 s0=torch.eye(Dk, dtype=torch.float64).expand(B, Hv, Dk, Dk).contiguous())
+    _, M = orun(ident, gated=False)
+    return M, N
+
+
+def test_segment_end_memory_is_an_affine_map_of_its_start():
+    # The update is affine in the memory (codegen_cuda::gdn, "The fusion"), so a segment of
+    # tokens maps its start memory S0 to S0 M + N.  This is the identity the sequence-split
+    # scan composes; checked on the oracle alone, with Dk != Dv, grouped heads, one segment and
+    # a chain of two.
+    _, inp = small(2, 7, 2, 4, 6, seed=62, Dk=5, Dv=6)
+    _, s_end = orun(inp, gated=False)
+    s0 = inp["s0"].numpy()
+    M, N = _transition_and_offset(inp, 0, 7)
+    assert M.shape == (2, 4, 5, 5) and N.shape == s0.shape
+    assert rel_err(s0 @ M + N, s_end) <= 1e-12
+    M1, N1 = _transition_and_offset(inp, 0, 3)
+    M2, N2 = _transition_and_offset(inp, 3, 7)
+    assert rel_err((s0 @ M1 + N1) @ M2 + N2, s_end) <= 1e-12
+    # M contracts (each factor alpha (I - beta k^ k^T) has spectral norm <= 1)
+    assert np.all(np.linalg.norm(M, ord=2, axis=(-2, -1)) <= 1 + 1e-12)
+
+
 def test_decode_steps_equal_scan():
     _, inp = small(1, 6, 1, 2, 8, seed=62)
     y, st = orun(inp)

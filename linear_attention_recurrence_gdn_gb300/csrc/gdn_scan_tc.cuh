@@ -41,7 +41,12 @@
 //   * the producers apply the gated RMSNorm: over the CTA when it owns a whole head; when a
 //     head's rows are split over NRB CTAs, those CTAs form a thread-block cluster and each
 //     token's partial sum of squares goes to the other CTAs through distributed shared memory
-//     (st.async completing on their mbarriers) before every CTA normalises its own rows.
+//     (st.async completing on their mbarriers) before every CTA normalises its own rows;
+//   * a launch may cover segments of the sequence (the sequence-split scan): each CTA takes
+//     its segment from the grid and reads the segment's tokens with the whole sequence's
+//     strides.  A transition launch carries the identity (Dk rows) through the update with
+//     v = 0, an offset launch starts from zeros; neither writes y, both write their end memory
+//     to the split scan's workspace.  The plain scan is one segment.
 #pragma once
 
 #include <math.h>

@@ -233,6 +233,14 @@ def test_binding_host_io_refuses_unpinned_host_tensors():
                             torch.zeros(1, 1, 16, 16), host_io=True)
 
 
+def test_binding_split_scan_refuses_cpu_tensors():
+    # no CPU path: the sequence-split scan, like the scan, takes CUDA tensors only
+    q = torch.zeros(1, 4, 1, 16)
+    g = torch.zeros(1, 4, 1)
+    with pytest.raises(gdn.GdnError, match="CUDA"):
+        gdn.gdn_scan_split(q, q, q, g, g, segments=2)
+
+
 def test_binding_shape_and_dtype_checks():
     B, S, Hk, Hv, D = 1, 2, 1, 2, 16
     q = torch.zeros(B, S, Hk, D, dtype=torch.bfloat16)

@@ -167,6 +167,32 @@ GDN_API int gdn_scan_split(const gdn_params *p, int segments, void *workspace,
 GDN_API size_t gdn_scan_split_workspace(const gdn_params *p, int segments);
 
 /*
+ * gdn_scan_split_noalloc -- gdn_scan_split for callers that cannot allocate device memory
+ * (code that runs inside another framework's memory pool or arena, or where a cudaMalloc
+ * would synchronise the device or is not allowed), so cannot provide the workspace.  It
+ * computes the same results as gdn_scan_split with a workspace, but takes its scratch from
+ * one fixed device array inside the library, GDN_SCAN_SPLIT_NOALLOC_MAX_BYTES (16 MiB), which
+ * every device that loads the library holds until the process exits.  The caller still passes
+ * every input and output in `p`.  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *   - Calls whose scratch, gdn_scan_split_workspace(p, segments), exceeds the maximum return
+ *     GDN_ERR_BAD_ARG before anything is enqueued (the sizes in gdn_last_error()); a single
+ *     segment needs no scratch and runs gdn_scan.
+ *   - The first call that needs scratch on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's contents (each
+ *     call writes every scratch element before reading it, so nothing needs clearing).  Calls
+ *     that overlap on the GPU (on different streams, or from different threads) race on it:
+ *     order them on one stream, or synchronise between them.
+ *   - Other errors as gdn_scan_split.
+ * Source: none on the pages -- the pages have no counterpart; a deployment variant of
+ * gdn_scan_split.
+ */
+#define GDN_SCAN_SPLIT_NOALLOC_MAX_BYTES (16u << 20)
+GDN_API int gdn_scan_split_noalloc(const gdn_params *p, int segments, void *stream);
+
+/*
  * gdn_reject_reason -- NULL when gdn_decode_step (is_decode != 0) or gdn_scan (is_decode
  * == 0) would accept `p`, else a short static string naming the first failed check.
  * Host-only; touches no device memory.

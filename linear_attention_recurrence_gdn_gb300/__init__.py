@@ -39,10 +39,12 @@ GDN_ERR_BAD_ARG = -7
 GDN_ERR_CUDA = -8
 GDN_ERR_TIMEOUT = -9
 
+GDN_SCAN_SPLIT_NOALLOC_MAX_BYTES = 16 << 20   # fixed scratch of gdn_scan_split_noalloc
+
 # Symbols declared in include/gdn.h (checked by the tests against the header).
 EXPORTED = ("gdn_decode_step", "gdn_scan", "gdn_scan_split", "gdn_scan_split_workspace",
-            "gdn_reject_reason", "gdn_status_string", "gdn_last_error", "gdn_device_status",
-            "gdn_selftest_wait_timeout", "gdn_version")
+            "gdn_scan_split_noalloc", "gdn_reject_reason", "gdn_status_string",
+            "gdn_last_error", "gdn_device_status", "gdn_selftest_wait_timeout", "gdn_version")
 
 
 class GdnParams(ctypes.Structure):
@@ -89,6 +91,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.gdn_scan_split.restype = ctypes.c_int
     lib.gdn_scan_split_workspace.argtypes = [P, ctypes.c_int]
     lib.gdn_scan_split_workspace.restype = ctypes.c_size_t
+    lib.gdn_scan_split_noalloc.argtypes = [P, ctypes.c_int, ctypes.c_void_p]
+    lib.gdn_scan_split_noalloc.restype = ctypes.c_int
     lib.gdn_reject_reason.argtypes = [P, ctypes.c_int]
     lib.gdn_reject_reason.restype = ctypes.c_char_p
     lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -272,6 +276,24 @@ def gdn_scan_split(q, k, v, log_decay, beta, state=None, y=None, *, segments, s0
     nbytes = workspace.numel() * workspace.element_size()
     st = lib.gdn_scan_split(ctypes.byref(prm), int(segments), _ptr(workspace), nbytes,
                             _stream_handle(stream, v.device))
+    _raise(lib, st, prm, 0)
+    return y, state
+
+
+def gdn_scan_split_noalloc(q, k, v, log_decay, beta, state, y, *, segments, s0=None, z=None,
+                           gn=None, head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None):
+    """``gdn_scan_split`` for callers that cannot allocate device memory: the C entry point
+    takes its scratch from a fixed array inside the library (at most
+    ``GDN_SCAN_SPLIT_NOALLOC_MAX_BYTES``) and allocates nothing.  ``state`` and ``y`` are the
+    caller's output tensors (required here).  Calls that overlap on the GPU share that array
+    and race: keep them on one stream.  Returns ``(y, state)``.
+    """
+    _require_cuda(q, k, v, log_decay, beta, state, y, z, gn, s0)
+    prm = make_params(q, k, v, log_decay, beta, state, y, z=z, gn=gn, s0=s0,
+                      head_major=head_major, qk_eps=qk_eps, norm_eps=norm_eps)
+    lib = library()
+    st = lib.gdn_scan_split_noalloc(ctypes.byref(prm), int(segments),
+                                    _stream_handle(stream, v.device))
     _raise(lib, st, prm, 0)
     return y, state
 

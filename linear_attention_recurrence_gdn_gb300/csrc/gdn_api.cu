@@ -8,6 +8,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "gdn.h"
@@ -268,3 +270,72 @@ int gdn_selftest_wait_timeout(void *stream, double limit_ms) {
 int gdn_version(void) { return GDN_VERSION; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ gdn_scan_split_noalloc
+//
+// The split scan for callers that may not allocate device memory: code that runs inside
+// another framework's memory pool or arena, or on a path where a cudaMalloc would
+// synchronise the device or fail.  Its scratch (transitions, offsets and start memories of
+// the segments) is one fixed array of this translation unit; every device that loads the
+// library holds it until the process exits.
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_split_scratch[GDN_SCAN_SPLIT_NOALLOC_MAX_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices];   // device address of g_split_scratch per device ordinal
+
+// The device address of the scratch array on the current device.  In host code the array's
+// name is only a host-side stand-in, so the address is looked up once per device (with that
+// device current) and kept.
+int split_scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) {
+        snprintf(g_last_error, sizeof g_last_error, "device ordinal %d beyond %d", dev, kMaxDevices);
+        return GDN_ERR_BAD_ARG;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_split_scratch);
+        if (e != cudaSuccess) return cuda_status(e);
+        g_scratch_addr[dev] = addr;
+    }
+    *out = g_scratch_addr[dev];
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" int gdn_scan_split_noalloc(const gdn_params *p, int segments, void *stream) {
+    const char *why;
+    int st = check(p, 0, &why);
+    if (st != GDN_OK) return st;
+    if (segments < 1) {
+        snprintf(g_last_error, sizeof g_last_error, "segments must be >= 1");
+        return GDN_ERR_BAD_ARG;
+    }
+    if (p->flags & GDN_FLAG_SCAN_TMEM) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "flags: GDN_FLAG_SCAN_TMEM applies to gdn_scan only");
+        return GDN_ERR_BAD_ARG;
+    }
+    if (p->B == 0 || p->S == 0) return gdn_scan(p, stream);
+    const size_t need = gdn::scan_split_workspace_floats(*p, segments) * sizeof(float);
+    if (need > GDN_SCAN_SPLIT_NOALLOC_MAX_BYTES) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "split scratch of %zu bytes exceeds the fixed %zu bytes of "
+                 "gdn_scan_split_noalloc (use fewer segments, or gdn_scan_split with a "
+                 "workspace)", need, static_cast<size_t>(GDN_SCAN_SPLIT_NOALLOC_MAX_BYTES));
+        return GDN_ERR_BAD_ARG;
+    }
+    void *scratch = nullptr;
+    if (need > 0 && (st = split_scratch_address(&scratch)) != GDN_OK) return st;
+    // every scratch element is written before it is read: nothing needs clearing
+    return cuda_status(gdn::launch_scan_split(*p, segments, static_cast<float *>(scratch),
+                                              static_cast<cudaStream_t>(stream)));
+}

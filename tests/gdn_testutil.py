@@ -1,6 +1,7 @@
 """Shared helpers of the GPU parity tests (device moves, oracle calls, error measures)."""
 from __future__ import annotations
 
+import json
 import os
 
 import numpy as np
@@ -14,6 +15,10 @@ DECODE_TOL = 1e-4
 SCAN_TOL = 2e-3
 
 CPUS = os.cpu_count() or 1
+
+# Where the full-size parity tests append their measured margins (JSON lines); unset: only
+# printed.  tests/parity_table.py turns such a file into the margin table under profiles/.
+PARITY_LOG = os.environ.get("GDN_PARITY_LOG")
 
 
 def small_workload(B=1, S=4, Hk=1, Hv=2, D=16, act="f32", head_major=False, s0_std=0.1,
@@ -44,6 +49,18 @@ def rel_err(gpu: torch.Tensor, ref: np.ndarray, mask=None) -> float:
     return float(np.max(np.abs(a - ref) / (1.0 + np.abs(ref))))
 
 
+def record_margin(workload: str, kernel: str, output: str, err_y: float, err_state: float,
+                  tol: float):
+    """Record a parity case's max |gpu - oracle| / (1 + |oracle|) on y and on the final state
+    next to its tolerance (printed, and appended to $GDN_PARITY_LOG when set)."""
+    rec = {"workload": workload, "kernel": kernel, "output": output, "err_y": err_y,
+           "err_state": err_state, "tol": tol}
+    print("parity-margin", json.dumps(rec))
+    if PARITY_LOG:
+        with open(PARITY_LOG, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+
 def guarded(shape, dtype=torch.float32, dev="cuda", fill=1234.5, guard=4096):
     """A tensor with `guard` sentinel elements on both sides inside one allocation.
 
@@ -61,4 +78,4 @@ def guard_intact(whole: torch.Tensor, n: int, guard=4096, fill=1234.5) -> bool:
 
 
 __all__ = ["DECODE_TOL", "SCAN_TOL", "small_workload", "to_dev", "oracle_ref", "rel_err",
-           "guarded", "guard_intact", "make_inputs"]
+           "guarded", "guard_intact", "make_inputs", "record_margin"]

@@ -13,8 +13,8 @@ import linear_attention_recurrence_gdn_gb300 as gdn
 from linear_attention_recurrence_gdn_gb300 import build as gbuild
 from linear_attention_recurrence_gdn_gb300.workloads import (LONG_B2, PREFILL_B4, TINY,
                                                              make_inputs)
-from gdn_testutil import (DECODE_TOL, SCAN_TOL, guard_intact, guarded, oracle_ref, rel_err,
-                          small_workload, to_dev)
+from gdn_testutil import (DECODE_TOL, SCAN_TOL, guard_intact, guarded, oracle_ref,
+                          record_margin, rel_err, small_workload, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,19 +48,26 @@ def test_tiny_workload():
     assert rel_err(y, yr) <= 1e-4
 
 
+@pytest.mark.parametrize("gated", [True, False], ids=["gated", "raw_o"])
 @pytest.mark.parametrize("w", [PREFILL_B4, LONG_B2], ids=lambda w: w.name)
-def test_full_size_scan_matches_oracle(w):
+def test_full_size_scan_matches_oracle(w, gated):
+    # raw o (no gated norm) as well: rmsnorm would hide a wrong scale on o
     inp = make_inputs(w)
     d = to_dev(inp)
     y, ywhole = guarded(tuple(d["v"].shape))
     st, swhole = guarded((w.B, w.Hv, w.Dv, w.Dk))
     gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, y, s0=d["s0"],
-                 z=d["z"], gn=d["gn"], head_major=w.head_major)
+                 z=d["z"] if gated else None, gn=d["gn"] if gated else None,
+                 head_major=w.head_major)
     torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
     del d
-    yr, sr = oracle_ref(inp, head_major=w.head_major)
-    assert rel_err(y, yr) <= SCAN_TOL
-    assert rel_err(st, sr) <= SCAN_TOL
+    yr, sr = oracle_ref(inp, gated=gated, head_major=w.head_major)
+    ey, es = rel_err(y, yr), rel_err(st, sr)
+    record_margin(w.name, "gdn_scan default", "gated y" if gated else "raw o", ey, es,
+                  SCAN_TOL)
+    assert ey <= SCAN_TOL
+    assert es <= SCAN_TOL
     assert guard_intact(ywhole, y.numel()) and guard_intact(swhole, st.numel())
 
 

@@ -17,8 +17,8 @@ import torch
 import linear_attention_recurrence_gdn_gb300 as gdn
 from linear_attention_recurrence_gdn_gb300 import build as gbuild
 from linear_attention_recurrence_gdn_gb300.workloads import PREFILL_B4, make_inputs
-from gdn_testutil import (SCAN_TOL, guard_intact, guarded, oracle_ref, rel_err, small_workload,
-                          to_dev)
+from gdn_testutil import (SCAN_TOL, guard_intact, guarded, oracle_ref, record_margin, rel_err,
+                          small_workload, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -129,17 +129,22 @@ def test_tmem_flag_on_other_shapes_runs_the_default_kernel(act, D):
     assert rel_err(y, yr) <= SCAN_TOL and rel_err(st, sr) <= SCAN_TOL
 
 
-def test_tmem_scan_full_size_prefill():
+@pytest.mark.parametrize("gated", [True, False], ids=["gated", "raw_o"])
+def test_tmem_scan_full_size_prefill(gated):
     w = PREFILL_B4
     inp = make_inputs(w)
     d = to_dev(inp)
     y, ywhole = guarded(tuple(d["v"].shape))
     st, swhole = guarded((w.B, w.Hv, w.Dv, w.Dk))
     gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, y, s0=d["s0"],
-                 z=d["z"], gn=d["gn"], head_major=w.head_major, tmem=True)
+                 z=d["z"] if gated else None, gn=d["gn"] if gated else None,
+                 head_major=w.head_major, tmem=True)
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == gdn.GDN_OK
     del d
-    yr, sr = oracle_ref(inp, head_major=w.head_major)
-    assert rel_err(y, yr) <= SCAN_TOL and rel_err(st, sr) <= SCAN_TOL
+    yr, sr = oracle_ref(inp, gated=gated, head_major=w.head_major)
+    ey, es = rel_err(y, yr), rel_err(st, sr)
+    record_margin(w.name, "gdn_scan tensor-memory (GDN_FLAG_SCAN_TMEM)",
+                  "gated y" if gated else "raw o", ey, es, SCAN_TOL)
+    assert ey <= SCAN_TOL and es <= SCAN_TOL
     assert guard_intact(ywhole, y.numel()) and guard_intact(swhole, st.numel())

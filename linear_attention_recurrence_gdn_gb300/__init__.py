@@ -271,12 +271,18 @@ def gdn_scan_split(q, k, v, log_decay, beta, state=None, y=None, *, segments, s0
                       head_major=head_major, qk_eps=qk_eps, norm_eps=norm_eps)
     lib = library()
     need = lib.gdn_scan_split_workspace(ctypes.byref(prm), int(segments))
-    if workspace is None:
+    own_workspace = workspace is None
+    if own_workspace:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=v.device)
     nbytes = workspace.numel() * workspace.element_size()
     st = lib.gdn_scan_split(ctypes.byref(prm), int(segments), _ptr(workspace), nbytes,
                             _stream_handle(stream, v.device))
     _raise(lib, st, prm, 0)
+    if own_workspace and stream is not None:
+        # the kernels use the workspace on `stream`, not on the current stream it was
+        # allocated on: keep the caching allocator from reusing it before `stream` is done
+        workspace.record_stream(stream if isinstance(stream, torch.cuda.Stream)
+                                else torch.cuda.ExternalStream(int(stream), device=v.device))
     return y, state
 
 

@@ -17,8 +17,8 @@ import torch
 
 import linear_attention_recurrence_gdn_gb300 as gdn
 from linear_attention_recurrence_gdn_gb300 import build as gbuild
-from linear_attention_recurrence_gdn_gb300.workloads import make_inputs
-from gdn_testutil import SCAN_TOL, oracle_ref, rel_err, small_workload, to_dev
+from linear_attention_recurrence_gdn_gb300.workloads import LONG_B2, make_inputs
+from gdn_testutil import SCAN_TOL, oracle_ref, record_margin, rel_err, small_workload, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -102,3 +102,68 @@ def test_split_workspace_size_formula():
         expect = 0 if g == 1 else 4 * ((g - 1) * bh * 64 * 64 + (g - 1) * bh * 128 * 64
                                        + g * bh * 128 * 64)
         assert need == expect, (nseg, need, expect)
+
+
+@pytest.mark.parametrize("nseg", [4, 8])
+def test_split_scan_long_slow_decay_few_heads(nseg):
+    # the regime the split is built and measured for: one sequence of 16384 f16 tokens with 8
+    # value heads and the long workload's slow decay (alpha up to 0.9997), where the f32
+    # composition S0 M + N runs over many near-identity transitions
+    w = LONG_B2.replace(name="long_f16_b1_s16384_hk2_hv8_d128", B=1, Hk=2, Hv=8)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    y, st = gdn.gdn_scan_split(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], s0=d["s0"],
+                               z=d["z"], gn=d["gn"], segments=nseg)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    del d
+    yr, sr = oracle_ref(inp)
+    ey, es = rel_err(y, yr), rel_err(st, sr)
+    record_margin(w.name, f"gdn_scan_split, {nseg} segments", "gated y", ey, es, SCAN_TOL)
+    assert ey <= SCAN_TOL and es <= SCAN_TOL
+
+
+def test_split_one_grid_and_two_launches_agree_around_the_threshold():
+    # With Dk == Dv the transitions and offsets share one grid while their 2 (g - 1) B Hv
+    # (segment, head) pairs fit in half the SMs, else they run as two launches.  One shape on
+    # each side of that threshold, from this device's SM count: both paths against the oracle.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    g = 3                                              # segments: 2 (g - 1) = 4 pairs per head
+    bh_under = (sms // 2) // (2 * (g - 1))             # largest B Hv on the one-grid side
+    results = []
+    for bh in (bh_under, bh_under + 1):
+        B, Hv = bh, 1
+        w = small_workload(B=B, S=96, Hk=1, Hv=Hv, D=64, act="bf16", seed=820 + bh,
+                           s0_std=0.05)
+        inp = make_inputs(w)
+        d = to_dev(inp)
+        y, st = gdn.gdn_scan_split(d["q"], d["k"], d["v"], d["log_decay"], d["beta"],
+                                   s0=d["s0"], z=d["z"], gn=d["gn"], segments=g)
+        torch.cuda.synchronize()
+        yr, sr = oracle_ref(inp)
+        assert rel_err(y, yr) <= SCAN_TOL and rel_err(st, sr) <= SCAN_TOL
+        results.append(2 * (g - 1) * B * Hv <= sms // 2)
+    assert results == [True, False]                    # one case on each side
+
+
+def test_split_scan_on_a_side_stream_keeps_its_own_workspace():
+    # The binding allocates the workspace on the current stream; the kernels run on a side
+    # stream.  Memory allocated and filled on the current stream right after the call must not
+    # receive the freed workspace block while the side stream still uses it.
+    w = small_workload(B=1, S=2000, Hk=2, Hv=4, D=128, act="bf16", seed=830, s0_std=0.05)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        y = torch.empty(d["v"].shape, dtype=torch.float32, device="cuda")
+        st = torch.empty(d["s0"].shape, dtype=torch.float32, device="cuda")
+    y.record_stream(side)
+    st.record_stream(side)
+    gdn.gdn_scan_split(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, y, s0=d["s0"],
+                       z=d["z"], gn=d["gn"], segments=4, stream=side)
+    junk = [torch.full((1 << 20,), 3.0e4, device="cuda") for _ in range(8)]
+    torch.cuda.synchronize()
+    del junk
+    yr, sr = oracle_ref(inp)
+    assert rel_err(y, yr) <= SCAN_TOL and rel_err(st, sr) <= SCAN_TOL

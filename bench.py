@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 from linear_attention_recurrence_gdn_gb300.workloads import (  # noqa: E402
-    DECODE_B64, LONG_B2, PREFILL_B4, Workload, make_inputs)
+    DECODE_B64, DECODE_B256_HM, LONG_B2, PREFILL_B4, Workload, make_inputs)
 
 METRIC = "GDN decode step: state HBM GB/s (% of peak); gdn_scan tokens/sec"
 FALLBACK_HBM_GBS = 6800.0
@@ -419,40 +419,36 @@ def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks:
     mma = scan_mma_flops(w) / secs / 1e12
     mma_sync_peak = sms * MMA_SYNC_MAC_PER_CLK_SM * 2 * sm_mhz * 1e6 / 1e12
     bf16 = peaks["bf16_tflops"]
+    method = scan_flops(w) / secs / 1e12
+    roof = {"bound": "tensor", "achieved": method, "peak": bf16, "unit": "TFLOP/s",
+            "frac": method / bf16, "traffic": None,
+            "work": "6 Dk Dv FLOP per token-head: the method's own products (S.k, S.q and the "
+                    "rank-1 update), whatever the kernel issues",
+            "peak_note": f"{peaks['source']} cuBLAS bf16 dense"}
     if tmem:
         tc = scan_tmem_mma_flops(w) / secs / 1e12
         cfg = dict(w.as_config(), kernel="tensor-memory chunked (GDN_FLAG_SCAN_TMEM)")
-        return {"config": cfg, "value": w.B * w.S / secs, "unit": "tokens/s", "ms": ms,
-                "reps": reps,
-                "roofline": {"bound": "tensor", "achieved": tc, "peak": bf16, "unit": "TFLOP/s",
-                             "frac": tc / bf16, "traffic": None,
-                             "peak_note": f"{peaks['source']} cuBLAS bf16 dense; this kernel "
-                                          f"issues tcgen05 MMAs (M = 128, N = 32..128)",
-                             "work": "tensor-core FLOPs of the chunked kernel's tcgen05 MMAs "
-                                     "(tables, [x | y], d, O, update, correction; hi/lo terms "
-                                     "counted)"},
-                "fp32_equivalent": {"achieved": fp32_eq, "peak": fp32_peak, "unit": "TFLOP/s",
-                                    "frac": fp32_eq / fp32_peak},
-                "hbm_bytes": scan_bytes(w)}
-    return {"config": w.as_config(), "value": w.B * w.S / secs, "unit": "tokens/s",
-            "ms": ms, "reps": reps,
-            "roofline": {"bound": "tensor", "achieved": mma, "peak": bf16, "unit": "TFLOP/s",
-                         "frac": mma / bf16, "traffic": None,
-                         "peak_note": f"{peaks['source']} cuBLAS bf16 dense (tcgen05); the "
-                                      f"kernel issues mma.sync, whose own ceiling is "
-                                      f"{MMA_SYNC_MAC_PER_CLK_SM} MAC/clk/SM = "
-                                      f"{mma_sync_peak:.0f} TFLOP/s at {sm_mhz:.0f} MHz "
-                                      f"(frac {mma / mma_sync_peak:.3f} of it)",
-                         "work": "tensor-core FLOPs of the block form's row MMAs (X, Y, d, O, "
-                                 "update; hi/lo operand terms counted)"},
+        roof["issued"] = {"achieved": tc, "frac": tc / bf16, "unit": "TFLOP/s",
+                          "work": "tcgen05 MMA FLOPs the chunked kernel issues (tables, "
+                                  "[x | y], d, O, update, correction; hi/lo terms counted)"}
+    else:
+        cfg = dict(w.as_config(), kernel="default")
+        roof["issued"] = {"achieved": mma, "frac": mma / bf16, "unit": "TFLOP/s",
+                          "frac_of_mma_sync_ceiling": mma / mma_sync_peak,
+                          "work": "mma.sync FLOPs the block form issues for its row MMAs (X, "
+                                  "Y, d, O, update; hi/lo operand terms counted)",
+                          "ceiling_note": f"mma.sync's own ceiling {MMA_SYNC_MAC_PER_CLK_SM} "
+                                          f"MAC/clk/SM = {mma_sync_peak:.0f} TFLOP/s at "
+                                          f"{sm_mhz:.0f} MHz"}
+    return {"config": cfg, "value": w.B * w.S / secs, "unit": "tokens/s", "ms": ms,
+            "reps": reps, "roofline": roof,
             "fp32_equivalent": {"achieved": fp32_eq, "peak": fp32_peak, "unit": "TFLOP/s",
                                 "frac": fp32_eq / fp32_peak,
                                 "work": "6 Dk Dv FLOP per token-head (the sequential "
                                         "recurrence's own count)",
                                 "peak_note": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
                                              f"x {sm_mhz:.0f} MHz: the sequential form's "
-                                             f"FP32 roofline, which the tensor-core form "
-                                             f"may exceed"},
+                                             f"FP32 roofline"},
             "hbm_bytes": scan_bytes(w)}
 
 
@@ -479,6 +475,54 @@ def oracle_decode_sample(w: Workload, batch: int, threads: int, min_seconds: flo
             "kind": "oracle", "seconds_per_call": sec,
             "sample": f"{calls} oracle decode step(s) of {batch} of {w.B} sequences "
                       f"(all {w.Hv} value heads) of {w.name}, fp64, {threads} threads"}
+
+
+def oracle_scan_sample(w: Workload, threads: int, min_seconds: float, tokens: int = 512):
+    """Time the fp64 oracle on the first `tokens` tokens of one sequence of scan workload `w`
+    (all its value heads), repeated until `min_seconds` have passed; tokens/s as gdn_scan's
+    metric counts them (B * S per call, all heads)."""
+    import oracle
+    ws = w.replace(B=1, S=min(tokens, w.S))
+    inp = make_inputs(ws)
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"], z=inp["z"],
+                   gn=inp["gn"], s0=inp["s0"], threads=threads)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return {"workload": w.name, "value": ws.S * calls / el, "unit": "tokens/s", "cores": threads,
+            "sample": f"{calls} oracle scan(s) of the first {ws.S} tokens of one of {w.B} "
+                      f"sequences (all {w.Hv} value heads), fp64, {threads} threads"}
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baselines(w: Workload, scans, seconds: float) -> dict:
+    """The oracle as it stands on this host: the decode workload on all cores (the line's
+    cpu_baseline value) and on one thread, and tokens/s of the scan workloads (all cores and
+    one thread)."""
+    cores = os.cpu_count() or 1
+    out = oracle_decode_sample(w, w.B, cores, seconds)
+    out.pop("seconds_per_call", None)
+    one = oracle_decode_sample(w, max(1, w.B // 16), 1, seconds / 4)
+    one.pop("seconds_per_call", None)
+    out["threads1"] = one
+    out["cpu_model"] = cpu_model()
+    out["scan"] = [oracle_scan_sample(x, cores, seconds / 4) for x in scans]
+    out["scan"] += [oracle_scan_sample(x, 1, seconds / 8, tokens=128) for x in scans]
+    return out
 
 
 def reference_arm(args, w: Workload):
@@ -612,6 +656,31 @@ def main(argv=None):
     value = aggregate_rate(decode_bytes(w), world, ms_step * 1e-3) / 1e9
     per_launch = decode_bytes(w) / (ms_step * 1e-3) / 1e9
 
+    # the large-batch decode workload (B = 256, head-major operands): each step moves four
+    # times the bytes, so a quarter of the steps
+    wl = DECODE_B256_HM
+    steps_l = max(args.warmup, args.steps // 4)
+    dec_l = bench_decode(gdn, wl, dev, steps_l, args.warmup, world, sampler)
+    sets_l = dec_l["sets"]
+    del dec_l["bufs"], dec_l["params"]
+    torch.cuda.empty_cache()
+
+    def decode_entry(wd: Workload, d: dict, steps: int, sets: int, traffic_file: str) -> dict:
+        gbs = decode_bytes(wd) / (d["ms_per_step"] * 1e-3) / 1e9
+        return {"config": dict(wd.as_config(), bytes_per_step=decode_bytes(wd),
+                               l2=f"rotating {sets} independent state/input sets"),
+                "value": aggregate_rate(decode_bytes(wd), world, d["ms_per_step"] * 1e-3) / 1e9,
+                "unit": "GB/s", "steps": steps, "ms_per_step": d["ms_per_step"],
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                             "traffic": profiled_traffic("gdn_decode.cuh", traffic_file),
+                             "peak_source": peaks["source"], "kernel": "gdn_decode_kernel",
+                             "frac_of_nominal_8tbs": gbs / 8000.0},
+                "clocks": d["clocks"]}
+
+    decodes = [decode_entry(w, dec, args.steps, dec["sets"], "decode_b64_dram_traffic.txt"),
+               decode_entry(wl, dec_l, steps_l, sets_l, "decode_b256_hm_dram_traffic.txt")]
+
     e2e = e2e_decode(gdn, w, dev, args.e2e_steps, world)
     scan = None
     if not args.no_scan and args.only == "all":
@@ -628,8 +697,7 @@ def main(argv=None):
         return 0
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = oracle_decode_sample(w, w.B, os.cpu_count() or 1, args.cpu_seconds)
-        cpu.pop("seconds_per_call", None)
+        cpu = cpu_baselines(w, [PREFILL_B4, LONG_B2], args.cpu_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -649,6 +717,7 @@ def main(argv=None):
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": dec["clocks"],
+        "decode_workloads": decodes,
         "scan": scan,
         "device": props.name,
     }

@@ -201,10 +201,13 @@ GDN_API int gdn_scan_split_noalloc(const gdn_params *p, int segments, void *stre
  */
 GDN_API const char *gdn_reject_reason(const gdn_params *p, int is_decode);
 
-/* gdn_status_string -- static text for a gdn_status value (unknown codes included). */
+/* gdn_status_string -- static text for a gdn_status value (unknown codes included).
+ * Source: none on the pages -- the library's own status codes. */
 GDN_API const char *gdn_status_string(int status);
 
-/* gdn_last_error -- text of the last GDN_ERR_CUDA seen by the calling thread ("" if none). */
+/* gdn_last_error -- text of the last GDN_ERR_CUDA seen by the calling thread ("" if none), or
+ * of the last rejection that gdn_reject_reason cannot name (split-scan arguments).
+ * Source: none on the pages -- the library's own error reporting. */
 GDN_API const char *gdn_last_error(void);
 
 /*
@@ -230,7 +233,8 @@ GDN_API int gdn_device_status(void *stream);
  */
 GDN_API int gdn_selftest_wait_timeout(void *stream, double limit_ms);
 
-/* gdn_version -- GDN_VERSION of the loaded library. */
+/* gdn_version -- GDN_VERSION of the loaded library.
+ * Source: none on the pages -- the library's own version number. */
 GDN_API int gdn_version(void);
 
 #ifdef __cplusplus

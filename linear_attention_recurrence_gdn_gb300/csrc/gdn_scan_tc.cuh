@@ -469,6 +469,7 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
         gn4[f] = fused_norm ? *reinterpret_cast<const float4 *>(p.gn + r0 + 4 * (ptid % TPT + TPT * f))
                             : make_float4(0.f, 0.f, 0.f, 0.f);
     const float inv_d = 1.0f / static_cast<float>(DV);
+    bool gave_up = false;                                  // a cluster wait ran out twice
     auto emit = [&](int c) {
         if (p.y == nullptr) return;                        // transitions and offsets: no y
         const int hb = c & 1, vs = c % C::NVZ;
@@ -499,7 +500,13 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
                         if (pr != rblk) st_async_peer(&sm.peer_ss[hb][rblk][tt], ss[it], &sm.peer_bar[hb], pr);
                 }
             }
-            if (!C::WHOLE_HEAD) mbar_wait_bounded(&sm.peer_bar[hb], static_cast<unsigned>((c >> 1) & 1));
+            // a wait that runs out sets the watchdog word and is tried once more; if that runs
+            // out too, this thread stops waiting and stops storing y (the call is then reported
+            // as timed out by gdn_device_status)
+            if (!C::WHOLE_HEAD && !gave_up &&
+                !mbar_wait_bounded(&sm.peer_bar[hb], static_cast<unsigned>((c >> 1) & 1)) &&
+                !mbar_wait_bounded(&sm.peer_bar[hb], static_cast<unsigned>((c >> 1) & 1)))
+                gave_up = true;
 #pragma unroll
             for (int it = 0; it < NIT; it++) {
                 const int tt = ptid / TPT + it * (PT / TPT);
@@ -510,7 +517,7 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
                         if (pr != rblk) tot += sm.peer_ss[hb][pr][tt];
                 }
                 const float rr = rsqrtf(fmaf(tot, inv_d, p.norm_eps));
-                if (tt < nt) {
+                if (tt < nt && !gave_up) {
                     float *yr = p.y + v_base + r0 + (t0 + tt) * v_ts;
 #pragma unroll
                     for (int f = 0; f < FPT; f++) {

@@ -123,7 +123,10 @@ struct alignas(1024) U3Smem {
     alignas(8) uint64_t bar_tab, bar_d, bar_o, bar_pre;   // MMA groups completed
     alignas(8) uint64_t bar_g[3];                 // correction operand written (64 arrivals)
     alignas(8) uint64_t bar_gates[2];             // decay products of a chunk written (32)
+    alignas(8) uint64_t bar_drain[2];             // final commits of the two MMA-issuing warps
+    alignas(8) uint64_t bar_tabdone;              // table warp 1's MMAs drained
     uint32_t tmem_base;
+    int abandon;                                  // a wait ran out twice: stop issuing work
 };
 static_assert(sizeof(U3Smem) + 1024 <= 227 * 1024, "shared memory");
 
@@ -169,6 +172,10 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         for (int i = 0; i < 3; i++) mbar_init(&sm.bar_g[i], 64);
         mbar_init(&sm.bar_gates[0], 32);
         mbar_init(&sm.bar_gates[1], 32);
+        mbar_init(&sm.bar_drain[0], 1);
+        mbar_init(&sm.bar_drain[1], 1);
+        mbar_init(&sm.bar_tabdone, 1);
+        sm.abandon = 0;
         mbar_init_fence();
     }
     __syncwarp();
@@ -178,10 +185,35 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const uint32_t kq0 = smem_u32(&sm.kq[0][0]);
+    // Bounded wait: if the wait runs out (the watchdog word is set) it is tried once more; if
+    // that runs out too the CTA abandons its work: every later wait returns false at once, no
+    // MMAs, copies or stores are issued, and what was issued is drained before tensor memory
+    // is freed.
+    volatile int *abandon = &sm.abandon;
+    auto bwait = [&](uint64_t *bar, unsigned parity) -> bool {
+        if (*abandon) return false;
+        if (mbar_wait_bounded(bar, parity) || mbar_wait_bounded(bar, parity)) return true;
+        *abandon = 1;
+        return false;
+    };
     // MMAs are issued by one elected lane of a converged warp
+    bool issued = false;
     auto issue = [&](int by_warp, auto &&body) {
         if (warp == by_warp) {
-            if (elect_one()) body();
+            if (__all_sync(0xffffffffu, !*abandon)) {
+                issued = true;
+                if (elect_one()) body();
+            }
+            __syncwarp();
+        }
+    };
+    // the MMAs this thread's warp issued have completed (bounded)
+    auto drain = [&](int i) {
+        if (issued) {
+            if (elect_one()) {
+                umma_commit(&sm.bar_drain[i]);
+                mbar_wait_bounded(&sm.bar_drain[i], 0);
+            }
             __syncwarp();
         }
     };
@@ -232,7 +264,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         };
         auto wait_mma = [&](uint64_t *bar, unsigned parity) {
             __syncwarp();
-            mbar_wait_bounded(bar, parity);
+            bwait(bar, parity);
             __syncwarp();
             tc_fence_after();
         };
@@ -261,7 +293,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         split_s();
         row_barrier();
         issue(0, [&] {                                     // tables and [x | y] of chunk 0
-            mbar_wait_bounded(&sm.bar_load[0], 0);
+            bwait(&sm.bar_load[0], 0);
             tc_fence_after();
             issue_tables(0);
             issue_pre(0);
@@ -331,7 +363,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 split_s();
                 row_barrier();
                 issue(0, [&] {
-                    mbar_wait_bounded(&sm.bar_load[(ch + 1) % uSlots], load_parity(ch + 1));
+                    bwait(&sm.bar_load[(ch + 1) % uSlots], load_parity(ch + 1));
                     tc_fence_after();
                     issue_pre(ch + 1);
                     umma_commit(&sm.bar_pre);
@@ -403,7 +435,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 }
                 if (more) {                                // next [x | y] += C (K_ch [K;Q]_{ch+1}^T)
                     const int gb = (ch + 1) % 3;           // prep ch+1 wrote it, use (ch) / 3 of gb
-                    mbar_wait_bounded(&sm.bar_g[gb], static_cast<unsigned>((ch / 3) & 1));
+                    bwait(&sm.bar_g[gb], static_cast<unsigned>((ch / 3) & 1));
                     tc_fence_after();
                     const uint32_t gh = smem_u32(&sm.ghi[gb][0]), gl = smem_u32(&sm.glo[gb][0]);
 #pragma unroll
@@ -433,14 +465,20 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         {
             float v[64];
             tm_ld64(tl + TM_S + 64 * hr, v);
+            if (!*abandon) {                               // no stores once abandoned
 #pragma unroll
-            for (int j4 = 0; j4 < 16; j4++)
-                *reinterpret_cast<float4 *>(so + 4 * j4) =
-                    make_float4(lam * v[4 * j4], lam * v[4 * j4 + 1], lam * v[4 * j4 + 2], lam * v[4 * j4 + 3]);
+                for (int j4 = 0; j4 < 16; j4++)
+                    *reinterpret_cast<float4 *>(so + 4 * j4) =
+                        make_float4(lam * v[4 * j4], lam * v[4 * j4 + 1], lam * v[4 * j4 + 2], lam * v[4 * j4 + 3]);
+            }
         }
+        drain(0);                                          // warp 0's MMAs
         tc_fence_before();
         bar_sync(uBarRow, uRT);
         if (warp == 0) {
+            // table warp 1's MMAs too (they are all consumed already unless the CTA abandoned)
+            if (lane == 0) mbar_wait_bounded(&sm.bar_tabdone, 0);
+            __syncwarp();
             tc_fence_after();
             tmem_dealloc(tmem, TM_COLS);
         }
@@ -457,7 +495,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         for (int ch = 0; ch < nchunks; ch++) {
             const int hb = ch & 1, tb = ch % 3;
             const int nt = min(uC, S - ch * uC);
-            mbar_wait_bounded(&sm.bar_tab, static_cast<unsigned>(ch & 1));
+            bwait(&sm.bar_tab, static_cast<unsigned>(ch & 1));
             __syncwarp();
             tc_fence_after();
             float tab[64];                                 // [cross (K_{ch-1}) | own chunk]
@@ -467,8 +505,8 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             if (ch + 1 < nchunks) {                        // the next chunk's tables, early
                 issue(uTabW0 + 1, [&] {
                     tc_fence_after();
-                    mbar_wait_bounded(&sm.bar_load[ch % uSlots], load_parity(ch));
-                    mbar_wait_bounded(&sm.bar_load[(ch + 1) % uSlots], load_parity(ch + 1));
+                    bwait(&sm.bar_load[ch % uSlots], load_parity(ch));
+                    bwait(&sm.bar_load[(ch + 1) % uSlots], load_parity(ch + 1));
                     issue_tables(ch + 1);
                 });
             }
@@ -487,7 +525,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.bar_g[tb]);
             }
-            mbar_wait_bounded(&sm.bar_gates[hb], static_cast<unsigned>((ch >> 1) & 1));
+            bwait(&sm.bar_gates[hb], static_cast<unsigned>((ch >> 1) & 1));
             __syncwarp();
             const float4 gt = sm.gts[hb][t];               // beta, e^cum, e^{cum_31 - cum}
             const float cum_t = sm.cum[hb][t];
@@ -696,6 +734,11 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
             if (ch + 1 < nchunks) bar_arrive(uBarTdone, 64 + uST);
             bar_arrive(uBarFull0 + tb, uNT);
         }
+        if (warp == uTabW0 + 1) {                          // this warp's table MMAs drained
+            drain(1);
+            if (lane == 0) mbar_arrive(&sm.bar_tabdone);
+            __syncwarp();
+        }
         return;
     }
 
@@ -713,8 +756,11 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
     }
 
     // tensor-map copies of chunk c into slot c % uSlots (one thread); rows past the end read 0
+    int last_issued[uSlots] = {-1, -1, -1, -1};           // per slot (thread stid == 0)
     auto issue_chunk = [&](int c) {
+        if (*abandon) return;
         const int slot = c % uSlots, t0 = c * uC;
+        last_issued[slot] = c;
         uint64_t *bar = &sm.bar_load[slot];
         char *kqs = reinterpret_cast<char *>(&sm.kq[slot][0]);
         mbar_arrive_expect_tx(bar, chunk_bytes);
@@ -736,6 +782,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
                        : make_float4(0.f, 0.f, 0.f, 0.f);
     const float inv_d = 1.0f / static_cast<float>(D);
     auto emit = [&](int c) {
+        if (*abandon) return;                              // no stores once abandoned
         const int hb = c & 1, slot = c % uSlots;
         const int t0 = c * uC, nt = min(uC, S - t0);
         for (int base = 4 * sw; base < nt; base += 4 * uStgW) {
@@ -834,7 +881,7 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
         }
         // q norms of chunk ch (warps 0-3: token 8 w + lane % 8, pieces lane / 8 + 4 i)
         if (sw < 4) {
-            mbar_wait_bounded(&sm.bar_load[slot], load_parity(ch));
+            bwait(&sm.bar_load[slot], load_parity(ch));
             const int tok = sw * 8 + (lane & 7), nq = lane >> 3;
             const char *kqs = reinterpret_cast<const char *>(&sm.kq[slot][0]);
             float ss = 0.f;
@@ -863,6 +910,11 @@ gdn_scan_umma_kernel(const __grid_constant__ gdn_params p, const __grid_constant
     for (int ch = max(0, nchunks - 2); ch < nchunks; ch++) {
         bar_sync(uBarEmpty0 + (ch & 1), uRT + uST);
         emit(ch);
+    }
+    // the copies this thread issued have landed (all consumed already unless the CTA abandoned)
+    if (stid == 0) {
+        for (int sl = 0; sl < uSlots; sl++)
+            if (last_issued[sl] >= 0) mbar_wait_bounded(&sm.bar_load[sl], load_parity(last_issued[sl]));
     }
 }
 

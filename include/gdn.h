@@ -79,11 +79,14 @@ typedef enum {
 } gdn_status;
 
 /* Option bits of gdn_params.flags.
- *   GDN_FLAG_SCAN_TMEM  gdn_scan only (gdn_decode_step rejects it): run the chunked kernel that
- *                       keeps each head's memory in tensor memory and does every product on
- *                       tcgen05 MMAs, where it applies (bf16 activations, Dk == Dv == 128);
- *                       other shapes run the default kernel.  Same results within the scan
- *                       tolerance; the default kernel is faster on the reference workloads. */
+ *   By default gdn_scan runs, for bf16 or f16 activations with Dk == Dv == 128 (16-byte aligned
+ *   q, k, v), the chunked kernel that writes the recurrence over 64-token chunks in WY form on
+ *   tcgen05 tensor cores, and for every other shape the 16-token block kernel on warp-level
+ *   MMAs.  Both give the same results within the scan tolerance.
+ *   GDN_FLAG_SCAN_TMEM  gdn_scan only (gdn_decode_step rejects it): run instead the 32-token
+ *                       look-ahead kernel that keeps each head's memory in tensor memory, where
+ *                       it applies (bf16 activations, Dk == Dv == 128); other shapes run the
+ *                       16-token block kernel. */
 #define GDN_FLAG_SCAN_TMEM 1
 /*   GDN_FLAG_HOST_IO    gdn_decode_step only (gdn_scan rejects it): q, k, v, z, log_decay,
  *                       beta and y may live in pinned host memory that is mapped into the
@@ -95,6 +98,9 @@ typedef enum {
  *                       device memory.  Device pointers remain valid with the flag.  Passing
  *                       memory the device cannot address is a fault, as with any bad pointer. */
 #define GDN_FLAG_HOST_IO 2
+/*   GDN_FLAG_SCAN_BLOCK16  gdn_scan (and gdn_scan_split) only: run the 16-token block kernel
+ *                       for every shape, also where the chunked kernel applies. */
+#define GDN_FLAG_SCAN_BLOCK16 4
 
 /* Operands of one call.  Shape fields follow GDNShape (num_key_heads = Hk, num_value_heads
  * = Hv, key_head_dim = Dk, value_head_dim = Dv) plus batch B and sequence length S. */
@@ -232,6 +238,19 @@ GDN_API int gdn_device_status(void *stream);
  * Source: none on the pages -- a test hook for the bounded waits.
  */
 GDN_API int gdn_selftest_wait_timeout(void *stream, double limit_ms);
+
+/*
+ * gdn_selftest_scan_wait_limit -- exercises the scan's own bounded waits without a GPU fault:
+ * sets, for later launches of the chunked scan kernel on the current device, the time limit
+ * of the first attempt of each of its mbarrier waits to `limit_us` microseconds (0 restores
+ * the default of about 2 s).  A first attempt that runs out sets the watchdog word, so
+ * gdn_device_status then reports GDN_ERR_TIMEOUT, and the wait is retried with the full limit;
+ * only if that also runs out does the CTA abandon its work.  So with a tiny limit a scan
+ * reports the timeout and still computes correct results.  Synchronises `stream`.  Returns
+ * GDN_ERR_BAD_ARG unless 0 <= limit_us <= 2e6, GDN_ERR_CUDA on a runtime error, else GDN_OK.
+ * Source: none on the pages -- a test hook for the bounded waits.
+ */
+GDN_API int gdn_selftest_scan_wait_limit(void *stream, double limit_us);
 
 /* gdn_version -- GDN_VERSION of the loaded library.
  * Source: none on the pages -- the library's own version number. */

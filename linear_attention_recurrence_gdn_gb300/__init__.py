@@ -26,6 +26,7 @@ LIBRARY = _build.LIBRARY
 GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 GDN_FLAG_SCAN_TMEM = 1          # gdn_params.flags: tensor-memory chunked scan where it applies
 GDN_FLAG_HOST_IO = 2            # gdn_params.flags: decode inputs and y in pinned host memory
+GDN_FLAG_SCAN_BLOCK16 = 4       # gdn_params.flags: the 16-token block scan kernel for every shape
 _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
 
 GDN_OK = 0
@@ -44,7 +45,8 @@ GDN_SCAN_SPLIT_NOALLOC_MAX_BYTES = 16 << 20   # fixed scratch of gdn_scan_split_
 # Symbols declared in include/gdn.h (checked by the tests against the header).
 EXPORTED = ("gdn_decode_step", "gdn_scan", "gdn_scan_split", "gdn_scan_split_workspace",
             "gdn_scan_split_noalloc", "gdn_reject_reason", "gdn_status_string",
-            "gdn_last_error", "gdn_device_status", "gdn_selftest_wait_timeout", "gdn_version")
+            "gdn_last_error", "gdn_device_status", "gdn_selftest_wait_timeout",
+            "gdn_selftest_scan_wait_limit", "gdn_version")
 
 
 class GdnParams(ctypes.Structure):
@@ -103,6 +105,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.gdn_device_status.restype = ctypes.c_int
     lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_void_p, ctypes.c_double]
     lib.gdn_selftest_wait_timeout.restype = ctypes.c_int
+    lib.gdn_selftest_scan_wait_limit.argtypes = [ctypes.c_void_p, ctypes.c_double]
+    lib.gdn_selftest_scan_wait_limit.restype = ctypes.c_int
     lib.gdn_version.argtypes = []
     lib.gdn_version.restype = ctypes.c_int
     if path is None:
@@ -223,11 +227,13 @@ def gdn_decode_step(q, k, v, log_decay, beta, state, y=None, *, z=None, gn=None,
 
 
 def gdn_scan(q, k, v, log_decay, beta, state=None, y=None, *, s0=None, z=None, gn=None,
-             head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None, tmem=False):
+             head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None, tmem=False,
+             block16=False):
     """The recurrence over the time axis from ``s0`` (None = zeros).
 
     Returns ``(y, state)``; ``state`` may be ``s0`` itself (in-place resume).  ``tmem=True``
-    sets GDN_FLAG_SCAN_TMEM (the tensor-memory chunked kernel where it applies).
+    sets GDN_FLAG_SCAN_TMEM (the 32-token look-ahead tensor-memory kernel where it applies);
+    ``block16=True`` sets GDN_FLAG_SCAN_BLOCK16 (the 16-token block kernel for every shape).
     """
     _require_cuda(q, k, v, log_decay, beta, state, y, z, gn, s0)
     if head_major:
@@ -242,7 +248,8 @@ def gdn_scan(q, k, v, log_decay, beta, state=None, y=None, *, s0=None, z=None, g
         state = torch.empty((B, Hv, Dv, Dk), dtype=torch.float32, device=v.device)
     prm = make_params(q, k, v, log_decay, beta, state, y, z=z, gn=gn, s0=s0,
                       head_major=head_major, qk_eps=qk_eps, norm_eps=norm_eps,
-                      flags=GDN_FLAG_SCAN_TMEM if tmem else 0)
+                      flags=(GDN_FLAG_SCAN_TMEM if tmem else 0) |
+                      (GDN_FLAG_SCAN_BLOCK16 if block16 else 0))
     lib = library()
     st = lib.gdn_scan(ctypes.byref(prm), _stream_handle(stream, v.device))
     _raise(lib, st, prm, 0)
@@ -329,6 +336,11 @@ def gdn_device_status(stream=None, device=None) -> int:
 def gdn_selftest_wait_timeout(limit_ms: float = 1.0, stream=None, device=None) -> int:
     """Launch the test hook whose bounded mbarrier wait runs out after ``limit_ms``."""
     return library().gdn_selftest_wait_timeout(_stream_handle(stream, device), float(limit_ms))
+
+
+def gdn_selftest_scan_wait_limit(limit_us: float, stream=None, device=None) -> int:
+    """Set the first-attempt limit of the chunked scan kernel's waits (0 = the default)."""
+    return library().gdn_selftest_scan_wait_limit(_stream_handle(stream, device), float(limit_us))
 
 
 def gdn_version() -> int:

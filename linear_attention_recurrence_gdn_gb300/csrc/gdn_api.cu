@@ -49,12 +49,16 @@ bool supported_dim(int d) { return (d >= 16 && d <= 128 && d % 16 == 0) || d == 
 int check(const gdn_params *p, int is_decode, const char **why) {
     *why = nullptr;
     if (p == nullptr) { *why = "params pointer is NULL"; return GDN_ERR_NULL_PTR; }
-    if ((p->flags & ~(GDN_FLAG_SCAN_TMEM | GDN_FLAG_HOST_IO)) != 0) {
+    if ((p->flags & ~(GDN_FLAG_SCAN_TMEM | GDN_FLAG_HOST_IO | GDN_FLAG_SCAN_BLOCK16)) != 0) {
         *why = "unknown flags bit";
         return GDN_ERR_BAD_ARG;
     }
     if (is_decode && (p->flags & GDN_FLAG_SCAN_TMEM)) {
         *why = "flags: GDN_FLAG_SCAN_TMEM applies to gdn_scan only";
+        return GDN_ERR_BAD_ARG;
+    }
+    if (is_decode && (p->flags & GDN_FLAG_SCAN_BLOCK16)) {
+        *why = "flags: GDN_FLAG_SCAN_BLOCK16 applies to gdn_scan only";
         return GDN_ERR_BAD_ARG;
     }
     if (!is_decode && (p->flags & GDN_FLAG_HOST_IO)) {
@@ -265,6 +269,13 @@ int gdn_selftest_wait_timeout(void *stream, double limit_ms) {
     if (!(limit_ms > 0.0 && limit_ms <= 2000.0)) return GDN_ERR_BAD_ARG;
     const uint64_t ns = static_cast<uint64_t>(limit_ms * 1e6);
     return cuda_status(gdn::launch_wait_timeout(static_cast<cudaStream_t>(stream), ns));
+}
+
+int gdn_selftest_scan_wait_limit(void *stream, double limit_us) {
+    if (!(limit_us >= 0.0 && limit_us <= 2e6)) return GDN_ERR_BAD_ARG;
+    const unsigned long long ns = static_cast<unsigned long long>(limit_us * 1e3);
+    return cuda_status(gdn::scan_wy_set_first_wait_limit(limit_us > 0.0 && ns == 0 ? 1 : ns,
+                                                         static_cast<cudaStream_t>(stream)));
 }
 
 int gdn_version(void) { return GDN_VERSION; }

@@ -83,6 +83,14 @@ bool scan_umma_supported(const gdn_params &p);
 cudaError_t launch_scan_umma(const gdn_params &p, cudaStream_t stream);
 cudaError_t scan_umma_watchdog(unsigned *flag, cudaStream_t stream);
 
+// The chunked (WY) scan on tcgen05: bf16 or f16 activations, Dk = Dv = 128, 16-byte aligned
+// q, k, v; its watchdog word; the first-attempt limit of its waits (0 = the default), set only
+// by the self-test hook (synchronises `stream`).
+bool scan_wy_supported(const gdn_params &p);
+cudaError_t launch_scan_wy(const gdn_params &p, cudaStream_t stream);
+cudaError_t scan_wy_watchdog(unsigned *flag, cudaStream_t stream);
+cudaError_t scan_wy_set_first_wait_limit(unsigned long long ns, cudaStream_t stream);
+
 // Reads and clears the scan kernels' watchdog words (synchronises `stream`).
 cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream);
 

@@ -82,6 +82,8 @@ gdn_scan_compose_kernel(const float *s0, const float *M, const float *N, float *
 
 cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
     if ((p.flags & GDN_FLAG_SCAN_TMEM) && scan_umma_supported(p)) return launch_scan_umma(p, stream);
+    if (!(p.flags & (GDN_FLAG_SCAN_TMEM | GDN_FLAG_SCAN_BLOCK16)) && scan_wy_supported(p))
+        return launch_scan_wy(p, stream);
     const ScanSplit whole{1, p.S, 0, nullptr, nullptr, nullptr};
     return launch_scan_dk(p, whole, stream);
 }
@@ -159,7 +161,8 @@ cudaError_t scan_watchdog(unsigned *flag, cudaStream_t stream) {
         scan_watchdog_dk112,
         scan_watchdog_dk128,
         scan_watchdog_dk256,
-        scan_umma_watchdog};
+        scan_umma_watchdog,
+        scan_wy_watchdog};
     unsigned any = 0;
     for (auto read : words) {
         unsigned f = 0;

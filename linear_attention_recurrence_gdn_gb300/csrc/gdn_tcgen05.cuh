@@ -50,6 +50,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // (lane base + i), columns [col, col + N).  `taddr` carries the warp's lane base in bits 16+.
 // Each load waits for its own completion inside the same asm statement, so no instruction can
 // read the destination registers before the data has arrived.
+__device__ __forceinline__ void tm_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        "\n\ttcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tm_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(

@@ -19,17 +19,18 @@
 //     as the A operand of [X | Y], X^T = U^T - S W^T (the corrections d of the chunk, one column
 //     per token), Y^T = S Q^T scaled per token and accumulated with the intra-chunk term into
 //     o, the corrections as A operands of the update and of the intra-chunk output, and one
-//     scratch region for the chunk tables [K;Q] K^T and for W^T;
+//     scratch region for the chunk tables [K;Q] K^T (W^T passes through X's columns);
 //   * every product is a tcgen05 MMA (kind::f16, M = 128, f32 accumulation) issued by one
 //     elected lane; f32 values enter as hi + lo pairs of the activation type (hi.hi + hi.lo +
 //     lo.hi, about 2^-16 relative per product for bf16), raw k, q, v are exact operands;
 //   * k, q, v arrive by tensor-map copies (TMA, 64 tokens x 64 features per box, 128-byte
-//     swizzle) into shared memory, two chunks of k, q in flight;
-//   * warp roles: 4 row warps (the serial chain: split of S into hi / lo, the corrections),
-//     4 output warps (per-token scale of Y, then o, the gated RMSNorm and the y stores),
-//     4 table warps (chunk tables -> A, rk, P, the unit-triangular inverse T in 16 x 16 blocks,
-//     the B operands of U and W, then W^T -> shared memory), one MMA warp (the chain's MMAs),
-//     one load warp (tensor-map copies and the decay products of each chunk);
+//     swizzle) into shared memory, two chunks of k, q resident;
+//   * warp roles: 4 row warps (the serial chain: split of S into hi / lo, the corrections,
+//     the per-token scale of Y, -W into shared memory), 4 output warps (o, the gated RMSNorm
+//     and the y stores), 6 table warps (chunk tables -> A, rk, P, the unit-triangular inverse T
+//     in 16 x 16 blocks, the B operands of U and W; one of them issues the tables and W^T
+//     MMAs), one MMA warp (the chain's MMAs), one load warp (the copies, the decay products and
+//     q norms of each chunk);
 //   * the table warps work one chunk ahead, so the chain per chunk is: split S -> X MMAs ->
 //     corrections -> update MMAs.
 // Every wait is an mbarrier wait with a time limit: a wait that runs out sets the watchdog
@@ -44,6 +45,7 @@
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_mma.cuh"
 #include "gdn_tcgen05.cuh"
 #include "gdn_tma.cuh"
 
@@ -73,11 +75,11 @@ constexpr int kThreads = 32 * kWarps;
 enum : uint32_t {
     TM_S = 0,        // f32 memory, 128 columns
     TM_SHI = 128,    // hi part of S as packed pairs (K = 128 in 64 columns)
-    TM_X = 192,      // U^T - S W^T: the chunk's corrections d, one column per token
+    TM_X = 192,      // W^T (lanes = j), then U^T - S W^T: the corrections d, one column per token
     TM_YO = 256,     // S Q^T, scaled per token, plus the intra-chunk term: o
     TM_VCH = 320, TM_VCL = 352,   // update operand: d_s rk_s G_63 / G_s, hi / lo (K = 64 tokens)
     TM_VUH = 384, TM_VUL = 416,   // intra-chunk operand: d_s, hi / lo
-    TM_SCR = 448,    // [K;Q] K^T (lanes 0-63: k rows, 64-127: q rows), then W^T (lanes = j)
+    TM_SCR = 448,    // [K;Q] K^T (lanes 0-63: k rows, 64-127: q rows)
     TM_COLS = 512
 };
 
@@ -134,7 +136,7 @@ enum Bar {
     B_PFREE = 13,    // 2: intra-chunk output MMAs done (P buffer and o ready)
     B_SPLIT = 15,    // row warps: S split and scaled (4 arrivals)
     B_VP = 16,       // row warps: correction operands written (4)
-    B_WRDY = 17,     // table warps: -W in shared memory (4)
+    B_WRDY = 17,     // row warps: -W in shared memory, W^T read out of X (4)
     B_BU = 18,       // table warps: U's B operand written (4)
     B_YSC = 19,      // output warps: Y scaled (4)
     B_YOFREE = 20,   // output warps: o read out of tensor memory (4)
@@ -196,9 +198,9 @@ __device__ __forceinline__ uint32_t sw_off(int row, int piece) {
     return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + (((piece ^ row) & 7) << 4));
 }
 
-// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void prefetch_l2(const void *ptr, unsigned bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+// One 128-byte line of global memory into L2.
+__device__ __forceinline__ void prefetch_line_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
 __device__ __forceinline__ void prefetch_l1(const void *ptr) {
@@ -220,6 +222,33 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+// One warp's 16 x 8 tile d += L R of f32 operands in shared memory (L 16 x 16 row-major with
+// stride ldl, R 16 x 8 row-major with stride ldr), by mma.sync m16n8k16 on bf16 hi + lo parts
+// (hi.hi + hi.lo + lo.hi, f32 accumulation).  Fragment layouts of the PTX ISA for m16n8k16:
+// lane = 4 g + c holds L rows g, g + 8 at columns 2c, 2c + 1 (+ 8), R rows 2c, 2c + 1 (+ 8) at
+// column g, and d rows g, g + 8 at columns 2c, 2c + 1.
+__device__ __forceinline__ void tile_mma(float (&d)[4], const float *L, int ldl, const float *R, int ldr,
+                                         int lane) {
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const float2 x = *reinterpret_cast<const float2 *>(L + (g + 8 * (e & 1)) * ldl + 2 * c + 8 * (e >> 1));
+        split2(x.x, x.y, ah[e], al[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; e++)
+        split2(R[(2 * c + 8 * e) * ldr + g], R[(2 * c + 1 + 8 * e) * ldr + g], bh[e], bl[e]);
+    mma3(d, ah, al, bh[0], bh[1], bl[0], bl[1]);
+}
+
+// s * d of a tile_mma into a 16 x 8 row-major f32 tile with stride ld.
+__device__ __forceinline__ void tile_store(float *D, int ld, const float (&d)[4], float s, int lane) {
+    const int g = lane >> 2, c = lane & 3;
+    *reinterpret_cast<float2 *>(D + g * ld + 2 * c) = make_float2(s * d[0], s * d[1]);
+    *reinterpret_cast<float2 *>(D + (g + 8) * ld + 2 * c) = make_float2(s * d[2], s * d[3]);
 }
 
 // mbarrier phase test that lets the hardware suspend the warp for up to `hint_ns` while the
@@ -323,15 +352,16 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
         // ================================= row warps ======================================
         const int a = 32 * warp + lane;                    // memory row = tensor-memory lane
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-        // -W of chunk n (row j = this thread's lane of W^T) into the MN-major B operand of X;
-        // the X MMAs of chunk n-1 have read the previous one
+        // -W of chunk n (row j = this thread's lane of W^T, held in X's columns until U^T of n
+        // overwrites them) into the MN-major B operand of X; the X MMAs of chunk n-1 have read
+        // the previous one
         auto w_pass = [&](int n) {
             wait(B_WT, static_cast<unsigned>(n & 1));
             tc_fence_after();
 #pragma unroll 1
             for (int h = 0; h < 2; h++) {
                 float w[32];
-                tm_ld32(tl + TM_SCR + 32 * h, w);
+                tm_ld32(tl + TM_X + 32 * h, w);
 #pragma unroll
                 for (int gg = 0; gg < 4; gg++) {
                     uint32_t hi[4], lo[4];
@@ -553,9 +583,8 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
         for (int n = 0; n < nch; n++) {
             const int pb = n & 1;
             if (warp == kTabW0) {
-                // the scratch is free once the row warps have read W^T of n-1 out of it
-                const bool ok = uniform((n == 0 || wait(B_WRDY, static_cast<unsigned>((n - 1) & 1))) &
-                                        wait(B_LDKQ + pb, static_cast<unsigned>((n >> 1) & 1)));
+                // the scratch is free: the table warps read the tables of n-1 before their inverse
+                const bool ok = uniform(wait(B_LDKQ + pb, static_cast<unsigned>((n >> 1) & 1)));
                 if (ok) {
                     issued = true;
                     if (elect_one()) {
@@ -574,6 +603,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             wait(B_TAB, static_cast<unsigned>(n & 1));
             wait(B_GATES + pb, static_cast<unsigned>((n >> 1) & 1));
             if (n >= 2) wait(B_PFREE + pb, static_cast<unsigned>(((n - 2) >> 1) & 1));
+            if (n >= 1) wait(B_WT, static_cast<unsigned>((n - 1) & 1));   // W^T of n-1 read Bw (= A)
             tc_fence_after();
             const uint32_t slot = kq_slot(n);
             const bool fac = sc.gamma[pb][1] != 0.f;       // uniform: factored exponentials
@@ -706,56 +736,32 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             }
             nbar_sync(NB_TAB, kTabT);
             // ---- off-diagonal blocks.  With H_ik = T_ii A_ik (i > k), stored in A's unused
-            //      upper block (k, i): T_ij = -sum_{k=j}^{i-1} H_ik T_kj, by levels i - j = 1, 2, 3
+            //      upper block (k, i): T_ij = -sum_{k=j}^{i-1} H_ik T_kj, by levels i - j = 1, 2, 3.
+            //      Each 16 x 8 half of an output block is one warp's mma.sync tile (f32 operands
+            //      as bf16 hi + lo, f32 accumulation).
             {
-                // a unit is 2 rows x 1 column of one 16 x 16 block: 128 units per block
-                auto hb = [&](int i, int k, int r, int c) -> float & {
-                    return Am[(16 * k + r) * kAS + 16 * i + c];
-                };
+                const int tw = tt >> 5;                    // 0..5
+                float *Hb = Am;                            // H_ik at Am + 16 k kAS + 16 i, stride kAS
 #pragma unroll 1
-                for (int u = tt; u < 6 * 128; u += kTabT) {
-                    // (i, k) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-                    const int q = u >> 7, cc = u & 15, r0 = ((u >> 4) & 7) * 2;
+                for (int task = tw; task < 12; task += 6) {   // (i, k) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+                    const int q = task >> 1, n0 = 8 * (task & 1);
                     const int i = q < 1 ? 1 : (q < 3 ? 2 : 3);
                     const int k = q < 1 ? 0 : (q < 3 ? q - 1 : q - 3);
-                    const float *tii = Tb + blk(i, i) * 256;
-                    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-                    for (int u4 = 0; u4 < 4; u4++) {
-                        const float4 x0 = *reinterpret_cast<const float4 *>(tii + r0 * 16 + 4 * u4);
-                        const float4 x1 = *reinterpret_cast<const float4 *>(tii + (r0 + 1) * 16 + 4 * u4);
-                        const float *ac = &Am[(16 * i + 4 * u4) * kAS + 16 * k + cc];
-                        const float a0v = ac[0], a1v = ac[kAS], a2v = ac[2 * kAS], a3v = ac[3 * kAS];
-                        acc0 = fmaf(x0.x, a0v, fmaf(x0.y, a1v, fmaf(x0.z, a2v, fmaf(x0.w, a3v, acc0))));
-                        acc1 = fmaf(x1.x, a0v, fmaf(x1.y, a1v, fmaf(x1.z, a2v, fmaf(x1.w, a3v, acc1))));
-                    }
-                    hb(i, k, r0, cc) = acc0;               // upper blocks: never read as A
-                    hb(i, k, r0 + 1, cc) = acc1;
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    tile_mma(d, Tb + blk(i, i) * 256, 16, Am + 16 * i * kAS + 16 * k + n0, kAS, lane);
+                    tile_store(Hb + 16 * k * kAS + 16 * i + n0, kAS, d, 1.f, lane);
                 }
                 nbar_sync(NB_TAB, kTabT);
 #pragma unroll 1
                 for (int L = 1; L < 4; L++) {
+                    const int ntask = 2 * (4 - L);         // blocks (j + L, j), two halves each
+                    if (tw < ntask) {
+                        const int j = tw >> 1, i = j + L, n0 = 8 * (tw & 1);
+                        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-                    for (int u = tt; u < (4 - L) * 128; u += kTabT) {
-                        const int j = u >> 7, i = j + L, cc = u & 15, r0 = ((u >> 4) & 7) * 2;
-                        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 1
-                        for (int k = j; k < i; k++) {
-                            const float *tkj = Tb + blk(k, j) * 256;
-#pragma unroll
-                            for (int v4 = 0; v4 < 16; v4 += 4) {
-                                const float t0v = tkj[v4 * 16 + cc], t1v = tkj[(v4 + 1) * 16 + cc];
-                                const float t2v = tkj[(v4 + 2) * 16 + cc], t3v = tkj[(v4 + 3) * 16 + cc];
-                                const float *p0 = &hb(i, k, r0, v4);
-                                const float4 x0 = *reinterpret_cast<const float4 *>(p0);
-                                const float4 x1 = *reinterpret_cast<const float4 *>(p0 + kAS);
-                                acc0 = fmaf(x0.x, t0v, fmaf(x0.y, t1v, fmaf(x0.z, t2v, fmaf(x0.w, t3v, acc0))));
-                                acc1 = fmaf(x1.x, t0v, fmaf(x1.y, t1v, fmaf(x1.z, t2v, fmaf(x1.w, t3v, acc1))));
-                            }
-                        }
-                        float *tij = Tb + blk(i, j) * 256;
-                        tij[r0 * 16 + cc] = -acc0;
-                        tij[(r0 + 1) * 16 + cc] = -acc1;
+                        for (int k = j; k < i; k++)
+                            tile_mma(d, Hb + 16 * k * kAS + 16 * i, kAS, Tb + blk(k, j) * 256 + n0, 16, lane);
+                        tile_store(Tb + blk(i, j) * 256 + n0, 16, d, -1.f, lane);
                     }
                     nbar_sync(NB_TAB, kTabT);
                 }
@@ -798,15 +804,16 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             fence_proxy_async_smem();
             nbar_sync(NB_TAB, kTabT);                        // B operands complete (A is dead)
             if (warp == kTabW0) {
-                if (uniform(true)) {                       // W^T = K^T Bw^T into the scratch
+                // W^T = K^T Bw^T into X's columns, once the corrections of n-1 are read out
+                if (uniform(n == 0 || wait(B_VP, static_cast<unsigned>((n - 1) & 1)))) {
                     issued = true;
                     if (elect_one()) {
                         tc_fence_after();
 #pragma unroll 1
                         for (int kt = 0; kt < 4; kt++) {
                             const uint64_t ak = desc_mn(slot + kt * 2048, 2 * kBox);
-                            umma_ss(tmem + TM_SCR, ak, desc_k(a_bw + kt * 32), kIdN64Amn, kt > 0);
-                            umma_ss(tmem + TM_SCR, ak, desc_k(a_bw + kBox + kt * 32), kIdN64Amn, true);
+                            umma_ss(tmem + TM_X, ak, desc_k(a_bw + kt * 32), kIdN64Amn, kt > 0);
+                            umma_ss(tmem + TM_X, ak, desc_k(a_bw + kBox + kt * 32), kIdN64Amn, true);
                         }
                         umma_commit(&bar[B_WT]);
                     }
@@ -825,9 +832,10 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
     } else if (warp == kMmaW) {
         // ================================ MMA warp =======================================
         bool issued = false;
-        auto issue_u = [&](int n) {                        // U^T of chunk n into X
+        auto issue_u = [&](int n) {                        // U^T of chunk n into X, once W^T is read
             const bool ok = uniform(wait(B_BU, static_cast<unsigned>(n & 1)) &
-                                    wait(B_LDV, static_cast<unsigned>(n & 1)));
+                                    wait(B_LDV, static_cast<unsigned>(n & 1)) &
+                                    wait(B_WRDY, static_cast<unsigned>(n & 1)));
             if (ok) {
                 issued = true;
                 if (elect_one()) {
@@ -1027,22 +1035,39 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             if (lane == 0) mbar_arrive(&bar[B_GATES + pb]);
         };
         // z rows of chunk n into L2 ahead of the output warps' gathers
-        auto prefetch_z = [&](int n) {
-            if (!gated) return;
+        // the 64 rows (256 bytes each) of one head's tensor in chunk n into L2, two lanes per
+        // row, from the load path (the tensor copy engine's queue stays free for the copies)
+        const int64_t k_ts = p.head_major ? kD : static_cast<int64_t>(p.Hk) * kD;
+        const int64_t k_base = p.head_major ? (static_cast<int64_t>(b) * p.Hk + hk) * S * kD
+                                            : (static_cast<int64_t>(b) * S * p.Hk + hk) * kD;
+        auto prefetch_rows = [&](const void *base, int64_t off, int64_t ts, int n) {
+            const TA *src = static_cast<const TA *>(base) + off;
 #pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const int t = n * kC + lane + 32 * h;
-                if (t < S)
-                    prefetch_l2(static_cast<const TA *>(p.z) + v_base + static_cast<int64_t>(t) * v_ts,
-                                kD * sizeof(TA));
+            for (int i = 0; i < kC / 16; i++) {
+                const int t = n * kC + 16 * i + (lane >> 1);
+                if (t < S) prefetch_line_l2(src + static_cast<int64_t>(t) * ts + 64 * (lane & 1));
             }
+        };
+        auto prefetch_z = [&](int n) {
+            if (gated) prefetch_rows(p.z, v_base, v_ts, n);
+        };
+        // k, q and v of chunk n, ahead of their copies
+        auto prefetch_kqv = [&](int n) {
+            if (n >= nch) return;
+            prefetch_rows(p.k, k_base, k_ts, n);
+            prefetch_rows(p.q, k_base, k_ts, n);
+            prefetch_rows(p.v, v_base, v_ts, n);
         };
         load_kq(0);
         load_v(0);
+        if (nch > 1) {
+            load_kq(1);
+            prefetch_rows(p.v, v_base, v_ts, 1);
+        }
+        prefetch_kqv(2);
         prefetch_z(0);
         gates(0);
         if (nch > 1) {
-            load_kq(1);
             prefetch_z(1);
             gates(1);
         }
@@ -1053,6 +1078,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                 // slot (n+1) & 1 was last read by the update of chunk n-1
                 wait(B_KQFREE + ((n + 1) & 1), static_cast<unsigned>(((n - 1) >> 1) & 1));
                 load_kq(n + 1);
+                prefetch_kqv(n + 2);
                 prefetch_z(n + 1);
                 // the scalars of parity (n+1) & 1 were last read by the output warps' scale
                 // pass of chunk n-1, which precedes its intra-chunk MMAs

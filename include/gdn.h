@@ -79,10 +79,15 @@ typedef enum {
 } gdn_status;
 
 /* Option bits of gdn_params.flags.
- *   By default gdn_scan runs, for bf16 or f16 activations with Dk == Dv == 128 (16-byte aligned
- *   q, k, v), the chunked kernel that writes the recurrence over 64-token chunks in WY form on
- *   tcgen05 tensor cores, and for every other shape the 16-token block kernel on warp-level
- *   MMAs.  Both give the same results within the scan tolerance.
+ *   Two scan kernels give the same results within the scan tolerance: the chunked kernel,
+ *   which writes the recurrence over 64-token chunks in WY form on tcgen05 tensor cores (bf16
+ *   or f16 activations with Dk == Dv == 128 and 16-byte aligned q, k, v; one CTA per head),
+ *   and the 16-token block kernel on warp-level MMAs (every shape; a head's rows may spread
+ *   over a cluster of CTAs).  By default gdn_scan runs the chunked kernel where it applies,
+ *   except for bf16 when the block kernel's launch would give no SM more than one CTA (as
+ *   measured, the block kernel is then faster); every other shape runs the block kernel.
+ *   At most one of GDN_FLAG_SCAN_TMEM, GDN_FLAG_SCAN_BLOCK16 and GDN_FLAG_SCAN_CHUNKED may be
+ *   set.
  *   GDN_FLAG_SCAN_TMEM  gdn_scan only (gdn_decode_step rejects it): run instead the 32-token
  *                       look-ahead kernel that keeps each head's memory in tensor memory, where
  *                       it applies (bf16 activations, Dk == Dv == 128); other shapes run the
@@ -101,6 +106,10 @@ typedef enum {
 /*   GDN_FLAG_SCAN_BLOCK16  gdn_scan (and gdn_scan_split) only: run the 16-token block kernel
  *                       for every shape, also where the chunked kernel applies. */
 #define GDN_FLAG_SCAN_BLOCK16 4
+/*   GDN_FLAG_SCAN_CHUNKED  gdn_scan (and gdn_scan_split) only: run the chunked kernel wherever
+ *                       it applies, also where the default would pick the block kernel;
+ *                       other shapes run the block kernel. */
+#define GDN_FLAG_SCAN_CHUNKED 8
 
 /* Operands of one call.  Shape fields follow GDNShape (num_key_heads = Hk, num_value_heads
  * = Hv, key_head_dim = Dk, value_head_dim = Dv) plus batch B and sequence length S. */

@@ -27,6 +27,7 @@ GDN_F32, GDN_BF16, GDN_F16 = 0, 1, 2
 GDN_FLAG_SCAN_TMEM = 1          # gdn_params.flags: tensor-memory chunked scan where it applies
 GDN_FLAG_HOST_IO = 2            # gdn_params.flags: decode inputs and y in pinned host memory
 GDN_FLAG_SCAN_BLOCK16 = 4       # gdn_params.flags: the 16-token block scan kernel for every shape
+GDN_FLAG_SCAN_CHUNKED = 8       # gdn_params.flags: the chunked scan kernel wherever it applies
 _DTYPE_CODE = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16, torch.float16: GDN_F16}
 
 GDN_OK = 0
@@ -228,12 +229,13 @@ def gdn_decode_step(q, k, v, log_decay, beta, state, y=None, *, z=None, gn=None,
 
 def gdn_scan(q, k, v, log_decay, beta, state=None, y=None, *, s0=None, z=None, gn=None,
              head_major=False, qk_eps=1e-6, norm_eps=1e-6, stream=None, tmem=False,
-             block16=False):
+             block16=False, chunked=False):
     """The recurrence over the time axis from ``s0`` (None = zeros).
 
     Returns ``(y, state)``; ``state`` may be ``s0`` itself (in-place resume).  ``tmem=True``
     sets GDN_FLAG_SCAN_TMEM (the 32-token look-ahead tensor-memory kernel where it applies);
-    ``block16=True`` sets GDN_FLAG_SCAN_BLOCK16 (the 16-token block kernel for every shape).
+    ``block16=True`` sets GDN_FLAG_SCAN_BLOCK16 (the 16-token block kernel for every shape),
+    ``chunked=True`` GDN_FLAG_SCAN_CHUNKED (the chunked kernel wherever it applies).
     """
     _require_cuda(q, k, v, log_decay, beta, state, y, z, gn, s0)
     if head_major:
@@ -249,7 +251,8 @@ def gdn_scan(q, k, v, log_decay, beta, state=None, y=None, *, s0=None, z=None, g
     prm = make_params(q, k, v, log_decay, beta, state, y, z=z, gn=gn, s0=s0,
                       head_major=head_major, qk_eps=qk_eps, norm_eps=norm_eps,
                       flags=(GDN_FLAG_SCAN_TMEM if tmem else 0) |
-                      (GDN_FLAG_SCAN_BLOCK16 if block16 else 0))
+                      (GDN_FLAG_SCAN_BLOCK16 if block16 else 0) |
+                      (GDN_FLAG_SCAN_CHUNKED if chunked else 0))
     lib = library()
     st = lib.gdn_scan(ctypes.byref(prm), _stream_handle(stream, v.device))
     _raise(lib, st, prm, 0)

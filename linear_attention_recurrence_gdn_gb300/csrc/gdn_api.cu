@@ -49,12 +49,22 @@ bool supported_dim(int d) { return (d >= 16 && d <= 128 && d % 16 == 0) || d == 
 int check(const gdn_params *p, int is_decode, const char **why) {
     *why = nullptr;
     if (p == nullptr) { *why = "params pointer is NULL"; return GDN_ERR_NULL_PTR; }
-    if ((p->flags & ~(GDN_FLAG_SCAN_TMEM | GDN_FLAG_HOST_IO | GDN_FLAG_SCAN_BLOCK16)) != 0) {
+    if ((p->flags & ~(GDN_FLAG_SCAN_TMEM | GDN_FLAG_HOST_IO | GDN_FLAG_SCAN_BLOCK16 |
+                      GDN_FLAG_SCAN_CHUNKED)) != 0) {
         *why = "unknown flags bit";
         return GDN_ERR_BAD_ARG;
     }
     if (is_decode && (p->flags & GDN_FLAG_SCAN_TMEM)) {
         *why = "flags: GDN_FLAG_SCAN_TMEM applies to gdn_scan only";
+        return GDN_ERR_BAD_ARG;
+    }
+    const int kernel_bits = p->flags & (GDN_FLAG_SCAN_TMEM | GDN_FLAG_SCAN_BLOCK16 | GDN_FLAG_SCAN_CHUNKED);
+    if (kernel_bits & (kernel_bits - 1)) {
+        *why = "flags: at most one of GDN_FLAG_SCAN_TMEM, GDN_FLAG_SCAN_BLOCK16, GDN_FLAG_SCAN_CHUNKED";
+        return GDN_ERR_BAD_ARG;
+    }
+    if (is_decode && (p->flags & GDN_FLAG_SCAN_CHUNKED)) {
+        *why = "flags: GDN_FLAG_SCAN_CHUNKED applies to gdn_scan only";
         return GDN_ERR_BAD_ARG;
     }
     if (is_decode && (p->flags & GDN_FLAG_SCAN_BLOCK16)) {

@@ -826,16 +826,17 @@ inline int device_sms() {
 // Rows per CTA among the candidates NWS (row warps, largest first): the fewest warps on the
 // busiest SM with every CTA resident at once (a sequential scan must not run in waves); ties go
 // to the larger CTA.  A candidate whose shared memory exceeds this device's limit is skipped.
+// `best` is the chosen candidate's index, `per_sm_out` the CTAs it gives the busiest SM (at once
+// or in waves).
 template <typename TA, int DK, int DV, int... NWS>
-cudaError_t launch_tc_best(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
+cudaError_t choose_tc(const gdn_params &p, const ScanSplit &sp, int *best, int64_t *per_sm_out) {
     constexpr int n = sizeof...(NWS);
     constexpr int nws[n] = {NWS...};
     cudaError_t (*const prep[n])(int *) = {prepare_tc<TA, DK, DV, NWS>...};
-    cudaError_t (*const launch[n])(const gdn_params &, const ScanSplit &, cudaStream_t) = {
-        launch_tc_cfg<TA, DK, DV, NWS>...};
     const int sms = std::max(1, device_sms());
     const int64_t heads = static_cast<int64_t>(p.B) * p.Hv * sp.nseg;   // (segment, head) pairs
-    int best = -1;
+    *best = -1;
+    *per_sm_out = 0;
     int64_t best_cost = INT64_MAX;
     for (int i = 0; i < n; i++) {
         int occ = 0;
@@ -846,9 +847,23 @@ cudaError_t launch_tc_best(const gdn_params &p, const ScanSplit &sp, cudaStream_
         const int64_t per_sm = (ctas + sms - 1) / sms;
         const int64_t waves = (per_sm + occ - 1) / occ;
         const int64_t cost = waves * std::min<int64_t>(per_sm, occ) * nws[i];
-        if (cost < best_cost) { best_cost = cost; best = i; }
+        if (cost < best_cost) {
+            best_cost = cost;
+            *best = i;
+            *per_sm_out = per_sm;
+        }
     }
-    if (best < 0) return cudaErrorInvalidConfiguration;
+    return *best < 0 ? cudaErrorInvalidConfiguration : cudaSuccess;
+}
+
+template <typename TA, int DK, int DV, int... NWS>
+cudaError_t launch_tc_best(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream) {
+    cudaError_t (*const launch[])(const gdn_params &, const ScanSplit &, cudaStream_t) = {
+        launch_tc_cfg<TA, DK, DV, NWS>...};
+    int best = -1;
+    int64_t per_sm = 0;
+    const cudaError_t e = choose_tc<TA, DK, DV, NWS...>(p, sp, &best, &per_sm);
+    if (e != cudaSuccess) return e;
     return launch[best](p, sp, stream);
 }
 

@@ -62,9 +62,11 @@ constexpr int kD = 128;                   // Dk = Dv
 constexpr float kMinLogDecay = -80.0f;    // exp(-80) ~ 1.8e-35: a full reset in f32
 constexpr uint64_t kLimitNs = 2000000000ull;
 
-// warp roles
-constexpr int kEpiW0 = 4;                 // warps 0-3: row warps (lane quarters 0-3); 4-7 output
-constexpr int kTabW0 = 8;                 // 4 table warps; warp 8 issues the table / W MMAs
+// warp roles: three groups of 4 warps (a warp reads tensor-memory lane quarter warp % 4), the
+// MMA warp, the load warp and 2 more table warps
+constexpr int kRowW0 = 0;                 // 4 row warps
+constexpr int kEpiW0 = 4;                 // 4 output warps
+constexpr int kTabW0 = 8;                 // 4 table warps; the first issues the table / W MMAs
 constexpr int kMmaW = 12;                 // issues the chain's MMAs; warp 13 is the load warp
 constexpr int kHelpW0 = 14;               // 2 more table warps (the inverse and B operands)
 constexpr int kWarps = 16;
@@ -348,10 +350,11 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
     const int64_t g_ts = p.head_major ? 1 : p.Hv;
     const int64_t g_base = p.head_major ? head * S : static_cast<int64_t>(b) * S * p.Hv + hv;
 
-    if (warp < kEpiW0) {
+    const bool tab_warp = warp >= kTabW0 && warp < kTabW0 + 4;
+    if (warp >= kRowW0 && warp < kRowW0 + 4) {
         // ================================= row warps ======================================
-        const int a = 32 * warp + lane;                    // memory row = tensor-memory lane
-        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        const int a = 32 * (warp & 3) + lane;              // memory row = tensor-memory lane
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         // -W of chunk n (row j = this thread's lane of W^T, held in X's columns until U^T of n
         // overwrites them) into the MN-major B operand of X; the X MMAs of chunk n-1 have read
         // the previous one
@@ -477,9 +480,9 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                         make_float4(s[4 * i], s[4 * i + 1], s[4 * i + 2], s[4 * i + 3]);
             }
         }
-    } else if (warp < kTabW0) {
+    } else if (warp >= kEpiW0 && warp < kEpiW0 + 4) {
         // ============================== output warps =====================================
-        const int q4 = warp - kEpiW0;
+        const int q4 = warp & 3;
         const int a = 32 * q4 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         const int etid = 32 * q4 + lane;                   // 0..127
@@ -568,12 +571,12 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                     if (t < nt) yc[t * v_ts] = o[t];
             }
         }
-    } else if (warp < kMmaW || warp >= kHelpW0) {
+    } else if (tab_warp || warp >= kHelpW0) {
         // =============================== table warps =====================================
-        // Warps 8-11 (lane quarters 0-3) read the chunk tables out of tensor memory; warps 14,
-        // 15 join them for the triangular inverse and the B operands.
-        const bool tabw = warp < kMmaW;
-        const int q4 = tabw ? warp - kTabW0 : 0;
+        // The four table warps (lane quarters 0-3) read the chunk tables out of tensor memory;
+        // the two helper warps join them for the triangular inverse and the B operands.
+        const bool tabw = tab_warp;
+        const int q4 = tabw ? (warp & 3) : 0;
         const int tt = tabw ? 32 * q4 + lane : 4 * 32 + 32 * (warp - kHelpW0) + lane;   // 0..191
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         float *Am = reinterpret_cast<float *>(smem + OFF_A);        // [64][kAS]

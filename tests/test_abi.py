@@ -108,6 +108,7 @@ def test_valid_params_have_no_reject_reason(lib):
     assert reject(lib, fake_params(S=1, flags=gdn.GDN_FLAG_HOST_IO), 1) is None
     assert reject(lib, fake_params(flags=gdn.GDN_FLAG_SCAN_TMEM), 0) is None
     assert reject(lib, fake_params(flags=gdn.GDN_FLAG_SCAN_BLOCK16), 0) is None
+    assert reject(lib, fake_params(flags=gdn.GDN_FLAG_SCAN_CHUNKED), 0) is None
     # empty sequence: empty tensors may come as NULL pointers, nothing is read or written
     assert reject(lib, fake_params(S=0, y=None, q=None, k=None, v=None, z=None, log_decay=None,
                                    beta=None), 0) is None
@@ -138,8 +139,13 @@ REJECTIONS = [
     (dict(norm_eps=float("nan")), 0, gdn.GDN_ERR_BAD_ARG, "eps"),
     (dict(norm_eps=float("inf")), 0, gdn.GDN_ERR_BAD_ARG, "eps"),
     (dict(head_major=2), 0, gdn.GDN_ERR_BAD_ARG, "head_major"),
-    (dict(flags=8), 0, gdn.GDN_ERR_BAD_ARG, "unknown flags"),
-    (dict(S=1, flags=16), 1, gdn.GDN_ERR_BAD_ARG, "unknown flags"),
+    (dict(flags=16), 0, gdn.GDN_ERR_BAD_ARG, "unknown flags"),
+    (dict(S=1, flags=32), 1, gdn.GDN_ERR_BAD_ARG, "unknown flags"),
+    (dict(S=1, flags=gdn.GDN_FLAG_SCAN_CHUNKED), 1, gdn.GDN_ERR_BAD_ARG, "gdn_scan only"),
+    (dict(flags=gdn.GDN_FLAG_SCAN_CHUNKED | gdn.GDN_FLAG_SCAN_BLOCK16), 0, gdn.GDN_ERR_BAD_ARG,
+     "at most one"),
+    (dict(flags=gdn.GDN_FLAG_SCAN_TMEM | gdn.GDN_FLAG_SCAN_BLOCK16), 0, gdn.GDN_ERR_BAD_ARG,
+     "at most one"),
     (dict(S=1, flags=gdn.GDN_FLAG_SCAN_BLOCK16), 1, gdn.GDN_ERR_BAD_ARG, "gdn_scan only"),
     (dict(S=1, flags=gdn.GDN_FLAG_SCAN_TMEM), 1, gdn.GDN_ERR_BAD_ARG, "gdn_scan only"),
     (dict(flags=gdn.GDN_FLAG_HOST_IO), 0, gdn.GDN_ERR_BAD_ARG, "gdn_decode_step only"),

@@ -52,21 +52,21 @@ def test_tiny_workload():
 @pytest.mark.parametrize("gated", [True, False], ids=["gated", "raw_o"])
 @pytest.mark.parametrize("w", [PREFILL_B4, LONG_B2], ids=lambda w: w.name)
 def test_full_size_scan_matches_oracle(w, gated, kernel):
-    # raw o (no gated norm) as well: rmsnorm would hide a wrong scale on o; both the default
-    # chunked kernel and the 16-token block kernel
+    # raw o (no gated norm) as well: rmsnorm would hide a wrong scale on o; both the chunked
+    # kernel and the 16-token block kernel
     inp = make_inputs(w)
     d = to_dev(inp)
     y, ywhole = guarded(tuple(d["v"].shape))
     st, swhole = guarded((w.B, w.Hv, w.Dv, w.Dk))
     gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, y, s0=d["s0"],
                  z=d["z"] if gated else None, gn=d["gn"] if gated else None,
-                 head_major=w.head_major, block16=kernel == "block16")
+                 head_major=w.head_major, block16=kernel == "block16", chunked=kernel == "chunked")
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == gdn.GDN_OK
     del d
     yr, sr = oracle_ref(inp, gated=gated, head_major=w.head_major)
     ey, es = rel_err(y, yr), rel_err(st, sr)
-    name = ("gdn_scan chunked WY (default)" if kernel == "chunked"
+    name = ("gdn_scan chunked WY (GDN_FLAG_SCAN_CHUNKED)" if kernel == "chunked"
             else "gdn_scan 16-token block (GDN_FLAG_SCAN_BLOCK16)")
     record_margin(w.name, name, "gated y" if gated else "raw o", ey, es, SCAN_TOL)
     assert ey <= SCAN_TOL

@@ -1,6 +1,7 @@
 """GPU parity of the chunked (WY-form, tcgen05) scan kernel against the fp64 oracle.
 
-gdn_scan runs this kernel by default for bf16 and f16 activations with Dk = Dv = 128.  It
+The kernel applies to bf16 and f16 activations with Dk = Dv = 128; these tests select it with
+GDN_FLAG_SCAN_CHUNKED (the default picks it or the block kernel by shape, checked last).  It
 writes the page's per-token recurrence (logicaffeine codegen_cuda::gdn, module description)
 exactly over chunks of 64 tokens: the chunk's corrections D = U - W S^T with U, W from the
 unit-triangular inverse T = (I + A)^-1, the outputs from the chunk-start memory plus the
@@ -31,11 +32,12 @@ def _built():
     gdn.library()
 
 
-def run(d, *, gated=True, head_major=False, s0="inp", block16=False):
+def run(d, *, gated=True, head_major=False, s0="inp", block16=False, auto=False):
     s0v = d["s0"] if s0 == "inp" else s0
     y, st = gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], s0=s0v,
                          z=d["z"] if gated else None, gn=d["gn"] if gated else None,
-                         head_major=head_major, block16=block16)
+                         head_major=head_major, block16=block16,
+                         chunked=not block16 and not auto)
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == gdn.GDN_OK
     return y, st
@@ -96,7 +98,7 @@ def test_chunked_scan_zero_state_null_buffer_and_in_place_resume():
     for a, b in ((0, 50), (50, 150)):
         sl = {k: d[k][:, a:b].contiguous() for k in ("q", "k", "v", "z", "log_decay", "beta")}
         yp, _ = gdn.gdn_scan(sl["q"], sl["k"], sl["v"], sl["log_decay"], sl["beta"], state,
-                             s0=state, z=sl["z"], gn=d["gn"])
+                             s0=state, z=sl["z"], gn=d["gn"], chunked=True)
         parts.append(yp)
     torch.cuda.synchronize()
     assert rel_err(torch.cat(parts, 1), yr) <= SCAN_TOL and rel_err(state, sr) <= SCAN_TOL
@@ -121,3 +123,19 @@ def test_chunked_scan_many_heads_and_zero_keys():
     y, st = run(to_dev(inp))
     yr, sr = oracle_ref(inp)
     assert rel_err(y, yr) <= SCAN_TOL and rel_err(st, sr) <= SCAN_TOL
+
+
+@pytest.mark.parametrize("act,B,Hv,want", [
+    ("f16", 1, 2, "chunked"),          # f16: the chunked kernel at every head count
+    ("bf16", 1, 2, "block16"),         # bf16, one CTA per SM for the block kernel
+    ("bf16", 4, 80, "chunked"),        # bf16, more heads than SMs: the block kernel would stack
+])
+def test_default_kernel_choice(act, B, Hv, want):
+    # the default runs one of the two kernels bit for bit (which one depends on the head count
+    # against this device's SMs: 320 heads exceed any GB300's)
+    w = small_workload(B=B, S=40, Hk=Hv // 2 if Hv > 1 else 1, Hv=Hv, D=128, act=act, seed=605,
+                       s0_std=0.05)
+    d = to_dev(make_inputs(w))
+    y0, s0 = run(d, auto=True)
+    y1, s1 = run(d, block16=want == "block16")
+    assert torch.equal(y0, y1) and torch.equal(s0, s1)

@@ -60,7 +60,7 @@ def test_scan_wait_that_runs_out_is_reported_and_the_scan_stays_correct():
     try:
         assert gdn.gdn_selftest_scan_wait_limit(0.001) == GDN_OK
         y, st = gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], s0=d["s0"],
-                             z=d["z"], gn=d["gn"])
+                             z=d["z"], gn=d["gn"], chunked=True)
         torch.cuda.synchronize()
         assert gdn.gdn_device_status() == GDN_ERR_TIMEOUT
         assert gdn.gdn_device_status() == GDN_OK
@@ -68,7 +68,7 @@ def test_scan_wait_that_runs_out_is_reported_and_the_scan_stays_correct():
     finally:
         assert gdn.gdn_selftest_scan_wait_limit(0.0) == GDN_OK
     y, st = gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], s0=d["s0"],
-                         z=d["z"], gn=d["gn"])
+                         z=d["z"], gn=d["gn"], chunked=True)
     torch.cuda.synchronize()
     assert gdn.gdn_device_status() == GDN_OK
     assert rel_err(y, yr) <= SCAN_TOL and rel_err(st, sr) <= SCAN_TOL

@@ -93,6 +93,20 @@ def scan_tmem_mma_flops(w: Workload) -> int:
     return w.B * w.Hv * per * (tables + pre + d_o + upd + corr)
 
 
+def scan_wy_mma_flops(w: Workload) -> int:
+    """Tensor-core FLOPs the chunked (WY) kernel issues per launch (M = 128, K = 16 MMAs).
+
+    Per head and 64-token chunk: the tables [K; Q] K^T (8 MMAs, N = 64), W^T and U^T (8 each,
+    N = 64: hi and lo B operands over K = 64), X = U^T - S W^T (24, N = 64: hi.hi, hi.lo, lo.hi
+    over K = 128), Y = S Q^T (16, N = 64), the update (8, N = 128) and the intra-chunk output
+    (12, N = 64).  Each M x N x 16 MMA is 2 * 128 * N * 16 FLOP.  The mma.sync tiles of the
+    triangular inverse (under 1%) are not counted.
+    """
+    n = (w.S + 63) // 64
+    per = 2 * 128 * 16
+    return w.B * w.Hv * n * per * ((8 + 8 + 8 + 24 + 16 + 12) * 64 + 8 * 128)
+
+
 def scan_bytes(w: Workload) -> int:
     e = w.elem_bytes
     s0 = 4 * w.B * w.Hv * w.Dv * w.Dk if w.s0_std is not None else 0
@@ -390,16 +404,40 @@ def bench_split(gdn, w: Workload, dev, reps: int):
     return out
 
 
+SCAN_KERNELS = {
+    "chunked": "chunked WY on tcgen05 (GDN_FLAG_SCAN_CHUNKED)",
+    "block16": "16-token block on mma.sync (GDN_FLAG_SCAN_BLOCK16)",
+    "tmem": "tensor-memory 32-token look-ahead (GDN_FLAG_SCAN_TMEM)",
+}
+
+
 def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks: dict,
-               tmem: bool = False):
+               kernel: str = "default"):
+    """gdn_scan on workload `w` with the given kernel ("default": no flag; the line then names
+    the kernel the default ran, found by comparing its output bit for bit with each kernel's)."""
     inp = make_inputs(w)
     d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     y = torch.empty(d["v"].shape, dtype=torch.float32, device=dev)
     st = torch.empty((w.B, w.Hv, w.Dv, w.Dk), dtype=torch.float32, device=dev)
 
-    def run():
+    def call(which):
         gdn.gdn_scan(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], st, y, s0=d["s0"],
-                     z=d["z"], gn=d["gn"], head_major=w.head_major, tmem=tmem)
+                     z=d["z"], gn=d["gn"], head_major=w.head_major, tmem=which == "tmem",
+                     block16=which == "block16", chunked=which == "chunked")
+
+    ran = kernel
+    if kernel == "default":
+        call("default")
+        ref = y.clone()
+        ran = "other"
+        for cand in ("chunked", "block16"):
+            call(cand)
+            if torch.equal(y, ref):
+                ran = cand
+                break
+
+    def run():
+        call(kernel)
 
     run()
     torch.cuda.synchronize(dev)
@@ -425,14 +463,19 @@ def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks:
             "work": "6 Dk Dv FLOP per token-head: the method's own products (S.k, S.q and the "
                     "rank-1 update), whatever the kernel issues",
             "peak_note": f"{peaks['source']} cuBLAS bf16 dense"}
-    if tmem:
+    label = SCAN_KERNELS.get(ran, ran)
+    cfg = dict(w.as_config(), kernel=("default: " + label) if kernel == "default" else label)
+    if ran == "tmem":
         tc = scan_tmem_mma_flops(w) / secs / 1e12
-        cfg = dict(w.as_config(), kernel="tensor-memory chunked (GDN_FLAG_SCAN_TMEM)")
         roof["issued"] = {"achieved": tc, "frac": tc / bf16, "unit": "TFLOP/s",
-                          "work": "tcgen05 MMA FLOPs the chunked kernel issues (tables, "
+                          "work": "tcgen05 MMA FLOPs the tensor-memory kernel issues (tables, "
                                   "[x | y], d, O, update, correction; hi/lo terms counted)"}
+    elif ran == "chunked":
+        tc = scan_wy_mma_flops(w) / secs / 1e12
+        roof["issued"] = {"achieved": tc, "frac": tc / bf16, "unit": "TFLOP/s",
+                          "work": "tcgen05 MMA FLOPs the chunked kernel issues (tables, W, U, "
+                                  "X, Y, update, intra-chunk output; hi/lo terms counted)"}
     else:
-        cfg = dict(w.as_config(), kernel="default")
         roof["issued"] = {"achieved": mma, "frac": mma / bf16, "unit": "TFLOP/s",
                           "frac_of_mma_sync_ceiling": mma / mma_sync_peak,
                           "work": "mma.sync FLOPs the block form issues for its row MMAs (X, "
@@ -450,6 +493,19 @@ def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks:
                                              f"x {sm_mhz:.0f} MHz: the sequential form's "
                                              f"FP32 roofline"},
             "hbm_bytes": scan_bytes(w)}
+
+
+def scan_lines(gdn, workloads, dev, reps: int, sms: int, sm_mhz: float, peaks: dict) -> list:
+    """Per workload: the default gdn_scan, then the other of the two main kernels; then the
+    first workload through the tensor-memory kernel."""
+    out = []
+    for x in workloads:
+        line = bench_scan(gdn, x, dev, reps, sms, sm_mhz, peaks)
+        out.append(line)
+        other = "block16" if "chunked" in line["config"]["kernel"] else "chunked"
+        out.append(bench_scan(gdn, x, dev, reps, sms, sm_mhz, peaks, kernel=other))
+    out.append(bench_scan(gdn, workloads[0], dev, reps, sms, sm_mhz, peaks, kernel="tmem"))
+    return out
 
 
 # ------------------------------------------------------------------- oracle baselines
@@ -608,10 +664,8 @@ def main(argv=None):
         scan_workloads = [x.replace(S=args.scan_S, name=f"{x.name}_S{args.scan_S}")
                           for x in scan_workloads]
     if args.only == "scan":
-        out = [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
-                          peaks["sm_max_mhz"], peaks) for x in scan_workloads]
-        out.append(bench_scan(gdn, scan_workloads[0], dev, args.scan_reps,
-                              props.multi_processor_count, peaks["sm_max_mhz"], peaks, tmem=True))
+        out = scan_lines(gdn, scan_workloads, dev, args.scan_reps, props.multi_processor_count,
+                         peaks["sm_max_mhz"], peaks)
         if rank == 0:
             print(json.dumps({"scan": out}), flush=True)
         return 0
@@ -686,10 +740,8 @@ def main(argv=None):
     if not args.no_scan and args.only == "all":
         sm_mhz = peaks["sm_max_mhz"]
         scan = {"metric": "gdn_scan tokens/sec", "note": "supplementary, not the headline",
-                "workloads": [bench_scan(gdn, x, dev, args.scan_reps, props.multi_processor_count,
-                                         sm_mhz, peaks) for x in scan_workloads]}
-        scan["workloads"].append(bench_scan(gdn, scan_workloads[0], dev, args.scan_reps,
-                                            props.multi_processor_count, sm_mhz, peaks, tmem=True))
+                "workloads": scan_lines(gdn, scan_workloads, dev, args.scan_reps,
+                                        props.multi_processor_count, sm_mhz, peaks)}
     if sampler:
         sampler.stop()
 

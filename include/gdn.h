@@ -25,6 +25,15 @@
  *   head_major = 1:  q,k [B,Hk,S,Dk]   v,z,y [B,Hv,S,Dv]   log_decay,beta [B,Hv,S]
  *   state, s0:       [B,Hv,Dv,Dk] f32, row = value index, column = key index.
  *   gn:              [Dv] f32.
+ *
+ * HEAD DIMS
+ *   Dk and Dv are independent.  Multiples of 16 from 16 to 128, and 256, run the tiled
+ *   kernels (tensor cores, bulk copies).  Any other Dk, Dv from 1 to 256 runs a general
+ *   kernel (f32 on CUDA cores, plain loads, one CTA per head), provided that the head's
+ *   memory with rows padded to an odd length fits in its shared memory:
+ *   Dv * (Dk | 1) * 4 + 8 * Dk + 96 <= 226 KB (e.g. any Dk, Dv up to 232).  Pruned widths
+ *   of any size are allowed by modelopt puzzletron.pruning.gated_delta_net
+ *   (slice_gated_delta_net_state_dict, GDNShape).  Other dims: GDN_ERR_UNSUPPORTED_DIM.
  *   y is always f32: the promoted type of gated_delta_fake on the same page (the memory is
  *   f32 even for a 16-bit model).
  *
@@ -69,7 +78,7 @@ typedef enum {
     GDN_OK = 0,
     GDN_ERR_NULL_PTR = -1,        /* a required pointer is NULL, or z/gn only one given     */
     GDN_ERR_BAD_SHAPE = -2,       /* dims < 0 or heads < 1, Hv % Hk != 0, S != 1 on decode   */
-    GDN_ERR_UNSUPPORTED_DIM = -3, /* Dk or Dv neither 256 nor a multiple of 16 in [16, 128]   */
+    GDN_ERR_UNSUPPORTED_DIM = -3, /* Dk or Dv above 256, or too large a memory (HEAD DIMS)    */
     GDN_ERR_BAD_DTYPE = -4,       /* unknown dtype, or gate dtype neither F32 nor act dtype  */
     GDN_ERR_MISALIGNED = -5,      /* a pointer is not aligned (16 B; gates: element size)    */
     GDN_ERR_ALIASING = -6,        /* y overlaps an operand, or state partially overlaps s0   */
@@ -169,7 +178,9 @@ GDN_API int gdn_scan(const gdn_params *p, void *stream);
  * 1.9x faster with 4 segments, 2.1x with 8, on one sequence of 16384 tokens with 8 heads).
  * `workspace`: device memory of at least gdn_scan_split_workspace(p, segments) bytes, 16-byte
  * aligned, overlapping no operand; the caller owns it.  When the sequence yields a single
- * segment (segments == 1, or S == 1) no workspace is needed and gdn_scan runs.  Errors as gdn_scan, plus GDN_ERR_BAD_ARG for
+ * segment (segments == 1, or S == 1) no workspace is needed and gdn_scan runs; so it does for
+ * head dims of the general kernel (HEAD DIMS above), whose whole sequence runs in one launch
+ * (segments ignored, no workspace).  Errors as gdn_scan, plus GDN_ERR_BAD_ARG for
  * segments < 1, a short workspace or GDN_FLAG_SCAN_TMEM, GDN_ERR_NULL_PTR / MISALIGNED /
  * ALIASING for the workspace (the reason in gdn_last_error()).
  */

@@ -43,7 +43,6 @@ int64_t dtype_bytes(int dt) {
 
 bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-bool supported_dim(int d) { return (d >= 16 && d <= 128 && d % 16 == 0) || d == 256; }
 
 // Returns GDN_OK or a status, and sets *why to a static reason.
 int check(const gdn_params *p, int is_decode, const char **why) {
@@ -87,8 +86,9 @@ int check(const gdn_params *p, int is_decode, const char **why) {
         return GDN_ERR_BAD_ARG;
     }
     if (p->Dk < 1 || p->Dv < 1) { *why = "Dk and Dv must be >= 1"; return GDN_ERR_BAD_SHAPE; }
-    if (!supported_dim(p->Dk) || !supported_dim(p->Dv)) {
-        *why = "Dk and Dv must be multiples of 16 from 16 to 128, or 256";
+    if (!(gdn::tiled_dim(p->Dk) && gdn::tiled_dim(p->Dv)) && !gdn::general_supported(p->Dk, p->Dv)) {
+        *why = "Dk and Dv must be at most 256, with Dv x (Dk rounded up to odd) x 4 bytes of "
+               "memory within 226 KB unless both are multiples of 16 up to 128, or 256";
         return GDN_ERR_UNSUPPORTED_DIM;
     }
     const int64_t eact = dtype_bytes(p->act_dtype);
@@ -252,7 +252,7 @@ const char *gdn_status_string(int status) {
         case GDN_OK: return "ok";
         case GDN_ERR_NULL_PTR: return "a required pointer is NULL (or only one of z, gn given)";
         case GDN_ERR_BAD_SHAPE: return "bad shape (dims, Hv % Hk, or S != 1 on decode)";
-        case GDN_ERR_UNSUPPORTED_DIM: return "unsupported head dim (Dk, Dv: multiples of 16 from 16 to 128, or 256)";
+        case GDN_ERR_UNSUPPORTED_DIM: return "unsupported head dim (above 256, or a memory too large for the general kernel)";
         case GDN_ERR_BAD_DTYPE: return "bad dtype";
         case GDN_ERR_MISALIGNED: return "misaligned pointer";
         case GDN_ERR_ALIASING: return "output overlaps an operand";

@@ -7,6 +7,7 @@
 namespace gdn {
 
 cudaError_t launch_decode(const gdn_params &p, cudaStream_t stream) {
+    if (!tiled_dims(p)) return launch_general(p, true, stream);
     switch (p.act_dtype) {
         case GDN_F32: return launch_decode_f32(p, stream);
         case GDN_BF16: return launch_decode_bf16(p, stream);

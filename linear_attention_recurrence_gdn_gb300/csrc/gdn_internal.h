@@ -87,6 +87,18 @@ cudaError_t scan_umma_watchdog(unsigned *flag, cudaStream_t stream);
 // The chunked (WY) scan on tcgen05: bf16 or f16 activations, Dk = Dv = 128, 16-byte aligned
 // q, k, v; its watchdog word; the first-attempt limit of its waits (0 = the default), set only
 // by the self-test hook (synchronises `stream`).
+// General kernel (gdn_general.cu): any Dk, Dv from 1 to 256 whose memory, rows padded to an odd
+// stride, fits in the shared memory of one CTA; used for the dims the tiled kernels do not take.
+constexpr size_t kGeneralSmemMax = 226 * 1024;
+// Head dims of the tiled kernels (decode, the block and chunked scans, the split scan).
+inline bool tiled_dim(int d) { return (d >= 16 && d <= 128 && d % 16 == 0) || d == 256; }
+inline bool tiled_dims(const gdn_params &p) { return tiled_dim(p.Dk) && tiled_dim(p.Dv); }
+size_t general_smem_bytes(int dk, int dv);
+bool general_supported(int dk, int dv);
+// decode: the memory is read from and written back to `state` (a decode step); else the scan
+// starts from s0 (NULL = zeros) and writes `state`.
+cudaError_t launch_general(const gdn_params &p, bool decode, cudaStream_t stream);
+
 bool scan_wy_supported(const gdn_params &p);
 cudaError_t launch_scan_wy(const gdn_params &p, cudaStream_t stream);
 cudaError_t scan_wy_watchdog(unsigned *flag, cudaStream_t stream);

@@ -81,6 +81,7 @@ gdn_scan_compose_kernel(const float *s0, const float *M, const float *N, float *
 }  // namespace
 
 cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
+    if (!tiled_dims(p)) return launch_general(p, false, stream);
     if ((p.flags & GDN_FLAG_SCAN_TMEM) && scan_umma_supported(p)) return launch_scan_umma(p, stream);
     if (!(p.flags & (GDN_FLAG_SCAN_TMEM | GDN_FLAG_SCAN_BLOCK16)) && scan_wy_supported(p)) {
         if (p.flags & GDN_FLAG_SCAN_CHUNKED) return launch_scan_wy(p, stream);
@@ -108,7 +109,7 @@ static int nseg_of(int S, int nseg) {
 }
 
 size_t scan_split_workspace_floats(const gdn_params &p, int nseg) {
-    if (p.S < 1 || nseg < 1) return 0;
+    if (p.S < 1 || nseg < 1 || !tiled_dims(p)) return 0;   // general dims: one launch, no split
     const int g = nseg_of(p.S, nseg);
     if (g < 2) return 0;
     const size_t bh = static_cast<size_t>(p.B) * p.Hv;
@@ -117,6 +118,7 @@ size_t scan_split_workspace_floats(const gdn_params &p, int nseg) {
 }
 
 cudaError_t launch_scan_split(const gdn_params &p, int nseg, float *ws, cudaStream_t stream) {
+    if (!tiled_dims(p)) return launch_general(p, false, stream);  // the whole sequence in one launch
     const int len = seg_len_of(p.S, nseg);
     const int g = nseg_of(p.S, nseg);
     if (g < 2) return launch_scan(p, stream);

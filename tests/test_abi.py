@@ -118,6 +118,11 @@ def test_valid_params_have_no_reject_reason(lib):
     for dk, dv in ((64, 128), (128, 32), (16, 64), (256, 128), (128, 256), (256, 48)):
         assert reject(lib, fake_params(Dk=dk, Dv=dv), 0) is None
         assert reject(lib, fake_params(Dk=dk, Dv=dv, S=1), 1) is None
+    # any other dims whose memory fits the general kernel
+    for dk, dv in ((40, 40), (64, 72), (144, 64), (1, 1), (100, 72), (232, 232), (255, 9),
+                   (239, 239)):
+        assert reject(lib, fake_params(Dk=dk, Dv=dv), 0) is None
+        assert reject(lib, fake_params(Dk=dk, Dv=dv, S=1), 1) is None
 
 
 REJECTIONS = [
@@ -128,11 +133,10 @@ REJECTIONS = [
     (dict(S=-2), 0, gdn.GDN_ERR_BAD_SHAPE, "B and S"),
     (dict(S=3), 1, gdn.GDN_ERR_BAD_SHAPE, "S == 1"),
     (dict(S=0), 1, gdn.GDN_ERR_BAD_SHAPE, "S == 1"),
-    (dict(Dk=40, Dv=40), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
-    (dict(Dk=240, Dv=256), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
-    (dict(Dk=256, Dv=512), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
-    (dict(Dk=64, Dv=72), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
-    (dict(Dk=144, Dv=64), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "multiples of 16"),
+    (dict(Dk=240, Dv=256), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "226 KB"),   # general: 241 KB
+    (dict(Dk=256, Dv=512), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "at most 256"),
+    (dict(Dk=300, Dv=16), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "at most 256"),
+    (dict(Dk=250, Dv=250, S=1), 1, gdn.GDN_ERR_UNSUPPORTED_DIM, "226 KB"),
     (dict(act_dtype=7), 0, gdn.GDN_ERR_BAD_DTYPE, "act_dtype"),
     (dict(act_dtype=gdn.GDN_BF16, gate_dtype=gdn.GDN_F16), 0, gdn.GDN_ERR_BAD_DTYPE, "gate_dtype"),
     (dict(qk_eps=-1.0), 0, gdn.GDN_ERR_BAD_ARG, "eps"),

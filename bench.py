@@ -393,14 +393,21 @@ def bench_split(gdn, w: Workload, dev, reps: int):
     tokens = w.B * w.S
     out = {"config": w.as_config(), "metric": "tokens/s", "lines": []}
     ms = timed(lambda: gdn.gdn_scan(*args, **kw))
+    y_ref, st_ref = y.clone(), st.clone()
     out["lines"].append({"segments": 1, "ms": ms, "value": tokens / (ms * 1e-3)})
+
+    def rel_diff(a, ref):                # max |a - ref| / (1 + |ref|), the scan tolerance's form
+        return float(((a - ref).abs() / (1 + ref.abs())).max())
+
     for nseg in (2, 4, 8):
         prm = gdn.make_params(*args, z=d["z"], gn=d["gn"], s0=d["s0"], head_major=w.head_major)
         wsb = torch.empty(max(16, gdn.gdn_scan_split_workspace(prm, nseg)), dtype=torch.uint8,
                           device=dev)
         ms_s = timed(lambda: gdn.gdn_scan_split(*args, segments=nseg, workspace=wsb, **kw))
         out["lines"].append({"segments": nseg, "ms": ms_s, "value": tokens / (ms_s * 1e-3),
-                             "speedup": ms / ms_s})
+                             "speedup": ms / ms_s,
+                             "max_rel_diff_vs_gdn_scan": {"y": rel_diff(y, y_ref),
+                                                          "state": rel_diff(st, st_ref)}})
     return out
 
 

@@ -189,7 +189,8 @@ GDN_API int gdn_scan_split(const gdn_params *p, int segments, void *workspace,
 
 /* Workspace bytes gdn_scan_split(p, segments, ...) needs: 0 when it needs none, or when `p`
  * would be rejected by gdn_scan.  (segments - 1) * B * Hv * (Dk + Dv) * Dk + segments * B * Hv
- * * Dv * Dk floats, with segments reduced so that none is empty. */
+ * * Dv * Dk floats, with segments reduced so that none is empty.  Source: none on the pages
+ * (a size query for gdn_scan_split). */
 GDN_API size_t gdn_scan_split_workspace(const gdn_params *p, int segments);
 
 /*

@@ -20,11 +20,13 @@
 //     per token), Y^T = S Q^T scaled per token and accumulated with the intra-chunk term into
 //     o, the corrections as A operands of the update and of the intra-chunk output, and one
 //     scratch region for the chunk tables [K;Q] K^T (W^T passes through X's columns);
-//   * every product is a tcgen05 MMA (kind::f16, M = 128, f32 accumulation) issued by one
-//     elected lane; f32 values enter as hi + lo pairs of the activation type (hi.hi + hi.lo +
-//     lo.hi, about 2^-16 relative per product for bf16), raw k, q, v are exact operands;
+//   * every chunk-sized product is a tcgen05 MMA (kind::f16, M = 128, f32 accumulation) issued
+//     by one elected lane; f32 values enter as hi + lo pairs of the activation type (hi.hi +
+//     hi.lo + lo.hi, about 2^-16 relative per product for bf16), raw k, q, v are exact
+//     operands; the 16 x 16 blocks of the triangular inverse's levels are mma.sync tiles;
 //   * k, q, v arrive by tensor-map copies (TMA, 64 tokens x 64 features per box, 128-byte
-//     swizzle) into shared memory, two chunks of k, q resident;
+//     swizzle) into shared memory, two chunks of k, q resident; the load warp prefetches their
+//     rows (and z's) into L2 two chunks ahead, since a box of 64 strided rows is slow to land;
 //   * warp roles: 4 row warps (the serial chain: split of S into hi / lo, the corrections,
 //     the per-token scale of Y, -W into shared memory), 4 output warps (o, the gated RMSNorm
 //     and the y stores), 6 table warps (chunk tables -> A, rk, P, the unit-triangular inverse T

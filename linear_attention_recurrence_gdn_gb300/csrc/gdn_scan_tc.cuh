@@ -425,7 +425,7 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
         for (int i = ptid; i < nt * C::KPIECES; i += PT) {
             const int tt = i / C::KPIECES, pc = i % C::KPIECES;
             const int64_t off = (t0 + tt) * k_ts;
-            char *dk, *dq;
+            char *dk = nullptr, *dq = nullptr;             // set below (the DIRECT_KQ branch returns)
             if constexpr (EXACT) {
                 dk = reinterpret_cast<char *>(&sm.op.k[c % 3][tt][0]);
                 dq = reinterpret_cast<char *>(&sm.op.q[c % 3][tt][0]);

@@ -53,6 +53,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -774,22 +775,38 @@ gdn_scan_tc_kernel(const gdn_params p, const ScanSplit sp) {
 }
 
 // Occupancy of one variant; a variant whose shared memory exceeds the per-CTA limit of this
-// device reports 0 (the caller then uses a variant with fewer rows per CTA).
+// device reports 0 (the caller then uses a variant with fewer rows per CTA).  Computed once per
+// device (with the kernel's shared-memory attribute set then) and kept: the queries cost more
+// host time than a short scan's launch.
 template <typename TA, int DK, int DV, int NW>
 cudaError_t prepare_tc(int *occupancy) {
     using C = TcCfg<TA, DK, DV, NW>;
+    constexpr int kDevices = 64;
+    static std::atomic<int> cached[kDevices];              // occupancy + 1; 0 = not yet known
     auto kern = gdn_scan_tc_kernel<TA, DK, DV, NW>;
     const int bytes = static_cast<int>(sizeof(TcSmem<TA, DK, DV, NW>));
     *occupancy = 0;
     int dev = 0, limit = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const bool cacheable = dev >= 0 && dev < kDevices;
+    if (cacheable) {
+        const int c = cached[dev].load(std::memory_order_acquire);
+        if (c > 0) {
+            *occupancy = c - 1;
+            return cudaSuccess;
+        }
+    }
     e = cudaDeviceGetAttribute(&limit, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    if (bytes > limit) return cudaSuccess;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, C::NT, bytes);
+    if (bytes <= limit) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, C::NT, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    if (cacheable) cached[dev].store(*occupancy + 1, std::memory_order_release);
+    return cudaSuccess;
 }
 
 template <typename TA, int DK, int DV, int NW>

@@ -44,6 +44,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -1157,9 +1158,18 @@ cudaError_t launch_wy(const gdn_params &p, cudaStream_t stream) {
         !wy_encode_map(&mv, p.v, p, p.Hv))
         return cudaErrorInvalidValue;
     const int bytes = static_cast<int>(kSmemBytes);
-    cudaError_t e = cudaFuncSetAttribute(gdn_scan_wy_kernel<TA>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    // the shared-memory attribute once per device (it persists in the device's context)
+    constexpr int kDevices = 64;
+    static std::atomic<bool> attr_set[kDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kDevices || !attr_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(gdn_scan_wy_kernel<TA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 bytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kDevices) attr_set[dev].store(true, std::memory_order_release);
+    }
     const int64_t ctas = static_cast<int64_t>(p.B) * p.Hv;
     gdn_scan_wy_kernel<TA><<<static_cast<unsigned>(ctas), kThreads, bytes, stream>>>(p, mk, mq, mv);
     return cudaGetLastError();

@@ -118,3 +118,19 @@ def test_general_dims_many_heads():
     torch.cuda.synchronize()
     yr, sr = oracle_ref(inp)
     assert rel_err(y, yr) <= 1e-4 and rel_err(st, sr) <= 1e-4
+
+
+def test_general_dims_host_fed_decode():
+    # GDN_FLAG_HOST_IO: the general kernel reads the inputs from pinned host memory and writes y
+    # there with plain loads and stores
+    w = small_workload(B=3, S=1, Hk=1, Hv=2, Dk=36, Dv=20, act="bf16", seed=904, s0_std=0.1)
+    inp = make_inputs(w)
+    host = {k: inp[k].contiguous().pin_memory()
+            for k in ("q", "k", "v", "z", "log_decay", "beta")}
+    state = inp["s0"].cuda()
+    y = gdn.gdn_decode_step(host["q"], host["k"], host["v"], host["log_decay"], host["beta"],
+                            state, z=host["z"], gn=inp["gn"].cuda(), host_io=True)
+    torch.cuda.synchronize()
+    assert not y.is_cuda
+    yr, sr = oracle_ref(inp)
+    assert rel_err(y, yr) <= DECODE_TOL and rel_err(state, sr) <= DECODE_TOL

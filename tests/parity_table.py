@@ -5,7 +5,7 @@ The full-size parity tests append one JSON line per case to the file named by th
 or raw o), max |gpu - oracle| / (1 + |oracle|) on y and on the final state, and the tolerance.
 
     GDN_PARITY_LOG=/tmp/margins.jsonl python -m pytest tests -m gpu
-    python tests/parity_table.py /tmp/margins.jsonl profiles/parity_errors.md "<command>"
+    python tests/parity_table.py /tmp/margins.jsonl <output table> "<command>"
 """
 from __future__ import annotations
 

@@ -415,7 +415,12 @@ SCAN_KERNELS = {
     "chunked": "chunked WY on tcgen05 (GDN_FLAG_SCAN_CHUNKED)",
     "block16": "16-token block on mma.sync (GDN_FLAG_SCAN_BLOCK16)",
     "tmem": "tensor-memory 32-token look-ahead (GDN_FLAG_SCAN_TMEM)",
+    "general": "general head dims (f32 on CUDA cores)",
 }
+
+
+def _tiled(d: int) -> bool:
+    return (16 <= d <= 128 and d % 16 == 0) or d == 256
 
 
 def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks: dict,
@@ -434,14 +439,20 @@ def bench_scan(gdn, w: Workload, dev, reps: int, sms: int, sm_mhz: float, peaks:
 
     ran = kernel
     if kernel == "default":
-        call("default")
-        ref = y.clone()
-        ran = "other"
-        for cand in ("chunked", "block16"):
-            call(cand)
-            if torch.equal(y, ref):
-                ran = cand
-                break
+        # which kernel the default ran: only one applies outside bf16 / f16 heads of 128
+        if not (_tiled(w.Dk) and _tiled(w.Dv)):
+            ran = "general"
+        elif not (w.act in ("bf16", "f16") and w.Dk == w.Dv == 128):
+            ran = "block16"
+        else:
+            call("default")
+            ref = y.clone()
+            ran = "other"
+            for cand in ("chunked", "block16"):
+                call(cand)
+                if torch.equal(y, ref):
+                    ran = cand
+                    break
 
     def run():
         call(kernel)
@@ -688,10 +699,14 @@ def main(argv=None):
         # dims of 256 (half the heads, so twice the state per token)
         decs = [DECODE_B64.replace(name="decode_bf16_b64_hk16_hv32_dk128_dv64", Dv=64),
                 DECODE_B64.replace(name="decode_bf16_b64_hk8_hv16_d256", Hk=8, Hv=16, Dk=256,
-                                   Dv=256)]
+                                   Dv=256),
+                # head dims that are not multiples of 16: the general kernel
+                DECODE_B64.replace(name="decode_bf16_b64_hk16_hv32_dk100_dv72", Dk=100, Dv=72)]
         scans = [PREFILL_B4.replace(name="prefill_bf16_b4_s4096_hk16_hv32_dk64_dv128", Dk=64),
                  PREFILL_B4.replace(name="prefill_bf16_b4_s4096_hk8_hv16_d256", Hk=8, Hv=16,
-                                    Dk=256, Dv=256)]
+                                    Dk=256, Dv=256),
+                 PREFILL_B4.replace(name="prefill_bf16_b4_s1024_hk16_hv32_dk100_dv72", S=1024,
+                                    Dk=100, Dv=72)]
         lines = []
         for rd in decs:
             dec = bench_decode(gdn, rd, dev, args.steps, args.warmup, world, None)

@@ -73,12 +73,26 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_p
     const int tid = threadIdx.x;
     const int64_t mem = static_cast<int64_t>(Dv) * Dk;
 
-    // the memory: a decode step updates `state` in place; a scan starts from s0 (or zeros)
+    // the memory: a decode step updates `state` in place; a scan starts from s0 (or zeros).
+    // A warp per row at a time, lanes along the row (coalesced, no index division), as
+    // 4-byte asynchronous copies that are all in flight at once.
+    const int warp = tid >> 5, lane = tid & 31;
     const float *from = decode ? p.state : p.s0;
-    for (int64_t i = tid; i < mem; i += kGenThreads) {
-        const int r = static_cast<int>(i / Dk), c = static_cast<int>(i - static_cast<int64_t>(r) * Dk);
-        Sm[r * ld + c] = from ? from[head * mem + i] : 0.f;
+    for (int r = warp; r < Dv; r += kGenWarps) {
+        const float *src = from ? from + head * mem + static_cast<int64_t>(r) * Dk : nullptr;
+        for (int c = lane; c < Dk; c += 32) {
+            if (src) {
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                                 static_cast<uint32_t>(__cvta_generic_to_shared(Sm + r * ld + c))),
+                             "l"(src + c)
+                             : "memory");
+            } else {
+                Sm[r * ld + c] = 0.f;
+            }
+        }
     }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
     const TA *q = static_cast<const TA *>(p.q), *k = static_cast<const TA *>(p.k);
     const TA *v = static_cast<const TA *>(p.v), *z = static_cast<const TA *>(p.z);
     const bool gated = z != nullptr;
@@ -86,46 +100,79 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_p
     const float qscale = rsqrtf(static_cast<float>(Dk));
     float *row = Sm + tid * ld;
 
+    // token t's offsets into q, k / v, z, y / the gates
+    auto kq_off = [&](int t) {
+        return p.head_major ? ((static_cast<int64_t>(b) * p.Hk + hk) * S + t) * Dk
+                            : ((static_cast<int64_t>(b) * S + t) * p.Hk + hk) * Dk;
+    };
+    auto v_off = [&](int t) {
+        return p.head_major ? ((static_cast<int64_t>(b) * p.Hv + hv) * S + t) * Dv
+                            : ((static_cast<int64_t>(b) * S + t) * p.Hv + hv) * Dv;
+    };
+    auto g_off = [&](int t) {
+        return p.head_major ? (static_cast<int64_t>(b) * p.Hv + hv) * S + t
+                            : (static_cast<int64_t>(b) * S + t) * p.Hv + hv;
+    };
+    // this thread's inputs of a token (k, q elements tid and tid + 256; v, z row tid; gates),
+    // loaded a token ahead so the loads' latency overlaps the current token's work
+    float nk0 = 0.f, nq0 = 0.f, nk1 = 0.f, nq1 = 0.f, nv = 0.f, nz = 0.f, ngl = 0.f, ngb = 0.f;
+    auto fetch = [&](int t) {
+        const int64_t ko = kq_off(t), vo = v_off(t), go = g_off(t);
+        nk0 = tid < Dk ? to_f32(k[ko + tid]) : 0.f;
+        nq0 = tid < Dk ? to_f32(q[ko + tid]) : 0.f;
+        nk1 = tid + kGenThreads < Dk ? to_f32(k[ko + tid + kGenThreads]) : 0.f;
+        nq1 = tid + kGenThreads < Dk ? to_f32(q[ko + tid + kGenThreads]) : 0.f;
+        nv = tid < Dv ? to_f32(v[vo + tid]) : 0.f;
+        nz = (gated && tid < Dv) ? to_f32(z[vo + tid]) : 0.f;
+        ngl = load_gate(p.log_decay, p.gate_dtype, go);
+        ngb = load_gate(p.beta, p.gate_dtype, go);
+    };
+    if (S > 0) fetch(0);
     for (int t = 0; t < S; t++) {
-        const int64_t kq_off = p.head_major
-            ? ((static_cast<int64_t>(b) * p.Hk + hk) * S + t) * Dk
-            : ((static_cast<int64_t>(b) * S + t) * p.Hk + hk) * Dk;
-        const int64_t v_off = p.head_major
-            ? ((static_cast<int64_t>(b) * p.Hv + hv) * S + t) * Dv
-            : ((static_cast<int64_t>(b) * S + t) * p.Hv + hv) * Dv;
-        const int64_t g_off = p.head_major ? (static_cast<int64_t>(b) * p.Hv + hv) * S + t
-                                           : (static_cast<int64_t>(b) * S + t) * p.Hv + hv;
+        const int64_t y_off = v_off(t);
         // k, q rows and their sums of squares and dot product
-        float skk = 0.f, sqq = 0.f, skq = 0.f;
-        for (int j = tid; j < Dk; j += kGenThreads) {
-            const float kj = to_f32(k[kq_off + j]), qj = to_f32(q[kq_off + j]);
-            kh[j] = kj;
-            qh[j] = qj;
-            skk = fmaf(kj, kj, skk);
-            sqq = fmaf(qj, qj, sqq);
-            skq = fmaf(kj, qj, skq);
+        const float k0 = nk0, q0 = nq0, k1 = nk1, q1 = nq1, va = nv, za = nz;
+        const float alpha = expf(fmaxf(ngl, kGenMinLogDecay));
+        const float beta = ngb;
+        if (t + 1 < S) fetch(t + 1);
+        if (tid < Dk) {
+            kh[tid] = k0;
+            qh[tid] = q0;
         }
-        const float alpha = expf(fmaxf(load_gate(p.log_decay, p.gate_dtype, g_off), kGenMinLogDecay));
-        const float beta = load_gate(p.beta, p.gate_dtype, g_off);
-        const float va = tid < Dv ? to_f32(v[v_off + tid]) : 0.f;
-        const float za = (gated && tid < Dv) ? to_f32(z[v_off + tid]) : 0.f;
+        if (tid + kGenThreads < Dk) {
+            kh[tid + kGenThreads] = k1;
+            qh[tid + kGenThreads] = q1;
+        }
+        float skk = fmaf(k0, k0, k1 * k1), sqq = fmaf(q0, q0, q1 * q1), skq = fmaf(k0, q0, k1 * q1);
         block_sum3(skk, sqq, skq, red);                    // also orders the kh, qh writes
         const float rk = rsqrtf(skk + p.qk_eps);
         const float rq = rsqrtf(sqq + p.qk_eps) * qscale;
         // row a: u, w against the raw rows, then the update with k^ = rk k
         float o = 0.f;
         if (tid < Dv) {
-            float u = 0.f, w = 0.f;
-            for (int j = 0; j < Dk; j++) {
-                const float s = row[j];
-                u = fmaf(s, kh[j], u);
-                w = fmaf(s, qh[j], w);
+            // four partial sums each, so the shared-memory loads of a row pipeline
+            float u4[4] = {0.f, 0.f, 0.f, 0.f}, w4[4] = {0.f, 0.f, 0.f, 0.f};
+            int j = 0;
+#pragma unroll 2
+            for (; j + 4 <= Dk; j += 4) {
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const float sj = row[j + e];
+                    u4[e] = fmaf(sj, kh[j + e], u4[e]);
+                    w4[e] = fmaf(sj, qh[j + e], w4[e]);
+                }
             }
-            u *= rk;
-            w *= rq;
+            for (; j < Dk; j++) {
+                const float sj = row[j];
+                u4[0] = fmaf(sj, kh[j], u4[0]);
+                w4[0] = fmaf(sj, qh[j], w4[0]);
+            }
+            const float u = ((u4[0] + u4[1]) + (u4[2] + u4[3])) * rk;
+            const float w = ((w4[0] + w4[1]) + (w4[2] + w4[3])) * rq;
             const float coef = beta * (va - alpha * u);
             const float ck = coef * rk;
-            for (int j = 0; j < Dk; j++) row[j] = fmaf(alpha, row[j], ck * kh[j]);
+#pragma unroll 8
+            for (int jj = 0; jj < Dk; jj++) row[jj] = fmaf(alpha, row[jj], ck * kh[jj]);
             o = fmaf(alpha, w, coef * (skq * rk * rq));
         }
         float ya = o;
@@ -135,13 +182,13 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_p
             block_sum3(ss, unused1, unused2, red);
             ya = g * rsqrtf(fmaf(ss, 1.0f / static_cast<float>(Dv), p.norm_eps)) * gna;
         }
-        if (tid < Dv) p.y[v_off + tid] = ya;
+        if (tid < Dv) p.y[y_off + tid] = ya;
         __syncthreads();                                   // kh, qh are rewritten next token
     }
     // the final memory
-    for (int64_t i = tid; i < mem; i += kGenThreads) {
-        const int r = static_cast<int>(i / Dk), c = static_cast<int>(i - static_cast<int64_t>(r) * Dk);
-        p.state[head * mem + i] = Sm[r * ld + c];
+    for (int r = warp; r < Dv; r += kGenWarps) {
+        float *dst = p.state + head * mem + static_cast<int64_t>(r) * Dk;
+        for (int c = lane; c < Dk; c += 32) dst[c] = Sm[r * ld + c];
     }
 }
 

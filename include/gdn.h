@@ -30,10 +30,11 @@
  *   Dk and Dv are independent.  Multiples of 16 from 16 to 128, and 256, run the tiled
  *   kernels (tensor cores, bulk copies).  Any other Dk, Dv from 1 to 256 runs a general
  *   kernel (f32 on CUDA cores, plain loads, one CTA per head), provided that the head's
- *   memory with rows padded to an odd length fits in its shared memory:
- *   Dv * (Dk | 1) * 4 + 8 * Dk + 96 <= 226 KB (e.g. any Dk, Dv up to 232).  Pruned widths
- *   of any size are allowed by modelopt puzzletron.pruning.gated_delta_net
- *   (slice_gated_delta_net_state_dict, GDNShape).  Other dims: GDN_ERR_UNSUPPORTED_DIM.
+ *   memory fits in its shared memory: Dv * ld * 4 + 8 * Dk4 + 96 <= 226 KB, Dk4 being Dk
+ *   rounded up to a multiple of 4 and ld a row stride of Dk4 plus at most 28 floats of bank
+ *   padding (e.g. any Dk, Dv up to 232).  Pruned widths of any size are allowed by modelopt
+ *   puzzletron.pruning.gated_delta_net (slice_gated_delta_net_state_dict, GDNShape).  Other
+ *   dims: GDN_ERR_UNSUPPORTED_DIM.
  *   y is always f32: the promoted type of gated_delta_fake on the same page (the memory is
  *   f32 even for a 16-bit model).
  *

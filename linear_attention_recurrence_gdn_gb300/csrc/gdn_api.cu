@@ -87,8 +87,8 @@ int check(const gdn_params *p, int is_decode, const char **why) {
     }
     if (p->Dk < 1 || p->Dv < 1) { *why = "Dk and Dv must be >= 1"; return GDN_ERR_BAD_SHAPE; }
     if (!(gdn::tiled_dim(p->Dk) && gdn::tiled_dim(p->Dv)) && !gdn::general_supported(p->Dk, p->Dv)) {
-        *why = "Dk and Dv must be at most 256, with Dv x (Dk rounded up to odd) x 4 bytes of "
-               "memory within 226 KB unless both are multiples of 16 up to 128, or 256";
+        *why = "Dk and Dv must be at most 256, with the head's memory (Dv padded rows of Dk "
+               "floats) within 226 KB unless both are multiples of 16 up to 128, or 256";
         return GDN_ERR_UNSUPPORTED_DIM;
     }
     const int64_t eact = dtype_bytes(p->act_dtype);

@@ -8,8 +8,8 @@
 //     u = S k^,  w = S q^,  coef = beta (v - alpha u),  S <- alpha S + coef k^^T,
 //     o = alpha w + coef (k^ . q^),  y = rmsnorm(o * silu(z)) * gn   (or y = o without z).
 // One CTA per (b, hv) head keeps the head's f32 memory in shared memory for the whole sequence
-// (rows padded to an odd stride, so the row threads' column walks hit distinct banks); thread a
-// owns memory row a.  Per token the k, q rows are staged and normalised with one block
+// (rows padded to whole float4s and a bank-spreading stride); 1 to 8 adjacent threads own a
+// memory row and split its float4s.  Per token the k, q rows are staged and normalised with one block
 // reduction, the rows are updated in place, and the gated RMSNorm reduces over the head's rows.
 // A decode step is the same kernel with S = 1.  Plain loads and stores throughout: the operands
 // may sit at any element offset (pinned host memory under GDN_FLAG_HOST_IO included).
@@ -26,8 +26,21 @@ constexpr int kGenThreads = 256;          // >= the largest Dv
 constexpr int kGenWarps = kGenThreads / 32;
 constexpr float kGenMinLogDecay = -80.0f; // exp(-80) ~ 1.8e-35: a full reset in f32
 
-// Row stride of the memory in shared memory: Dk rounded up to odd.
-__host__ __device__ constexpr int gen_ld(int dk) { return dk | 1; }
+// Threads per memory row: the most of 8, 4, 2, 1 with TPR * Dv <= 256 (more threads on the
+// row walks of a small head).
+__host__ __device__ constexpr int gen_tpr(int dv) { return dv <= 32 ? 8 : dv <= 64 ? 4 : dv <= 128 ? 2 : 1; }
+// Dk rounded up to whole float4s (the padding columns stay zero).
+__host__ __device__ constexpr int gen_dk4(int dk) { return (dk + 3) & ~3; }
+// Row stride of the memory in shared memory (floats): dk4 or a little more, with ld / (4 TPR)
+// odd when TPR < 8, so the float4 reads of the 8 / TPR rows one quarter-warp covers fall on
+// distinct banks (at most 8 TPR - 4 floats of padding a row).
+__host__ __device__ constexpr int gen_ld(int dk, int dv) {
+    const int tpr = gen_tpr(dv);
+    int ld = gen_dk4(dk);
+    if (tpr < 8)
+        while (ld % (8 * tpr) != 4 * tpr) ld += 4;
+    return ld;
+}
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -60,28 +73,31 @@ __device__ __forceinline__ void block_sum3(float &a, float &b, float &c, float *
 
 template <typename TA>
 __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_params p, bool decode) {
-    extern __shared__ float gsm[];
-    const int Dk = p.Dk, Dv = p.Dv, S = p.S, ld = gen_ld(Dk);
+    extern __shared__ __align__(16) float gsm[];
+    const int Dk = p.Dk, Dv = p.Dv, S = p.S;
+    const int TPR = gen_tpr(Dv), dk4 = gen_dk4(Dk), ld = gen_ld(Dk, Dv), nc = dk4 / 4;
     float *Sm = gsm;                                       // [Dv][ld]
-    float *kh = Sm + Dv * ld;                              // [Dk]
-    float *qh = kh + Dk;                                   // [Dk]
-    float *red = qh + Dk;                                  // [3][kGenWarps]
+    float *kh = Sm + Dv * ld;                              // [dk4]
+    float *qh = kh + dk4;                                  // [dk4]
+    float *red = qh + dk4;                                 // [3][kGenWarps]
     const int64_t head = blockIdx.x;                       // b * Hv + hv
     const int b = static_cast<int>(head / p.Hv);
     const int hv = static_cast<int>(head - static_cast<int64_t>(b) * p.Hv);
     const int hk = hv / (p.Hv / p.Hk);
     const int tid = threadIdx.x;
+    const int a = tid / TPR, part = tid - a * TPR;         // this thread's row and column part
+    const bool live = a < Dv;
     const int64_t mem = static_cast<int64_t>(Dv) * Dk;
 
     // the memory: a decode step updates `state` in place; a scan starts from s0 (or zeros).
-    // A warp per row at a time, lanes along the row (coalesced, no index division), as
-    // 4-byte asynchronous copies that are all in flight at once.
+    // A warp per row at a time, lanes along the row (coalesced), as 4-byte asynchronous copies
+    // that are all in flight at once; the padding columns are zeroed.
     const int warp = tid >> 5, lane = tid & 31;
     const float *from = decode ? p.state : p.s0;
     for (int r = warp; r < Dv; r += kGenWarps) {
         const float *src = from ? from + head * mem + static_cast<int64_t>(r) * Dk : nullptr;
-        for (int c = lane; c < Dk; c += 32) {
-            if (src) {
+        for (int c = lane; c < ld; c += 32) {
+            if (src && c < Dk) {
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                                  static_cast<uint32_t>(__cvta_generic_to_shared(Sm + r * ld + c))),
                              "l"(src + c)
@@ -96,9 +112,11 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_p
     const TA *q = static_cast<const TA *>(p.q), *k = static_cast<const TA *>(p.k);
     const TA *v = static_cast<const TA *>(p.v), *z = static_cast<const TA *>(p.z);
     const bool gated = z != nullptr;
-    const float gna = (gated && tid < Dv) ? p.gn[tid] : 0.f;
+    const float gna = (gated && live) ? p.gn[a] : 0.f;
     const float qscale = rsqrtf(static_cast<float>(Dk));
-    float *row = Sm + tid * ld;
+    float4 *row4 = reinterpret_cast<float4 *>(Sm + (live ? a : 0) * ld);
+    const float4 *kh4 = reinterpret_cast<const float4 *>(kh);
+    const float4 *qh4 = reinterpret_cast<const float4 *>(qh);
 
     // token t's offsets into q, k / v, z, y / the gates
     auto kq_off = [&](int t) {
@@ -113,76 +131,70 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_p
         return p.head_major ? (static_cast<int64_t>(b) * p.Hv + hv) * S + t
                             : (static_cast<int64_t>(b) * S + t) * p.Hv + hv;
     };
-    // this thread's inputs of a token (k, q elements tid and tid + 256; v, z row tid; gates),
-    // loaded a token ahead so the loads' latency overlaps the current token's work
-    float nk0 = 0.f, nq0 = 0.f, nk1 = 0.f, nq1 = 0.f, nv = 0.f, nz = 0.f, ngl = 0.f, ngb = 0.f;
+    // this thread's inputs of a token (k, q element tid; v, z of its row; the gates), loaded a
+    // token ahead so the loads' latency overlaps the current token's work
+    float nk = 0.f, nq = 0.f, nv = 0.f, nz = 0.f, ngl = 0.f, ngb = 0.f;
     auto fetch = [&](int t) {
         const int64_t ko = kq_off(t), vo = v_off(t), go = g_off(t);
-        nk0 = tid < Dk ? to_f32(k[ko + tid]) : 0.f;
-        nq0 = tid < Dk ? to_f32(q[ko + tid]) : 0.f;
-        nk1 = tid + kGenThreads < Dk ? to_f32(k[ko + tid + kGenThreads]) : 0.f;
-        nq1 = tid + kGenThreads < Dk ? to_f32(q[ko + tid + kGenThreads]) : 0.f;
-        nv = tid < Dv ? to_f32(v[vo + tid]) : 0.f;
-        nz = (gated && tid < Dv) ? to_f32(z[vo + tid]) : 0.f;
+        nk = tid < Dk ? to_f32(k[ko + tid]) : 0.f;
+        nq = tid < Dk ? to_f32(q[ko + tid]) : 0.f;
+        nv = live ? to_f32(v[vo + a]) : 0.f;
+        nz = (gated && live) ? to_f32(z[vo + a]) : 0.f;
         ngl = load_gate(p.log_decay, p.gate_dtype, go);
         ngb = load_gate(p.beta, p.gate_dtype, go);
     };
     if (S > 0) fetch(0);
     for (int t = 0; t < S; t++) {
         const int64_t y_off = v_off(t);
-        // k, q rows and their sums of squares and dot product
-        const float k0 = nk0, q0 = nq0, k1 = nk1, q1 = nq1, va = nv, za = nz;
+        // k, q rows (zero-padded to whole float4s) and their sums of squares and dot product
+        const float kt = nk, qt = nq, va = nv, za = nz;
         const float alpha = expf(fmaxf(ngl, kGenMinLogDecay));
         const float beta = ngb;
         if (t + 1 < S) fetch(t + 1);
-        if (tid < Dk) {
-            kh[tid] = k0;
-            qh[tid] = q0;
+        if (tid < dk4) {
+            kh[tid] = kt;
+            qh[tid] = qt;
         }
-        if (tid + kGenThreads < Dk) {
-            kh[tid + kGenThreads] = k1;
-            qh[tid + kGenThreads] = q1;
-        }
-        float skk = fmaf(k0, k0, k1 * k1), sqq = fmaf(q0, q0, q1 * q1), skq = fmaf(k0, q0, k1 * q1);
+        float skk = kt * kt, sqq = qt * qt, skq = kt * qt;
         block_sum3(skk, sqq, skq, red);                    // also orders the kh, qh writes
         const float rk = rsqrtf(skk + p.qk_eps);
         const float rq = rsqrtf(sqq + p.qk_eps) * qscale;
-        // row a: u, w against the raw rows, then the update with k^ = rk k
+        // row a: u, w against the raw rows (the row's TPR threads take every TPR-th float4),
+        // then the update with k^ = rk k
+        float uu = 0.f, ww = 0.f;
+        if (live) {
+#pragma unroll 4
+            for (int c = part; c < nc; c += TPR) {
+                const float4 s4 = row4[c];
+                uu = dot4(s4, kh4[c], uu);
+                ww = dot4(s4, qh4[c], ww);
+            }
+        }
+        for (int off = 1; off < TPR; off <<= 1) {          // the row's threads are adjacent lanes
+            uu += __shfl_xor_sync(0xffffffffu, uu, off);
+            ww += __shfl_xor_sync(0xffffffffu, ww, off);
+        }
         float o = 0.f;
-        if (tid < Dv) {
-            // four partial sums each, so the shared-memory loads of a row pipeline
-            float u4[4] = {0.f, 0.f, 0.f, 0.f}, w4[4] = {0.f, 0.f, 0.f, 0.f};
-            int j = 0;
-#pragma unroll 2
-            for (; j + 4 <= Dk; j += 4) {
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const float sj = row[j + e];
-                    u4[e] = fmaf(sj, kh[j + e], u4[e]);
-                    w4[e] = fmaf(sj, qh[j + e], w4[e]);
-                }
-            }
-            for (; j < Dk; j++) {
-                const float sj = row[j];
-                u4[0] = fmaf(sj, kh[j], u4[0]);
-                w4[0] = fmaf(sj, qh[j], w4[0]);
-            }
-            const float u = ((u4[0] + u4[1]) + (u4[2] + u4[3])) * rk;
-            const float w = ((w4[0] + w4[1]) + (w4[2] + w4[3])) * rq;
+        if (live) {
+            const float u = uu * rk, w = ww * rq;
             const float coef = beta * (va - alpha * u);
             const float ck = coef * rk;
-#pragma unroll 8
-            for (int jj = 0; jj < Dk; jj++) row[jj] = fmaf(alpha, row[jj], ck * kh[jj]);
+#pragma unroll 4
+            for (int c = part; c < nc; c += TPR) {
+                const float4 s4 = row4[c], k4 = kh4[c];
+                row4[c] = make_float4(fmaf(alpha, s4.x, ck * k4.x), fmaf(alpha, s4.y, ck * k4.y),
+                                      fmaf(alpha, s4.z, ck * k4.z), fmaf(alpha, s4.w, ck * k4.w));
+            }
             o = fmaf(alpha, w, coef * (skq * rk * rq));
         }
         float ya = o;
         if (gated) {
-            const float g = tid < Dv ? o * silu(za) : 0.f;
-            float ss = g * g, unused1 = 0.f, unused2 = 0.f;
+            const float g = live ? o * silu(za) : 0.f;
+            float ss = part == 0 ? g * g : 0.f, unused1 = 0.f, unused2 = 0.f;
             block_sum3(ss, unused1, unused2, red);
             ya = g * rsqrtf(fmaf(ss, 1.0f / static_cast<float>(Dv), p.norm_eps)) * gna;
         }
-        if (tid < Dv) p.y[y_off + tid] = ya;
+        if (live && part == 0) p.y[y_off + a] = ya;
         __syncthreads();                                   // kh, qh are rewritten next token
     }
     // the final memory
@@ -206,7 +218,7 @@ cudaError_t launch_general_typed(const gdn_params &p, bool decode, cudaStream_t 
 }  // namespace
 
 size_t general_smem_bytes(int dk, int dv) {
-    return sizeof(float) * (static_cast<size_t>(dv) * gen_ld(dk) + 2 * static_cast<size_t>(dk) +
+    return sizeof(float) * (static_cast<size_t>(dv) * gen_ld(dk, dv) + 2 * static_cast<size_t>(gen_dk4(dk)) +
                             3 * kGenWarps);
 }
 

@@ -120,7 +120,7 @@ def test_valid_params_have_no_reject_reason(lib):
         assert reject(lib, fake_params(Dk=dk, Dv=dv, S=1), 1) is None
     # any other dims whose memory fits the general kernel
     for dk, dv in ((40, 40), (64, 72), (144, 64), (1, 1), (100, 72), (232, 232), (255, 9),
-                   (239, 239)):
+                   (236, 236)):
         assert reject(lib, fake_params(Dk=dk, Dv=dv), 0) is None
         assert reject(lib, fake_params(Dk=dk, Dv=dv, S=1), 1) is None
 
@@ -137,6 +137,7 @@ REJECTIONS = [
     (dict(Dk=256, Dv=512), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "at most 256"),
     (dict(Dk=300, Dv=16), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "at most 256"),
     (dict(Dk=250, Dv=250, S=1), 1, gdn.GDN_ERR_UNSUPPORTED_DIM, "226 KB"),
+    (dict(Dk=239, Dv=239), 0, gdn.GDN_ERR_UNSUPPORTED_DIM, "226 KB"),   # rows padded to 244
     (dict(act_dtype=7), 0, gdn.GDN_ERR_BAD_DTYPE, "act_dtype"),
     (dict(act_dtype=gdn.GDN_BF16, gate_dtype=gdn.GDN_F16), 0, gdn.GDN_ERR_BAD_DTYPE, "gate_dtype"),
     (dict(qk_eps=-1.0), 0, gdn.GDN_ERR_BAD_ARG, "eps"),

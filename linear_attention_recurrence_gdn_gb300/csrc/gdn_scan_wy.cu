@@ -106,24 +106,29 @@ constexpr uint32_t OFF_TB = OFF_A + 64 * kAS * 4;     // T in 16 x 16 f32 blocks
 constexpr uint32_t OFF_SC = OFF_TB + 10 * 1024;       // per-chunk scalars, see Scal
 constexpr uint32_t kAlignPad = 1024;
 
+// Arrays by chunk parity are written one chunk ahead by another role; the single ones live
+// within one chunk of the table warps.
 struct Scal {
+    float turn[4][4 * 32];   // output warps: 4 tokens x 32 rows of o per warp (16-byte aligned)
     float cum[2][kC];        // chunk-inclusive sums of clamped log_decay (by chunk parity)
     float beta[2][kC];       // beta (0 past the end)
-    float ef[2][kC];         // e^{cum_t - m}, m = cum_31 (used when the chunk is "factored")
-    float eg[2][kC];         // e^{m - cum_t}
-    float gamma[2][4];       // [0] e^{cum_63}; [1] 1 when every |cum_t - m| <= 80 ("factored")
-    float rk[2][kC];         // 1 / ||k_t||
+    float gamma[2][2];       // [0] e^{cum_63}; [1] 1 when every |cum_t - m| <= 80, m = cum_31
     float rq[2][kC];         // 1 / ||q_t|| / sqrt(Dk)
-    float colk[2][kC];       // rk_s e^{m - cum_s}: the column factor of A and P
     float cvec[2][kC];       // rk_t e^{cum_63 - cum_t}: the update's per-token factor
     float ysc[2][kC];        // e^{cum_t} rq_t: the per-token scale of S q_t
-    float bws[2][kC];        // beta_s e^{cum_s} rk_s: W's per-token factor
+    float rk[kC];            // 1 / ||k_t||
+    float colk[kC];          // rk_s e^{m - cum_s}: the column factor of A and P ("factored")
+    float bws[kC];           // beta_s e^{cum_s} rk_s: W's per-token factor
     float red[4][kC];        // gated norm: partial sums of squares per output warp
     float rr[kC];            // gated norm: 1 / rms per token
-    uint64_t bar[32];        // mbarriers (see enum Bar)
+    uint64_t bar[24];        // mbarriers (see enum Bar)
     uint32_t tmem_base;
     int abandon;
 };
+static_assert(offsetof(Scal, turn) % 16 == 0 && offsetof(Scal, cvec) % 8 == 0 &&
+                  offsetof(Scal, colk) % 16 == 0 && offsetof(Scal, bws) % 16 == 0 &&
+                  offsetof(Scal, bar) % 8 == 0 && OFF_SC % 16 == 0,
+              "vector accesses of the scalars");
 constexpr uint32_t kSmemBytes = OFF_SC + static_cast<uint32_t>(sizeof(Scal)) + kAlignPad;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -148,6 +153,7 @@ enum Bar {
     B_DRAIN = 21,    // 2: final commits of the two MMA-issuing warps
     B_COUNT = 23
 };
+static_assert(B_COUNT <= 24, "mbarrier slots");
 
 // named barriers (ids 1-3): table warps, output warps
 enum { NB_TAB = 1, NB_EPI = 2 };
@@ -208,8 +214,13 @@ __device__ __forceinline__ void prefetch_line_l2(const void *ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
-__device__ __forceinline__ void prefetch_l1(const void *ptr) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
+// silu(z) = z / (1 + e^{-z}) with e^x = 2^{x log2 e}, from the hardware's base-2 exponential
+// and reciprocal approximations (ex2.approx, rcp.approx: a few ulp); z -> -inf gives -0.
+__device__ __forceinline__ float silu_ex2(float z) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return z * r;
 }
 
 __device__ __forceinline__ void nbar_sync(int id, int count) {
@@ -485,23 +496,32 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
         }
     } else if (warp >= kEpiW0 && warp < kEpiW0 + 4) {
         // ============================== output warps =====================================
+        // Tensor memory hands thread a row a of o for the chunk's 64 tokens.  For the gated
+        // norm each warp turns its 32 rows through a private shared-memory tile, 4 tokens (one
+        // block) at a time, so that lane 4 j + i then holds rows 4 j .. 4 j + 3 of its warp's 32
+        // for token 4 b + i: z arrives by one 8-byte load per block, a token's squares add up
+        // in the thread and over three shuffles, and y leaves by one 16-byte store per block.
         const int q4 = warp & 3;
-        const int a = 32 * q4 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         const int etid = 32 * q4 + lane;                   // 0..127
-        const float gna = gated ? p.gn[a] : 0.f;
+        const int ti = lane & 3;                           // token of the block
+        const int r0 = 32 * q4 + 4 * (lane >> 2);          // first of the 4 rows after the turn
+        const float4 g4 = gated ? *reinterpret_cast<const float4 *>(p.gn + r0) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float inv_d = 1.0f / static_cast<float>(kD);
-        const unsigned short *zg =
-            gated ? reinterpret_cast<const unsigned short *>(static_cast<const TA *>(p.z)) + v_base + a
-                  : nullptr;
+        const TA *zr = gated ? static_cast<const TA *>(p.z) + v_base + r0 : nullptr;
+        float *tile = sc.turn[q4];                         // 4 tokens x 32 rows
         for (int c = 0; c < nch; c++) {
             const int pb = c & 1;
             const int t0 = c * kC, nt = min(kC, S - t0);
-            // z rows of the chunk into L1 (one 128-byte line per thread: token etid / 2, half
-            // etid % 2 of the row), so the gathers below hit L1
-            if (gated && (etid >> 1) < nt)
-                prefetch_l1(static_cast<const TA *>(p.z) + v_base +
-                            static_cast<int64_t>(t0 + (etid >> 1)) * v_ts + 64 * (etid & 1));
+            // z of the chunk in the turned layout (tokens past the end read the last token's,
+            // never stored), loaded while o is still being computed
+            uint2 zb[16];
+            if (gated) {
+#pragma unroll
+                for (int bk = 0; bk < 16; bk++)
+                    zb[bk] = *reinterpret_cast<const uint2 *>(
+                        zr + static_cast<int64_t>(t0 + min(4 * bk + ti, nt - 1)) * v_ts);
+            }
             // o of the chunk, out of tensor memory at once
             wait(B_PFREE + pb, static_cast<unsigned>((c >> 1) & 1));
             tc_fence_after();
@@ -510,68 +530,73 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             tc_fence_before();
             arrive_warp(B_YOFREE);
             const bool live = !*abandon;
-            if (gated) {
-                // gated RMSNorm over the head's 128 rows, per token.  The z of 32 tokens are
-                // loaded at once (one round trip; rows past the end read as the last token's,
-                // never stored), then 8 tokens at a time are gated and their squares reduced.
-                const unsigned short *zc = zg + static_cast<int64_t>(t0) * v_ts;
+            if (!gated) {
+                // raw o: the natural layout stores it, a warp's 32 rows being 128 contiguous
+                // bytes of a token
+                if (live) {
+                    float *yc = p.y + v_base + static_cast<int64_t>(t0) * v_ts + 32 * q4 + lane;
 #pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    uint32_t zp[16];
-#pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const int t = 32 * h + 2 * i;
-                        zp[i] = static_cast<uint32_t>(zc[min(t, nt - 1) * v_ts]) |
-                                (static_cast<uint32_t>(zc[min(t + 1, nt - 1) * v_ts]) << 16);
-                    }
-#pragma unroll
-                    for (int g = 4 * h; g < 4 * h + 4; g++) {
-                        float r[8];
-#pragma unroll
-                        for (int j = 0; j < 8; j += 2) {
-                            const int t = 8 * g + j;
-                            const float2 zz = O::unpack(zp[(t - 32 * h) >> 1]);
-                            o[t] *= silu_fast(zz.x);
-                            o[t + 1] *= silu_fast(zz.y);
-                            r[j] = o[t] * o[t];
-                            r[j + 1] = o[t + 1] * o[t + 1];
-                        }
-#pragma unroll
-                        for (int off = 4, cnt = 8; off >= 1; off >>= 1, cnt >>= 1) {   // lane L: token L % 8
-                            const bool upper = (lane & off) != 0;
-#pragma unroll
-                            for (int i = 0; i < 4; i++) {
-                                if (i < cnt / 2) {
-                                    const float send = upper ? r[i] : r[i + cnt / 2];
-                                    const float keep = upper ? r[i + cnt / 2] : r[i];
-                                    r[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                                }
-                            }
-                        }
-                        r[0] += __shfl_xor_sync(0xffffffffu, r[0], 8);
-                        r[0] += __shfl_xor_sync(0xffffffffu, r[0], 16);
-                        if (lane < 8) sc.red[q4][8 * g + lane] = r[0];
-                    }
+                    for (int t = 0; t < kC; t++)
+                        if (t < nt) yc[t * v_ts] = o[t];
                 }
-                nbar_sync(NB_EPI, 128);
-                if (etid < kC)
-                    sc.rr[etid] = rsqrtf(fmaf(sc.red[0][etid] + sc.red[1][etid] + sc.red[2][etid] +
-                                                  sc.red[3][etid], inv_d, p.norm_eps));
-                nbar_sync(NB_EPI, 128);
-#pragma unroll
-                for (int j4 = 0; j4 < 16; j4++) {
-                    const float4 r4 = *reinterpret_cast<const float4 *>(&sc.rr[4 * j4]);
-                    o[4 * j4] *= r4.x * gna;
-                    o[4 * j4 + 1] *= r4.y * gna;
-                    o[4 * j4 + 2] *= r4.z * gna;
-                    o[4 * j4 + 3] *= r4.w * gna;
-                }
+                continue;
             }
-            if (live) {
-                float *yc = p.y + v_base + static_cast<int64_t>(t0) * v_ts + a;
+            // the turn: afterwards o[4 b + e] is row r0 + e of token 4 b + ti.  Row r of token e
+            // sits at word 32 e + (r ^ 8 e): the writes of a token cover 32 distinct banks, and
+            // the 16-byte reads of any 8 lanes (rows 4 j .. 4 j + 3 at word 32 i + 4 (j ^ 2 i))
+            // too.  Only shared-memory traffic here, so that the gating below is one batch of
+            // independent work rather than 16 dependent rounds.
 #pragma unroll
-                for (int t = 0; t < kC; t++)
-                    if (t < nt) yc[t * v_ts] = o[t];
+            for (int bk = 0; bk < 16; bk++) {
+#pragma unroll
+                for (int e = 0; e < 4; e++) tile[32 * e + (lane ^ (8 * e))] = o[4 * bk + e];
+                __syncwarp();
+                const float4 v = *reinterpret_cast<const float4 *>(tile + 32 * ti + ((r0 & 31) ^ (8 * ti)));
+                __syncwarp();
+                o[4 * bk] = v.x; o[4 * bk + 1] = v.y; o[4 * bk + 2] = v.z; o[4 * bk + 3] = v.w;
+            }
+            // gated RMSNorm over the head's 128 rows: the gate, this lane's 4 squares per token,
+            // then the warp's 32 (three shuffles per token), then the 4 warps' partial sums
+#pragma unroll
+            for (int bk = 0; bk < 16; bk++) {
+                const float2 za = O::unpack(zb[bk].x), zc2 = O::unpack(zb[bk].y);
+                o[4 * bk] *= silu_ex2(za.x);
+                o[4 * bk + 1] *= silu_ex2(za.y);
+                o[4 * bk + 2] *= silu_ex2(zc2.x);
+                o[4 * bk + 3] *= silu_ex2(zc2.y);
+            }
+            float ss[16];
+#pragma unroll
+            for (int bk = 0; bk < 16; bk++) {
+                ss[bk] = o[4 * bk] * o[4 * bk];
+                ss[bk] = fmaf(o[4 * bk + 1], o[4 * bk + 1], ss[bk]);
+                ss[bk] = fmaf(o[4 * bk + 2], o[4 * bk + 2], ss[bk]);
+                ss[bk] = fmaf(o[4 * bk + 3], o[4 * bk + 3], ss[bk]);
+            }
+#pragma unroll
+            for (int m = 4; m <= 16; m <<= 1) {
+#pragma unroll
+                for (int bk = 0; bk < 16; bk++) ss[bk] += __shfl_xor_sync(0xffffffffu, ss[bk], m);
+            }
+            if (lane < 4) {
+#pragma unroll
+                for (int bk = 0; bk < 16; bk++) sc.red[q4][4 * bk + lane] = ss[bk];
+            }
+            nbar_sync(NB_EPI, 128);
+            if (etid < kC)
+                sc.rr[etid] = rsqrtf(fmaf(sc.red[0][etid] + sc.red[1][etid] + sc.red[2][etid] +
+                                              sc.red[3][etid], inv_d, p.norm_eps));
+            nbar_sync(NB_EPI, 128);
+            if (live) {
+                float *yc = p.y + v_base + static_cast<int64_t>(t0) * v_ts + r0;
+#pragma unroll
+                for (int bk = 0; bk < 16; bk++) {
+                    const int t = 4 * bk + ti;
+                    const float r = sc.rr[t];
+                    const float4 v = make_float4(o[4 * bk] * (r * g4.x), o[4 * bk + 1] * (r * g4.y),
+                                                 o[4 * bk + 2] * (r * g4.z), o[4 * bk + 3] * (r * g4.w));
+                    if (t < nt) *reinterpret_cast<float4 *>(yc + static_cast<int64_t>(t) * v_ts) = v;
+                }
             }
         }
     } else if (tab_warp || warp >= kHelpW0) {
@@ -625,17 +650,17 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                 }
                 const float rk = rsqrtf(dg + p.qk_eps);
                 const float ct = sc.cum[pb][t];
-                sc.rk[pb][t] = rk;
-                sc.colk[pb][t] = rk * sc.eg[pb][t];
+                sc.rk[t] = rk;
+                sc.colk[t] = rk * __expf(fminf(sc.cum[pb][kC / 2 - 1] - ct, 80.f));
                 sc.cvec[pb][t] = rk * __expf(sc.cum[pb][kC - 1] - ct);
-                sc.bws[pb][t] = sc.beta[pb][t] * __expf(ct) * rk;
+                sc.bws[t] = sc.beta[pb][t] * __expf(ct) * rk;
             }
             nbar_sync(NB_TAB, kTabT);                        // rk of the chunk written
             if (tt < kC) {
                 // A[t][s] = beta_t rk_t rk_s e^{cum_t - cum_s} (k_t . k_s), s < t
                 const int t = tt;
-                const float ct = sc.cum[pb][t], bt = sc.beta[pb][t] * sc.rk[pb][t];
-                const float rowf = bt * sc.ef[pb][t];
+                const float ct = sc.cum[pb][t], bt = sc.beta[pb][t] * sc.rk[t];
+                const float rowf = bt * __expf(fminf(ct - sc.cum[pb][kC / 2 - 1], 80.f));
                 if (fac) {                                 // e^{cum_t - cum_s} = ef_t eg_s
 #pragma unroll 1
                     for (int h = 0; h < 2; h++) {          // 32 columns at a time
@@ -644,7 +669,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
 #pragma unroll
                         for (int g4 = 0; g4 < 8; g4++) {
                             const int s0 = 32 * h + 4 * g4;
-                            const float4 c4 = *reinterpret_cast<const float4 *>(&sc.colk[pb][s0]);
+                            const float4 c4 = *reinterpret_cast<const float4 *>(&sc.colk[s0]);
                             const float cf[4] = {c4.x, c4.y, c4.z, c4.w};
                             float a4[4];
 #pragma unroll
@@ -663,7 +688,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                             float vj = 0.f;
 #pragma unroll
                             for (int jj = 0; jj < 8; jj++) vj = jj == j ? v8[jj] : vj;
-                            Am[t * kAS + s_] = s_ < t ? bt * sc.rk[pb][s_] * __expf(ct - sc.cum[pb][s_]) * vj : 0.f;
+                            Am[t * kAS + s_] = s_ < t ? bt * sc.rk[s_] * __expf(ct - sc.cum[pb][s_]) * vj : 0.f;
                         }
                     }
                 }
@@ -671,7 +696,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                 // P[t][s] = e^{cum_t - cum_s} rk_s rq_t (q_t . k_s), s <= t: B of the intra term
                 const int t = tt - kC;
                 const float ct = sc.cum[pb][t], rq = sc.rq[pb][t];
-                const float rowf = rq * sc.ef[pb][t];
+                const float rowf = rq * __expf(fminf(ct - sc.cum[pb][kC / 2 - 1], 80.f));
                 const uint32_t ph = a_p(n), pl = ph + kBox;
                 if (fac) {                                 // e^{cum_t - cum_s} = ef_t eg_s
 #pragma unroll 1
@@ -681,7 +706,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
 #pragma unroll
                         for (int j = 0; j < 32; j++) {
                             const int s_ = 32 * h + j;
-                            v[j] = s_ <= t ? rowf * sc.colk[pb][s_] * v[j] : 0.f;
+                            v[j] = s_ <= t ? rowf * sc.colk[s_] * v[j] : 0.f;
                         }
 #pragma unroll
                         for (int gg = 0; gg < 4; gg++) {
@@ -701,7 +726,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
 #pragma unroll
                         for (int j = 0; j < 8; j++) {
                             const int s_ = 8 * g + j;
-                            v8[j] = s_ <= t ? rq * sc.rk[pb][s_] * __expf(ct - sc.cum[pb][s_]) * v8[j] : 0.f;
+                            v8[j] = s_ <= t ? rq * sc.rk[s_] * __expf(ct - sc.cum[pb][s_]) * v8[j] : 0.f;
                         }
                         uint32_t hi[4], lo[4];
 #pragma unroll
@@ -791,8 +816,8 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                     }
                     const float4 b0 = *reinterpret_cast<const float4 *>(&sc.beta[pb][s0]);
                     const float4 b1 = *reinterpret_cast<const float4 *>(&sc.beta[pb][s0 + 4]);
-                    const float4 w0 = *reinterpret_cast<const float4 *>(&sc.bws[pb][s0]);
-                    const float4 w1 = *reinterpret_cast<const float4 *>(&sc.bws[pb][s0 + 4]);
+                    const float4 w0 = *reinterpret_cast<const float4 *>(&sc.bws[s0]);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(&sc.bws[s0 + 4]);
                     const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
                     const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                     uint32_t uh[4], ul[4], wh[4], wl[4];
@@ -1005,10 +1030,6 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             const float first = __shfl_sync(0xffffffffu, c0, 0);
             sc.cum[pb][lane] = c0;
             sc.cum[pb][lane + 32] = c1;
-            sc.ef[pb][lane] = __expf(fminf(c0 - m, 80.f));
-            sc.ef[pb][lane + 32] = __expf(fminf(c1 - m, 80.f));
-            sc.eg[pb][lane] = __expf(fminf(m - c0, 80.f));
-            sc.eg[pb][lane + 32] = __expf(fminf(m - c1, 80.f));
             sc.beta[pb][lane] = be[0];
             sc.beta[pb][lane + 32] = be[1];
             if (lane == 0) {

@@ -29,10 +29,10 @@
 //     rows (and z's) into L2 two chunks ahead, since a box of 64 strided rows is slow to land;
 //   * warp roles: 4 row warps (the serial chain: split of S into hi / lo, the corrections,
 //     the per-token scale of Y, -W into shared memory), 4 output warps (o, the gated RMSNorm
-//     and the y stores), 6 table warps (chunk tables -> A, rk, P, the unit-triangular inverse T
-//     in 16 x 16 blocks, the B operands of U and W; one of them issues the tables and W^T
-//     MMAs), one MMA warp (the chain's MMAs), one load warp (the copies, the decay products and
-//     q norms of each chunk);
+//     and the y stores), 6 table warps (q norms while the chunk tables MMA runs, then tables
+//     -> A, rk, P, the unit-triangular inverse T in 16 x 16 blocks, the B operands of U and W;
+//     one of them issues the tables and W^T MMAs), one MMA warp (the chain's MMAs), one load
+//     warp (the copies and the decay products of each chunk);
 //   * the table warps work one chunk ahead, so the chain per chunk is: split S -> X MMAs ->
 //     corrections -> update MMAs.
 // Every wait is an mbarrier wait with a time limit: a wait that runs out sets the watchdog
@@ -113,9 +113,8 @@ struct Scal {
     float cum[2][kC];        // chunk-inclusive sums of clamped log_decay (by chunk parity)
     float beta[2][kC];       // beta (0 past the end)
     float gamma[2][2];       // [0] e^{cum_63}; [1] 1 when every |cum_t - m| <= 80, m = cum_31
-    float rq[2][kC];         // 1 / ||q_t|| / sqrt(Dk)
     float cvec[2][kC];       // rk_t e^{cum_63 - cum_t}: the update's per-token factor
-    float ysc[2][kC];        // e^{cum_t} rq_t: the per-token scale of S q_t
+    float ysc[2][kC];        // e^{cum_t} rq_t: the per-token scale of S q_t (table warps)
     float rk[kC];            // 1 / ||k_t||
     float colk[kC];          // rk_s e^{m - cum_s}: the column factor of A and P ("factored")
     float bws[kC];           // beta_s e^{cum_s} rk_s: W's per-token factor
@@ -281,6 +280,19 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, unsigned parit
     return ok != 0;
 }
 
+// Non-blocking test of a phase (acquire semantics, like the waits).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // One bounded attempt: suspending tests until the phase completes or `limit_ns` has passed.
 __device__ __forceinline__ bool wy_wait_for(uint64_t *bar, unsigned parity, uint64_t limit_ns) {
     const unsigned hint = limit_ns < 20000ull ? static_cast<unsigned>(limit_ns) : 20000u;
@@ -347,7 +359,12 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
     const unsigned long long first_ns = g_wy_first_limit_ns;
     volatile int *abandon = &sc.abandon;
 
-    auto wait = [&](int i, unsigned parity) -> bool { return wy_wait(&bar[i], parity, abandon, first_ns); };
+    // a phase already complete is taken inline (most waits of a steady chunk are); otherwise
+    // the out-of-line bounded wait
+    auto wait = [&](int i, unsigned parity) -> bool {
+        if (mbar_test(&bar[i], parity) && !*abandon) return true;
+        return wy_wait(&bar[i], parity, abandon, first_ns);
+    };
     auto uniform = [&](bool ok) { return __all_sync(0xffffffffu, ok && !*abandon); };
     auto arrive_warp = [&](int i) {                        // one arrival per warp
         __syncwarp();
@@ -463,6 +480,8 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             arrive_warp(B_VP);
 
             // S q_t scaled by e^{cum_t} rq_t, in place, before the intra-chunk term is added
+            // (the scales are the table warps', published by their B_BU arrivals of chunk c)
+            wait(B_BU, static_cast<unsigned>(c & 1));
             wait(B_Y, static_cast<unsigned>(c & 1));
             tc_fence_after();
 #pragma unroll 1
@@ -613,6 +632,25 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
         bool issued = false;
         for (int n = 0; n < nch; n++) {
             const int pb = n & 1;
+            // the P rows' q norms (rq carries 1 / sqrt(Dk)) from the chunk's q boxes, while
+            // the tables MMA runs
+            float rq = 0.f;
+            if (tt >= kC && tt < 2 * kC && uniform(wait(B_LDKQ + pb, static_cast<unsigned>((n >> 1) & 1)))) {
+                const int t = tt - kC;
+                const uint32_t qs = kq_slot(n) + kBox;
+                float ss = 0.f;
+#pragma unroll 4
+                for (int pc = 0; pc < 16; pc++) {
+                    const uint4 w = lds128(qs + (pc >> 3) * 2 * kBox + sw_off(t, pc));
+                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const float2 f = O::unpack(u[e]);
+                        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                    }
+                }
+                rq = n * kC + t < S ? rsqrtf(ss + p.qk_eps) * rsqrtf(static_cast<float>(kD)) : 0.f;
+            }
             if (warp == kTabW0) {
                 // the scratch is free: the table warps read the tables of n-1 before their inverse
                 const bool ok = uniform(wait(B_LDKQ + pb, static_cast<unsigned>((n >> 1) & 1)));
@@ -695,7 +733,8 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             } else if (tt < 2 * kC) {
                 // P[t][s] = e^{cum_t - cum_s} rk_s rq_t (q_t . k_s), s <= t: B of the intra term
                 const int t = tt - kC;
-                const float ct = sc.cum[pb][t], rq = sc.rq[pb][t];
+                const float ct = sc.cum[pb][t];
+                sc.ysc[pb][t] = __expf(ct) * rq;               // read by the row warps after B_BU
                 const float rowf = rq * __expf(fminf(ct - sc.cum[pb][kC / 2 - 1], 80.f));
                 const uint32_t ph = a_p(n), pl = ph + kBox;
                 if (fac) {                                 // e^{cum_t - cum_s} = ef_t eg_s
@@ -1002,7 +1041,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             }
             last_v = n;
         };
-        auto gates = [&](int n) {                          // decay products and q norms of chunk n
+        auto gates = [&](int n) {                          // decay products of chunk n
             const int pb = n & 1, t0 = n * kC;
             float g[2], be[2];
 #pragma unroll
@@ -1035,28 +1074,6 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             if (lane == 0) {
                 sc.gamma[pb][0] = expf(tot);
                 sc.gamma[pb][1] = (first - m <= 80.f && m - tot <= 80.f) ? 1.f : 0.f;
-            }
-            // q norms (rq carries 1 / sqrt(Dk)) and the per-token scale of S q, once the k, q
-            // boxes of the chunk have landed
-            wait(B_LDKQ + (n & 1), static_cast<unsigned>((n >> 1) & 1));
-            const uint32_t slot = kq_slot(n);
-#pragma unroll 1
-            for (int h = 0; h < 2; h++) {
-                const int t = lane + 32 * h;
-                float ss = 0.f;
-#pragma unroll 4
-                for (int pc = 0; pc < 16; pc++) {
-                    const uint4 w = lds128(slot + kBox + (pc >> 3) * 2 * kBox + sw_off(t, pc));
-                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const float2 f = O::unpack(u[e]);
-                        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-                    }
-                }
-                const float rq = t0 + t < S ? rsqrtf(ss + p.qk_eps) * rsqrtf(static_cast<float>(kD)) : 0.f;
-                sc.rq[pb][t] = rq;
-                sc.ysc[pb][t] = __expf(h ? c1 : c0) * rq;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_GATES + pb]);

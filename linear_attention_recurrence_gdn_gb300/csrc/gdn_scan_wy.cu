@@ -118,6 +118,7 @@ struct Scal {
     float rk[kC];            // 1 / ||k_t||
     float colk[kC];          // rk_s e^{m - cum_s}: the column factor of A and P ("factored")
     float bws[kC];           // beta_s e^{cum_s} rk_s: W's per-token factor
+    float rqs[kC];           // rq_t, handed from the P-row warps to the helpers
     float red[4][kC];        // gated norm: partial sums of squares per output warp
     float rr[kC];            // gated norm: 1 / rms per token
     uint64_t bar[24];        // mbarriers (see enum Bar)
@@ -623,7 +624,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
         // The four table warps (lane quarters 0-3) read the chunk tables out of tensor memory;
         // the two helper warps join them for the triangular inverse and the B operands.
         const bool tabw = tab_warp;
-        const int q4 = tabw ? (warp & 3) : 0;
+        const int q4 = warp & 3;                           // tensor-memory lane quarter
         const int tt = tabw ? 32 * q4 + lane : 4 * 32 + 32 * (warp - kHelpW0) + lane;   // 0..191
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         float *Am = reinterpret_cast<float *>(smem + OFF_A);        // [64][kAS]
@@ -692,6 +693,8 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                 sc.colk[t] = rk * __expf(fminf(sc.cum[pb][kC / 2 - 1] - ct, 80.f));
                 sc.cvec[pb][t] = rk * __expf(sc.cum[pb][kC - 1] - ct);
                 sc.bws[t] = sc.beta[pb][t] * __expf(ct) * rk;
+            } else if (tt < 2 * kC) {
+                sc.rqs[tt - kC] = rq;
             }
             nbar_sync(NB_TAB, kTabT);                        // rk of the chunk written
             if (tt < kC) {
@@ -730,42 +733,42 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                         }
                     }
                 }
-            } else if (tt < 2 * kC) {
-                // P[t][s] = e^{cum_t - cum_s} rk_s rq_t (q_t . k_s), s <= t: B of the intra term
-                const int t = tt - kC;
+            } else {
+                // P[t][s] = e^{cum_t - cum_s} rk_s rq_t (q_t . k_s), s <= t: B of the intra term.
+                // The P-row warps take columns 0-31, the helpers (same lane quarters) 32-63.
+                const int h = tt >= 2 * kC ? 1 : 0;
+                const int t = tt - kC - kC * h;
                 const float ct = sc.cum[pb][t];
-                sc.ysc[pb][t] = __expf(ct) * rq;               // read by the row warps after B_BU
-                const float rowf = rq * __expf(fminf(ct - sc.cum[pb][kC / 2 - 1], 80.f));
+                const float rqt = h ? sc.rqs[t] : rq;
+                if (!h) sc.ysc[pb][t] = __expf(ct) * rq;       // read by the row warps after B_BU
+                const float rowf = rqt * __expf(fminf(ct - sc.cum[pb][kC / 2 - 1], 80.f));
                 const uint32_t ph = a_p(n), pl = ph + kBox;
                 if (fac) {                                 // e^{cum_t - cum_s} = ef_t eg_s
-#pragma unroll 1
-                    for (int h = 0; h < 2; h++) {          // 32 columns at a time
-                        float v[32];
-                        tm_ld32(tl + TM_SCR + 32 * h, v);
+                    float v[32];
+                    tm_ld32(tl + TM_SCR + 32 * h, v);
 #pragma unroll
-                        for (int j = 0; j < 32; j++) {
-                            const int s_ = 32 * h + j;
-                            v[j] = s_ <= t ? rowf * sc.colk[s_] * v[j] : 0.f;
-                        }
+                    for (int j = 0; j < 32; j++) {
+                        const int s_ = 32 * h + j;
+                        v[j] = s_ <= t ? rowf * sc.colk[s_] * v[j] : 0.f;
+                    }
 #pragma unroll
-                        for (int gg = 0; gg < 4; gg++) {
-                            const int g = 4 * h + gg;
-                            uint32_t hi[4], lo[4];
+                    for (int gg = 0; gg < 4; gg++) {
+                        const int g = 4 * h + gg;
+                        uint32_t hi[4], lo[4];
 #pragma unroll
-                            for (int e = 0; e < 4; e++) O::split2(v[8 * gg + 2 * e], v[8 * gg + 2 * e + 1], hi[e], lo[e]);
-                            sts128(ph + sw_off(t, g), hi[0], hi[1], hi[2], hi[3]);
-                            sts128(pl + sw_off(t, g), lo[0], lo[1], lo[2], lo[3]);
-                        }
+                        for (int e = 0; e < 4; e++) O::split2(v[8 * gg + 2 * e], v[8 * gg + 2 * e + 1], hi[e], lo[e]);
+                        sts128(ph + sw_off(t, g), hi[0], hi[1], hi[2], hi[3]);
+                        sts128(pl + sw_off(t, g), lo[0], lo[1], lo[2], lo[3]);
                     }
                 } else {                                   // a chunk of very fast decay: per element
 #pragma unroll 1
-                    for (int g = 0; g < 8; g++) {
+                    for (int g = 4 * h; g < 4 * h + 4; g++) {
                         float v8[8];
                         tm_ld8(tl + TM_SCR + 8 * g, v8);
 #pragma unroll
                         for (int j = 0; j < 8; j++) {
                             const int s_ = 8 * g + j;
-                            v8[j] = s_ <= t ? rq * sc.rk[s_] * __expf(ct - sc.cum[pb][s_]) * v8[j] : 0.f;
+                            v8[j] = s_ <= t ? rqt * sc.rk[s_] * __expf(ct - sc.cum[pb][s_]) * v8[j] : 0.f;
                         }
                         uint32_t hi[4], lo[4];
 #pragma unroll

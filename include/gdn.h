@@ -94,8 +94,9 @@ typedef enum {
  *   or f16 activations with Dk == Dv == 128 and 16-byte aligned q, k, v; one CTA per head),
  *   and the 16-token block kernel on warp-level MMAs (every shape; a head's rows may spread
  *   over a cluster of CTAs).  By default gdn_scan runs the chunked kernel where it applies,
- *   except for bf16 when the block kernel's launch would give no SM more than one CTA (as
- *   measured, the block kernel is then faster); every other shape runs the block kernel.
+ *   except for bf16 when the block kernel's launch would split each head over several CTAs
+ *   and give no SM more than one CTA (few heads; as measured, the block kernel is then
+ *   faster); every other shape runs the block kernel.
  *   At most one of GDN_FLAG_SCAN_TMEM, GDN_FLAG_SCAN_BLOCK16 and GDN_FLAG_SCAN_CHUNKED may be
  *   set.
  *   GDN_FLAG_SCAN_TMEM  gdn_scan only (gdn_decode_step rejects it): run instead the 32-token

@@ -66,7 +66,9 @@ cudaError_t launch_scan_tc_dk80(const gdn_params &p, const ScanSplit &sp, cudaSt
 cudaError_t launch_scan_tc_dk96(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
 cudaError_t launch_scan_tc_dk112(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
 cudaError_t launch_scan_tc_dk128(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
-cudaError_t scan_tc_dk128_per_sm(const gdn_params &p, int64_t *per_sm);
+// The block kernel's launch plan for Dk = Dv = 128 (16-bit activations): CTAs per SM and per
+// head of the configuration it would choose.
+cudaError_t scan_tc_dk128_plan(const gdn_params &p, int64_t *per_sm, int *ctas_per_head);
 cudaError_t launch_scan_tc_dk256(const gdn_params &p, const ScanSplit &sp, cudaStream_t stream);
 cudaError_t scan_watchdog_dk16(unsigned *flag, cudaStream_t stream);
 cudaError_t scan_watchdog_dk32(unsigned *flag, cudaStream_t stream);

@@ -86,16 +86,18 @@ cudaError_t launch_scan(const gdn_params &p, cudaStream_t stream) {
     if (!(p.flags & (GDN_FLAG_SCAN_TMEM | GDN_FLAG_SCAN_BLOCK16)) && scan_wy_supported(p)) {
         if (p.flags & GDN_FLAG_SCAN_CHUNKED) return launch_scan_wy(p, stream);
         // The chunked kernel runs one CTA per head; the block kernel splits a head's rows over a
-        // cluster of CTAs when heads are few.  Measured on GB300 (S 4096 and 16384, 16 to 256
-        // heads): for f16 the chunked kernel is 1.2-4x faster at every head count (the block
-        // kernel splits f16 rows into bf16 hi + lo, three MMA terms); for bf16 the block kernel
-        // is 1.06-1.35x faster while its launch gives each SM at most one CTA, and 2-2.7x slower
-        // once it stacks CTAs on an SM (at once or in waves).
+        // cluster of CTAs when heads are few.  Measured on GB300 (S 4096, 4 to 256 heads): for
+        // f16 the chunked kernel is 1.35-4.8x faster at every head count (the block kernel
+        // splits f16 rows into bf16 hi + lo, three MMA terms); for bf16 the block kernel is
+        // 1.1-1.17x faster when it splits each head over 2 or 4 CTAs with at most one CTA per
+        // SM (up to 64 heads), the chunked kernel 1.06x faster at one CTA per head (128 heads)
+        // and 2-3x faster once the block kernel stacks CTAs on an SM.
         if (p.act_dtype != GDN_BF16) return launch_scan_wy(p, stream);
         int64_t per_sm = 0;
-        const cudaError_t e = scan_tc_dk128_per_sm(p, &per_sm);
+        int per_head = 1;
+        const cudaError_t e = scan_tc_dk128_plan(p, &per_sm, &per_head);
         if (e != cudaSuccess) return e;
-        if (per_sm > 1) return launch_scan_wy(p, stream);
+        if (per_sm > 1 || per_head == 1) return launch_scan_wy(p, stream);
     }
     const ScanSplit whole{1, p.S, 0, nullptr, nullptr, nullptr};
     return launch_scan_dk(p, whole, stream);

@@ -127,7 +127,8 @@ def test_chunked_scan_many_heads_and_zero_keys():
 
 @pytest.mark.parametrize("act,B,Hv,want", [
     ("f16", 1, 2, "chunked"),          # f16: the chunked kernel at every head count
-    ("bf16", 1, 2, "block16"),         # bf16, one CTA per SM for the block kernel
+    ("bf16", 1, 2, "block16"),         # bf16, few heads: the block kernel splits each over CTAs
+    ("bf16", 4, 32, "chunked"),        # bf16, 128 heads: the block kernel would run one per CTA
     ("bf16", 4, 80, "chunked"),        # bf16, more heads than SMs: the block kernel would stack
 ])
 def test_default_kernel_choice(act, B, Hv, want):

@@ -410,8 +410,10 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             tc_fence_before();
             arrive_warp(B_WRDY);
         };
-        w_pass(0);
-        for (int c = 0; c < nch; c++) {
+        // the memory at the start of chunk c (after the update of c-1; Y of c-1 has read the
+        // hi / lo parts of c-1): split into hi (tensor memory) and lo (shared memory), then
+        // gamma S stored back for the update of c
+        auto split = [&](int c) {
             const int pb = c & 1;
             wait(B_GATES + pb, static_cast<unsigned>((c >> 1) & 1));
             const float gam = sc.gamma[pb][0];
@@ -456,7 +458,11 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             fence_proxy_async_smem();
             tc_fence_before();
             arrive_warp(B_SPLIT);
-
+        };
+        split(0);
+        w_pass(0);
+        for (int c = 0; c < nch; c++) {
+            const int pb = c & 1;
             // corrections d_t = X[a][t] -> intra-chunk operand (d) and update operand (d cvec)
             wait(B_X, static_cast<unsigned>(c & 1));
             tc_fence_after();
@@ -496,7 +502,12 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             tm_wait_st();
             tc_fence_before();
             arrive_warp(B_YSC);
-            if (c + 1 < nch) w_pass(c + 1);                 // X of chunk c is done
+            if (c + 1 < nch) {
+                // the next chunk's split runs here, while the table warps finish its W: only
+                // the W pass then stands between them and the next X MMAs
+                split(c + 1);
+                w_pass(c + 1);                             // X of chunk c is done
+            }
         }
         // final memory row a
         const bool ok = wait(B_UPD, static_cast<unsigned>((nch - 1) & 1));

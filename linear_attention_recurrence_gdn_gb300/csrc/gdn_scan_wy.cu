@@ -744,6 +744,35 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                         }
                     }
                 }
+                // ---- T = (I + A)^-1 in 16 x 16 blocks: the diagonal blocks by forward
+                // substitution, each from the A rows of its own warp (blocks 0, 1: this warp's
+                // rows 0-31; 2, 3: the other's), so a warp barrier suffices
+                __syncwarp();
+                {
+                    const int i = tt >> 4, cs = tt & 15;
+                    float x[16];
+#pragma unroll
+                    for (int r = 0; r < 16; r++) x[r] = r == cs ? 1.f : 0.f;
+#pragma unroll
+                    for (int r = 1; r < 16; r++) {
+                        const float *arow = &Am[(16 * i + r) * kAS + 16 * i];
+                        float acc = 0.f;
+#pragma unroll
+                        for (int u4 = 0; u4 < 4; u4++) {
+                            if (4 * u4 < r) {
+                                const float4 a4 = *reinterpret_cast<const float4 *>(arow + 4 * u4);
+                                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                                for (int e = 0; e < 4; e++)
+                                    if (4 * u4 + e < r) acc = fmaf(av[e], x[4 * u4 + e], acc);
+                            }
+                        }
+                        x[r] -= acc;
+                    }
+                    float *tb = Tb + blk(i, i) * 256;
+#pragma unroll
+                    for (int r = 0; r < 16; r++) tb[r * 16 + cs] = x[r];
+                }
             } else {
                 // P[t][s] = e^{cum_t - cum_s} rk_s rq_t (q_t . k_s), s <= t: B of the intra term.
                 // The P-row warps take columns 0-31, the helpers (same lane quarters) 32-63.
@@ -791,34 +820,7 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                 fence_proxy_async_smem();
             }
             tc_fence_before();
-            nbar_sync(NB_TAB, kTabT);                        // A complete
-            // ---- T = (I + A)^-1 in 16 x 16 blocks: diagonal blocks by forward substitution
-            if (tt < kC) {
-                const int i = tt >> 4, cs = tt & 15;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; r++) x[r] = r == cs ? 1.f : 0.f;
-#pragma unroll
-                for (int r = 1; r < 16; r++) {
-                    const float *arow = &Am[(16 * i + r) * kAS + 16 * i];
-                    float acc = 0.f;
-#pragma unroll
-                    for (int u4 = 0; u4 < 4; u4++) {
-                        if (4 * u4 < r) {
-                            const float4 a4 = *reinterpret_cast<const float4 *>(arow + 4 * u4);
-                            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                            for (int e = 0; e < 4; e++)
-                                if (4 * u4 + e < r) acc = fmaf(av[e], x[4 * u4 + e], acc);
-                        }
-                    }
-                    x[r] -= acc;
-                }
-                float *tb = Tb + blk(i, i) * 256;
-#pragma unroll
-                for (int r = 0; r < 16; r++) tb[r * 16 + cs] = x[r];
-            }
-            nbar_sync(NB_TAB, kTabT);
+            nbar_sync(NB_TAB, kTabT);                        // A, P and T's diagonal blocks complete
             // ---- off-diagonal blocks.  With H_ik = T_ii A_ik (i > k), stored in A's unused
             //      upper block (k, i): T_ij = -sum_{k=j}^{i-1} H_ik T_kj, by levels i - j = 1, 2, 3.
             //      Each 16 x 8 half of an output block is one warp's mma.sync tile (f32 operands

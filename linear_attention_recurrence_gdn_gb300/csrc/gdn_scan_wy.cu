@@ -604,15 +604,24 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                 ss[bk] = fmaf(o[4 * bk + 2], o[4 * bk + 2], ss[bk]);
                 ss[bk] = fmaf(o[4 * bk + 3], o[4 * bk + 3], ss[bk]);
             }
+            // the sums over the 8 lanes of a token class (lane 4 j + ti, j = 0..7) by halving
+            // exchanges: after the exchange across lane bit 4 + m a lane keeps the blocks whose
+            // bit m matches its own, so lane j ends with blocks 2 j, 2 j + 1 summed (14 shuffles)
+            const int rj = lane >> 2;
 #pragma unroll
-            for (int m = 4; m <= 16; m <<= 1) {
+            for (int m = 2, cnt = 8; m >= 0; m--, cnt >>= 1) {
+                const bool up = (rj >> m) & 1;
 #pragma unroll
-                for (int bk = 0; bk < 16; bk++) ss[bk] += __shfl_xor_sync(0xffffffffu, ss[bk], m);
+                for (int i = 0; i < 8; i++) {
+                    if (i < cnt) {
+                        const float send = up ? ss[i] : ss[i + cnt];
+                        const float keep = up ? ss[i + cnt] : ss[i];
+                        ss[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4 << m);
+                    }
+                }
             }
-            if (lane < 4) {
-#pragma unroll
-                for (int bk = 0; bk < 16; bk++) sc.red[q4][4 * bk + lane] = ss[bk];
-            }
+            sc.red[q4][4 * (2 * rj) + ti] = ss[0];
+            sc.red[q4][4 * (2 * rj + 1) + ti] = ss[1];
             nbar_sync(NB_EPI, 128);
             if (etid < kC)
                 sc.rr[etid] = rsqrtf(fmaf(sc.red[0][etid] + sc.red[1][etid] + sc.red[2][etid] +

@@ -19,7 +19,8 @@
 //     as the A operand of [X | Y], X^T = U^T - S W^T (the corrections d of the chunk, one column
 //     per token), Y^T = S Q^T scaled per token and accumulated with the intra-chunk term into
 //     o, the corrections as A operands of the update and of the intra-chunk output, and one
-//     scratch region for the chunk tables [K;Q] K^T (W^T passes through X's columns);
+//     scratch region for the chunk tables [K;Q] K^T (W^T passes through the update
+//     operand's columns between an update and the next chunk's corrections);
 //   * every chunk-sized product is a tcgen05 MMA (kind::f16, M = 128, f32 accumulation) issued
 //     by one elected lane; f32 values enter as hi + lo pairs of the activation type (hi.hi +
 //     hi.lo + lo.hi, about 2^-16 relative per product for bf16), raw k, q, v are exact
@@ -80,9 +81,10 @@ constexpr int kThreads = 32 * kWarps;
 enum : uint32_t {
     TM_S = 0,        // f32 memory, 128 columns
     TM_SHI = 128,    // hi part of S as packed pairs (K = 128 in 64 columns)
-    TM_X = 192,      // W^T (lanes = j), then U^T - S W^T: the corrections d, one column per token
+    TM_X = 192,      // U^T - S W^T: the corrections d, one column per token
     TM_YO = 256,     // S Q^T, scaled per token, plus the intra-chunk term: o
-    TM_VCH = 320, TM_VCL = 352,   // update operand: d_s rk_s G_63 / G_s, hi / lo (K = 64 tokens)
+    TM_VCH = 320, TM_VCL = 352,   // update operand: d_s rk_s G_63 / G_s, hi / lo (K = 64 tokens);
+                                  // between the update and the next corrections: W^T (lanes = j)
     TM_VUH = 384, TM_VUL = 416,   // intra-chunk operand: d_s, hi / lo
     TM_SCR = 448,    // [K;Q] K^T (lanes 0-63: k rows, 64-127: q rows)
     TM_COLS = 512
@@ -146,7 +148,7 @@ enum Bar {
     B_PFREE = 13,    // 2: intra-chunk output MMAs done (P buffer and o ready)
     B_SPLIT = 15,    // row warps: S split and scaled (4 arrivals)
     B_VP = 16,       // row warps: correction operands written (4)
-    B_WRDY = 17,     // row warps: -W in shared memory, W^T read out of X (4)
+    B_WRDY = 17,     // row warps: -W in shared memory, W^T read out (4)
     B_BU = 18,       // table warps: U's B operand written (4)
     B_YSC = 19,      // output warps: Y scaled (4)
     B_YOFREE = 20,   // output warps: o read out of tensor memory (4)
@@ -387,16 +389,16 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
         // ================================= row warps ======================================
         const int a = 32 * (warp & 3) + lane;              // memory row = tensor-memory lane
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        // -W of chunk n (row j = this thread's lane of W^T, held in X's columns until U^T of n
-        // overwrites them) into the MN-major B operand of X; the X MMAs of chunk n-1 have read
-        // the previous one
+        // -W of chunk n (row j = this thread's lane of W^T, held in the update operand's columns
+        // from the update of n-1 to the corrections of n) into the MN-major B operand of X; the
+        // X MMAs of chunk n-1 have read the previous one
         auto w_pass = [&](int n) {
             wait(B_WT, static_cast<unsigned>(n & 1));
             tc_fence_after();
 #pragma unroll 1
             for (int h = 0; h < 2; h++) {
                 float w[32];
-                tm_ld32(tl + TM_X + 32 * h, w);
+                tm_ld32(tl + TM_VCH + 32 * h, w);
 #pragma unroll
                 for (int gg = 0; gg < 4; gg++) {
                     uint32_t hi[4], lo[4];
@@ -899,16 +901,17 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             fence_proxy_async_smem();
             nbar_sync(NB_TAB, kTabT);                        // B operands complete (A is dead)
             if (warp == kTabW0) {
-                // W^T = K^T Bw^T into X's columns, once the corrections of n-1 are read out
-                if (uniform(n == 0 || wait(B_VP, static_cast<unsigned>((n - 1) & 1)))) {
+                // W^T = K^T Bw^T into the update operand's columns, once the update of n-1 has
+                // read them (U^T of n then goes into X without waiting for W's read-out)
+                if (uniform(n == 0 || wait(B_UPD, static_cast<unsigned>((n - 1) & 1)))) {
                     issued = true;
                     if (elect_one()) {
                         tc_fence_after();
 #pragma unroll 1
                         for (int kt = 0; kt < 4; kt++) {
                             const uint64_t ak = desc_mn(slot + kt * 2048, 2 * kBox);
-                            umma_ss(tmem + TM_X, ak, desc_k(a_bw + kt * 32), kIdN64Amn, kt > 0);
-                            umma_ss(tmem + TM_X, ak, desc_k(a_bw + kBox + kt * 32), kIdN64Amn, true);
+                            umma_ss(tmem + TM_VCH, ak, desc_k(a_bw + kt * 32), kIdN64Amn, kt > 0);
+                            umma_ss(tmem + TM_VCH, ak, desc_k(a_bw + kBox + kt * 32), kIdN64Amn, true);
                         }
                         umma_commit(&bar[B_WT]);
                     }
@@ -927,10 +930,11 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
     } else if (warp == kMmaW) {
         // ================================ MMA warp =======================================
         bool issued = false;
-        auto issue_u = [&](int n) {                        // U^T of chunk n into X, once W^T is read
+        // U^T of chunk n into X (the corrections of n-1 were read out before the update of
+        // n-1 was issued, earlier on this warp)
+        auto issue_u = [&](int n) {
             const bool ok = uniform(wait(B_BU, static_cast<unsigned>(n & 1)) &
-                                    wait(B_LDV, static_cast<unsigned>(n & 1)) &
-                                    wait(B_WRDY, static_cast<unsigned>(n & 1)));
+                                    wait(B_LDV, static_cast<unsigned>(n & 1)));
             if (ok) {
                 issued = true;
                 if (elect_one()) {

@@ -11,8 +11,10 @@
 // (rows padded to whole float4s and a bank-spreading stride); 1 to 8 adjacent threads own a
 // memory row and split its float4s.  Per token the k, q rows are staged and normalised with one block
 // reduction, the rows are updated in place, and the gated RMSNorm reduces over the head's rows.
-// A decode step is the same kernel with S = 1.  Plain loads and stores throughout: the operands
-// may sit at any element offset (pinned host memory under GDN_FLAG_HOST_IO included).
+// A decode step has its own kernel: the memory streams through shared memory in its dense
+// layout (16-byte copies wherever Dv Dk is a multiple of 4), with up to 4 heads per SM in
+// flight.  Plain loads and stores of the step's inputs and outputs: they may sit at any
+// element offset (pinned host memory under GDN_FLAG_HOST_IO included).
 #include <math.h>
 
 #include "gdn_common.cuh"
@@ -72,7 +74,7 @@ __device__ __forceinline__ void block_sum3(float &a, float &b, float &c, float *
 }
 
 template <typename TA>
-__global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_params p, bool decode) {
+__global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_params p) {
     extern __shared__ __align__(16) float gsm[];
     const int Dk = p.Dk, Dv = p.Dv, S = p.S;
     const int TPR = gen_tpr(Dv), dk4 = gen_dk4(Dk), ld = gen_ld(Dk, Dv), nc = dk4 / 4;
@@ -89,11 +91,11 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_p
     const bool live = a < Dv;
     const int64_t mem = static_cast<int64_t>(Dv) * Dk;
 
-    // the memory: a decode step updates `state` in place; a scan starts from s0 (or zeros).
-    // A warp per row at a time, lanes along the row (coalesced), as 4-byte asynchronous copies
-    // that are all in flight at once; the padding columns are zeroed.
+    // the memory from s0 (or zeros): a warp per row at a time, lanes along the row (coalesced),
+    // as 4-byte asynchronous copies that are all in flight at once; the padding columns are
+    // zeroed
     const int warp = tid >> 5, lane = tid & 31;
-    const float *from = decode ? p.state : p.s0;
+    const float *from = p.s0;
     for (int r = warp; r < Dv; r += kGenWarps) {
         const float *src = from ? from + head * mem + static_cast<int64_t>(r) * Dk : nullptr;
         for (int c = lane; c < ld; c += 32) {
@@ -204,14 +206,135 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_p
     }
 }
 
+// One decode step (S = 1) for a head: the same arithmetic as the scan kernel's token, on the
+// memory in its dense [Dv][Dk] layout in shared memory.  The memory's copy in is issued first
+// and lands while the k, q norms are reduced; the row walks read scalars (a row of odd Dk is
+// not float4-aligned); the memory goes back by 16-byte stores where it can.  At most 64
+// registers a thread, so 4 CTAs share an SM when their memory fits.
+template <typename TA>
+__global__ void __launch_bounds__(kGenThreads, 4) gdn_general_decode_kernel(const gdn_params p) {
+    extern __shared__ __align__(16) float gsm[];
+    const int Dk = p.Dk, Dv = p.Dv;
+    const int TPR = gen_tpr(Dv), dk4 = gen_dk4(Dk);
+    const int64_t mem = static_cast<int64_t>(Dv) * Dk;
+    const int mem4 = static_cast<int>((mem + 3) / 4);
+    float *Sm = gsm;                                       // [Dv][Dk], dense
+    float *kh = Sm + 4 * mem4;                             // [dk4]
+    float *qh = kh + dk4;                                  // [dk4]
+    float *red = qh + dk4;                                 // [3][kGenWarps]
+    const int64_t head = blockIdx.x;                       // b * Hv + hv
+    const int b = static_cast<int>(head / p.Hv);
+    const int hv = static_cast<int>(head - static_cast<int64_t>(b) * p.Hv);
+    const int hk = hv / (p.Hv / p.Hk);
+    const int tid = threadIdx.x;
+    const int a = tid / TPR, part = tid - a * TPR;
+    const bool live = a < Dv;
+    float *gmem = p.state + head * mem;
+    // 16-byte copies when every head's memory starts on a 16-byte boundary (state is)
+    const bool vec = (mem & 3) == 0;
+    if (vec) {
+        for (int i = tid; i < mem4; i += kGenThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                             static_cast<uint32_t>(__cvta_generic_to_shared(Sm + 4 * i))),
+                         "l"(gmem + 4 * i)
+                         : "memory");
+    } else {
+        for (int i = tid; i < mem; i += kGenThreads)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                             static_cast<uint32_t>(__cvta_generic_to_shared(Sm + i))),
+                         "l"(gmem + i)
+                         : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    // the step's inputs while the memory lands
+    const TA *q = static_cast<const TA *>(p.q), *k = static_cast<const TA *>(p.k);
+    const TA *v = static_cast<const TA *>(p.v), *z = static_cast<const TA *>(p.z);
+    const bool gated = z != nullptr;
+    // with one token both layouts put head (b, h) at b * H + h
+    const int64_t ko = (static_cast<int64_t>(b) * p.Hk + hk) * Dk;
+    const int64_t vo = (static_cast<int64_t>(b) * p.Hv + hv) * Dv;
+    const int64_t go = static_cast<int64_t>(b) * p.Hv + hv;
+    const float kt = tid < Dk ? to_f32(k[ko + tid]) : 0.f;
+    const float qt = tid < Dk ? to_f32(q[ko + tid]) : 0.f;
+    const float va = live ? to_f32(v[vo + a]) : 0.f;
+    const float za = (gated && live) ? to_f32(z[vo + a]) : 0.f;
+    const float alpha = expf(fmaxf(load_gate(p.log_decay, p.gate_dtype, go), kGenMinLogDecay));
+    const float beta = load_gate(p.beta, p.gate_dtype, go);
+    const float gna = (gated && live) ? p.gn[a] : 0.f;
+    if (tid < dk4) {
+        kh[tid] = kt;
+        qh[tid] = qt;
+    }
+    float skk = kt * kt, sqq = qt * qt, skq = kt * qt;
+    block_sum3(skk, sqq, skq, red);                        // also orders the kh, qh writes
+    const float rk = rsqrtf(skk + p.qk_eps);
+    const float rq = rsqrtf(sqq + p.qk_eps) * rsqrtf(static_cast<float>(Dk));
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    // row a: u, w against the raw rows (the row's TPR threads take every TPR-th element), then
+    // the update with k^ = rk k
+    float *row = Sm + static_cast<int64_t>(live ? a : 0) * Dk;
+    float uu = 0.f, ww = 0.f;
+    if (live) {
+#pragma unroll 4
+        for (int c = part; c < Dk; c += TPR) {
+            const float s = row[c];
+            uu = fmaf(s, kh[c], uu);
+            ww = fmaf(s, qh[c], ww);
+        }
+    }
+    for (int off = 1; off < TPR; off <<= 1) {              // the row's threads are adjacent lanes
+        uu += __shfl_xor_sync(0xffffffffu, uu, off);
+        ww += __shfl_xor_sync(0xffffffffu, ww, off);
+    }
+    float o = 0.f;
+    if (live) {
+        const float u = uu * rk, w = ww * rq;
+        const float coef = beta * (va - alpha * u);
+        const float ck = coef * rk;
+#pragma unroll 4
+        for (int c = part; c < Dk; c += TPR) row[c] = fmaf(alpha, row[c], ck * kh[c]);
+        o = fmaf(alpha, w, coef * (skq * rk * rq));
+    }
+    float ya = o;
+    if (gated) {
+        const float g = live ? o * silu(za) : 0.f;
+        float ss = part == 0 ? g * g : 0.f, unused1 = 0.f, unused2 = 0.f;
+        block_sum3(ss, unused1, unused2, red);
+        ya = g * rsqrtf(fmaf(ss, 1.0f / static_cast<float>(Dv), p.norm_eps)) * gna;
+    }
+    if (live && part == 0) p.y[vo + a] = ya;
+    __syncthreads();                                       // every row updated
+    if (vec) {
+        float4 *dst = reinterpret_cast<float4 *>(gmem);
+        const float4 *src = reinterpret_cast<const float4 *>(Sm);
+        for (int i = tid; i < mem4; i += kGenThreads) dst[i] = src[i];
+    } else {
+        for (int i = tid; i < mem; i += kGenThreads) gmem[i] = Sm[i];
+    }
+}
+
+size_t general_decode_smem_bytes(int dk, int dv) {
+    return sizeof(float) * (4 * ((static_cast<size_t>(dv) * dk + 3) / 4) + 2 * static_cast<size_t>(gen_dk4(dk)) +
+                            3 * kGenWarps);
+}
+
 template <typename TA>
 cudaError_t launch_general_typed(const gdn_params &p, bool decode, cudaStream_t stream) {
+    const int64_t heads = static_cast<int64_t>(p.B) * p.Hv;
+    if (decode) {
+        const int bytes = static_cast<int>(general_decode_smem_bytes(p.Dk, p.Dv));
+        cudaError_t e = cudaFuncSetAttribute(gdn_general_decode_kernel<TA>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        gdn_general_decode_kernel<TA><<<static_cast<unsigned>(heads), kGenThreads, bytes, stream>>>(p);
+        return cudaGetLastError();
+    }
     const int bytes = static_cast<int>(general_smem_bytes(p.Dk, p.Dv));
     cudaError_t e = cudaFuncSetAttribute(gdn_general_kernel<TA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    const int64_t heads = static_cast<int64_t>(p.B) * p.Hv;
-    gdn_general_kernel<TA><<<static_cast<unsigned>(heads), kGenThreads, bytes, stream>>>(p, decode);
+    gdn_general_kernel<TA><<<static_cast<unsigned>(heads), kGenThreads, bytes, stream>>>(p);
     return cudaGetLastError();
 }
 

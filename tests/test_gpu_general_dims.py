@@ -134,3 +134,20 @@ def test_general_dims_host_fed_decode():
     assert not y.is_cuda
     yr, sr = oracle_ref(inp)
     assert rel_err(y, yr) <= DECODE_TOL and rel_err(state, sr) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("Dk,Dv,B,Hv", [(40, 24, 8, 96), (200, 196, 2, 100), (9, 7, 4, 64)],
+                         ids=["small_heads", "large_heads", "scalar_copies"])
+def test_general_dims_decode_many_heads(Dk, Dv, B, Hv):
+    # the general decode kernel over many heads: several resident per SM (small memories), one
+    # per SM in waves (large), and the memory by 4-byte copies (Dv Dk not a multiple of 4)
+    w = small_workload(B=B, S=1, Hk=Hv // 4, Hv=Hv, Dk=Dk, Dv=Dv, act="bf16", seed=905 + Dk,
+                       s0_std=0.1)
+    inp = make_inputs(w)
+    d = to_dev(inp)
+    state = d["s0"].clone()
+    y = gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["log_decay"], d["beta"], state,
+                            z=d["z"], gn=d["gn"])
+    torch.cuda.synchronize()
+    yr, sr = oracle_ref(inp)
+    assert rel_err(y, yr) <= DECODE_TOL and rel_err(state, sr) <= DECODE_TOL

@@ -339,7 +339,7 @@ def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
     Through the binding's HostDecodeStep: the per-step inputs (q, k, v, z, log_decay, beta)
     sit in one pinned host buffer and y in pinned host memory; a step is one C-ABI call with
     GDN_FLAG_HOST_IO, whose kernel reads the inputs from host memory and writes y there over
-    the chip-to-chip link, then a stream synchronize.
+    the chip-to-chip link, then a wait on an event recorded behind it.
     """
     inp = make_inputs(w)
     names = ["q", "k", "v", "z", "log_decay", "beta"]
@@ -361,7 +361,7 @@ def e2e_decode(gdn, w: Workload, dev, steps: int, world: int):
             "steps": steps, "ms_per_step": 1e3 * sec / steps,
             "note": "state resident in HBM; per step one C-ABI call reading the inputs from "
                     "pinned host memory and writing y to pinned host memory "
-                    "(GDN_FLAG_HOST_IO), then a stream synchronize"}
+                    "(GDN_FLAG_HOST_IO), then a wait on an event recorded behind it"}
 
 
 # ------------------------------------------------------------------------------ scan

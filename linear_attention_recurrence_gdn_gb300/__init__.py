@@ -356,8 +356,8 @@ class HostDecodeStep:
     The step's inputs (q, k, v, z, log_decay, beta) sit in one pinned host buffer (views in
     :attr:`host`, each input 256-byte aligned) and y in pinned :attr:`y_host`.  :meth:`run`
     is one C-ABI call with GDN_FLAG_HOST_IO, whose kernel reads each head's inputs from host
-    memory and writes y there, and one stream synchronisation.  Write a step's inputs into
-    :attr:`host` before calling :meth:`run`.
+    memory and writes y there, and one wait on an event recorded behind it.  Write a step's
+    inputs into :attr:`host` before calling :meth:`run`.
 
     ``like`` holds tensors with the step's shapes and dtypes (S == 1, per ``head_major``);
     ``z`` and ``gn`` are both given or both omitted (raw o).  ``state`` (updated in place) and
@@ -392,6 +392,7 @@ class HostDecodeStep:
                                    qk_eps=qk_eps, norm_eps=norm_eps, flags=GDN_FLAG_HOST_IO)
         self._lib = library()
         self._device = state.device
+        self._done = torch.cuda.Event()
 
     def run(self, sync: bool = True, stream: torch.cuda.Stream | None = None):
         """One step on ``stream`` (a torch CUDA stream; default: the current stream); returns
@@ -400,5 +401,8 @@ class HostDecodeStep:
         st = self._lib.gdn_decode_step(ctypes.byref(self._params), s.cuda_stream)
         _raise(self._lib, st, self._params, 1)
         if sync:
-            s.synchronize()
+            # an event recorded behind the step and waited on (measured ~3 us a step quicker
+            # than a stream synchronize on GB300)
+            self._done.record(s)
+            self._done.synchronize()
         return self.y_host

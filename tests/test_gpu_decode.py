@@ -109,6 +109,28 @@ def test_host_decode_step_over_several_steps(head_major, gated, act):
     assert rel_err(state, sr) <= DECODE_TOL
 
 
+def test_host_decode_step_on_its_own_stream():
+    # a stepper bound to a side stream, and one step on another stream named in run()
+    steps = 3
+    w = small_workload(B=2, S=steps, Hk=2, Hv=4, D=128, act="bf16", seed=660, s0_std=0.05)
+    inp = make_inputs(w)
+    names = ["q", "k", "v", "log_decay", "beta", "z"]
+    step_in = lambda t: {n: inp[n].narrow(1, t, 1).contiguous() for n in names}
+    state = inp["s0"].to("cuda")
+    gn = inp["gn"].to("cuda")
+    side, other = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    stepper = gdn.HostDecodeStep(step_in(0), state, gn, stream=side)
+    ys = []
+    for t in range(steps):
+        for n, x in step_in(t).items():
+            stepper.host[n].copy_(x)
+        ys.append(stepper.run(stream=other if t == 1 else None).clone())
+    yr, sr = oracle_ref(inp)
+    assert rel_err(torch.cat(ys, 1), yr) <= DECODE_TOL
+    assert rel_err(state, sr) <= DECODE_TOL
+
+
 @pytest.mark.parametrize("placement", ["inputs_host", "y_host", "all_host"])
 @pytest.mark.parametrize("dims", [(128, 128), (64, 256), (256, 80)], ids=lambda d: f"{d[0]}x{d[1]}")
 def test_decode_host_io_placements(placement, dims):

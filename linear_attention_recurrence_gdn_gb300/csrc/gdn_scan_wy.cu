@@ -149,7 +149,7 @@ enum Bar {
     B_SPLIT = 15,    // row warps: S split and scaled (4 arrivals)
     B_VP = 16,       // row warps: correction operands written (4)
     B_WRDY = 17,     // row warps: -W in shared memory, W^T read out (4)
-    B_BU = 18,       // table warps: U's B operand written (4)
+    B_BU = 18,       // table warps: U's B operand, the chunk's cvec and Y scales written (4)
     B_YSC = 19,      // output warps: Y scaled (4)
     B_YOFREE = 20,   // output warps: o read out of tensor memory (4)
     B_DRAIN = 21,    // 2: final commits of the two MMA-issuing warps
@@ -465,7 +465,10 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
         w_pass(0);
         for (int c = 0; c < nch; c++) {
             const int pb = c & 1;
-            // corrections d_t = X[a][t] -> intra-chunk operand (d) and update operand (d cvec)
+            // corrections d_t = X[a][t] -> intra-chunk operand (d) and update operand (d cvec);
+            // cvec and the scales of Y are the table warps', published by their B_BU arrivals
+            // of chunk c (complete before U, so before X, of chunk c)
+            wait(B_BU, static_cast<unsigned>(c & 1));
             wait(B_X, static_cast<unsigned>(c & 1));
             tc_fence_after();
 #pragma unroll 1
@@ -489,8 +492,6 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
             arrive_warp(B_VP);
 
             // S q_t scaled by e^{cum_t} rq_t, in place, before the intra-chunk term is added
-            // (the scales are the table warps', published by their B_BU arrivals of chunk c)
-            wait(B_BU, static_cast<unsigned>(c & 1));
             wait(B_Y, static_cast<unsigned>(c & 1));
             tc_fence_after();
 #pragma unroll 1

@@ -850,16 +850,31 @@ gdn_scan_wy_kernel(const __grid_constant__ gdn_params p, const __grid_constant__
                     tile_store(Hb + 16 * k * kAS + 16 * i + n0, kAS, d, 1.f, lane);
                 }
                 nbar_sync(NB_TAB, kTabT);
+                // Level 3 (block (3, 0)) has three terms; warps 4 and 5, idle in level 2, sum the
+                // first two there (T_00, T_10 are known after level 1) and keep them in
+                // registers, so level 3 adds only H_32 T_20.
+                float d30[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                 for (int L = 1; L < 4; L++) {
                     const int ntask = 2 * (4 - L);         // blocks (j + L, j), two halves each
-                    if (tw < ntask) {
+                    if (L < 3 && tw < ntask) {
                         const int j = tw >> 1, i = j + L, n0 = 8 * (tw & 1);
                         float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                         for (int k = j; k < i; k++)
                             tile_mma(d, Hb + 16 * k * kAS + 16 * i, kAS, Tb + blk(k, j) * 256 + n0, 16, lane);
                         tile_store(Tb + blk(i, j) * 256 + n0, 16, d, -1.f, lane);
+                    }
+                    if (tw >= 4) {
+                        const int n0 = 8 * (tw & 1);
+                        if (L == 2) {
+#pragma unroll 1
+                            for (int k = 0; k < 2; k++)
+                                tile_mma(d30, Hb + 16 * k * kAS + 48, kAS, Tb + blk(k, 0) * 256 + n0, 16, lane);
+                        } else if (L == 3) {
+                            tile_mma(d30, Hb + 32 * kAS + 48, kAS, Tb + blk(2, 0) * 256 + n0, 16, lane);
+                            tile_store(Tb + blk(3, 0) * 256 + n0, 16, d30, -1.f, lane);
+                        }
                     }
                     nbar_sync(NB_TAB, kTabT);
                 }

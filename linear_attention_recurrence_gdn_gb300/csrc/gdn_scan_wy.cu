@@ -28,16 +28,18 @@
 //   * k, q, v arrive by tensor-map copies (TMA, 64 tokens x 64 features per box, 128-byte
 //     swizzle) into shared memory, two chunks of k, q resident; the load warp prefetches their
 //     rows (and z's) into L2 two chunks ahead, since a box of 64 strided rows is slow to land;
-//   * warp roles: 4 row warps (the serial chain: split of S into hi / lo, the corrections,
-//     the per-token scale of Y, -W into shared memory), 4 output warps (o, the gated RMSNorm
-//     and the y stores), 6 table warps (q norms while the chunk tables MMA runs, then tables
+//   * warp roles: 4 row warps (the serial chain: the corrections, the per-token scale of Y,
+//     the next chunk's split of S into hi / lo, -W into shared memory), 4 output warps (o; for
+//     the gated RMSNorm o turned through a small shared-memory tile so a lane holds 4 rows of
+//     one token; the y stores), 6 table warps (q norms while the chunk tables MMA runs, then tables
 //     -> A, rk, P, the unit-triangular inverse T in 16 x 16 blocks, the B operands of U and W;
 //     one of them issues the tables and W^T MMAs), one MMA warp (the chain's MMAs), one load
 //     warp (the copies and the decay products of each chunk);
 //   * the table warps work one chunk ahead, so the chain per chunk is: split S -> X MMAs ->
 //     corrections -> update MMAs.
-// Every wait is an mbarrier wait with a time limit: a wait that runs out sets the watchdog
-// word and is retried once with the full limit; if that also runs out the CTA abandons its
+// Every wait is an mbarrier wait: a phase already complete is taken by an inline test, else
+// the wait has a time limit; a wait that runs out sets the watchdog word and is retried once
+// with the full limit; if that also runs out the CTA abandons its
 // work (later waits return at once, no new copies or MMAs, no stores), drains the MMAs and
 // copies it issued, frees its tensor memory and returns.
 #include <cuda.h>

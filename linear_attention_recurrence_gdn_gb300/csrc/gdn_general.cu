@@ -206,6 +206,173 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_kernel(const gdn_p
     }
 }
 
+// The scan in chunks of C tokens (C a power of two up to 32, as many as shared memory takes):
+// the arithmetic of the kernel above, reordered so that nothing waits per token but the row
+// walks.  Per chunk: every token's k, q rows are normalised at once (a warp per token; k^ and
+// q^ / sqrt(Dk) into shared memory with k^ . q^, the gates, v and z), then the tokens run one
+// after another, each row's threads updating their own row with no barrier between tokens,
+// and the outputs o_t of the chunk wait in shared memory for the gated RMSNorm, a warp per
+// token, which also stores y.
+template <typename TA>
+__global__ void __launch_bounds__(kGenThreads, 1) gdn_general_chunk_kernel(const gdn_params p, int C) {
+    extern __shared__ __align__(16) float gsm[];
+    const int Dk = p.Dk, Dv = p.Dv, S = p.S;
+    const int TPR = gen_tpr(Dv), dk4 = gen_dk4(Dk), ld = gen_ld(Dk, Dv), nc = dk4 / 4;
+    float *Sm = gsm;                                       // [Dv][ld]
+    float *KH = Sm + Dv * ld;                              // [C][dk4]: k_t rk_t
+    float *QH = KH + C * dk4;                              // [C][dk4]: q_t rq_t / sqrt(Dk)
+    float *VB = QH + C * dk4;                              // [C][Dv]: v
+    float *ZB = VB + C * Dv;                               // [C][Dv]: z
+    float *OB = ZB + C * Dv;                               // [C][Dv]: o, then o silu(z)
+    float *AL = OB + C * Dv;                               // [C]: alpha
+    float *BE = AL + C;                                    // [C]: beta
+    float *KQ = BE + C;                                    // [C]: k^ . q^
+    const int64_t head = blockIdx.x;                       // b * Hv + hv
+    const int b = static_cast<int>(head / p.Hv);
+    const int hv = static_cast<int>(head - static_cast<int64_t>(b) * p.Hv);
+    const int hk = hv / (p.Hv / p.Hk);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int a = tid / TPR, part = tid - a * TPR;         // this thread's row and column part
+    const bool live = a < Dv;
+    const int64_t mem = static_cast<int64_t>(Dv) * Dk;
+
+    // the memory from s0 (or zeros), as in the kernel above
+    for (int r = warp; r < Dv; r += kGenWarps) {
+        const float *src = p.s0 ? p.s0 + head * mem + static_cast<int64_t>(r) * Dk : nullptr;
+        for (int c = lane; c < ld; c += 32) {
+            if (src && c < Dk) {
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                                 static_cast<uint32_t>(__cvta_generic_to_shared(Sm + r * ld + c))),
+                             "l"(src + c)
+                             : "memory");
+            } else {
+                Sm[r * ld + c] = 0.f;
+            }
+        }
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const TA *q = static_cast<const TA *>(p.q), *k = static_cast<const TA *>(p.k);
+    const TA *v = static_cast<const TA *>(p.v), *z = static_cast<const TA *>(p.z);
+    const bool gated = z != nullptr;
+    const float qscale = rsqrtf(static_cast<float>(Dk));
+    float4 *row4 = reinterpret_cast<float4 *>(Sm + (live ? a : 0) * ld);
+    auto kq_off = [&](int t) {
+        return p.head_major ? ((static_cast<int64_t>(b) * p.Hk + hk) * S + t) * Dk
+                            : ((static_cast<int64_t>(b) * S + t) * p.Hk + hk) * Dk;
+    };
+    auto v_off = [&](int t) {
+        return p.head_major ? ((static_cast<int64_t>(b) * p.Hv + hv) * S + t) * Dv
+                            : ((static_cast<int64_t>(b) * S + t) * p.Hv + hv) * Dv;
+    };
+    auto g_off = [&](int t) {
+        return p.head_major ? (static_cast<int64_t>(b) * p.Hv + hv) * S + t
+                            : (static_cast<int64_t>(b) * S + t) * p.Hv + hv;
+    };
+    for (int t0 = 0; t0 < S; t0 += C) {
+        const int nt = min(C, S - t0);
+        // the chunk's k, q rows normalised, a warp per token (Dk <= 256: 8 elements a lane)
+        for (int tt = warp; tt < nt; tt += kGenWarps) {
+            const int64_t ko = kq_off(t0 + tt);
+            float kv[8], qv[8], sk = 0.f, sq = 0.f, skq = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int c = lane + 32 * i;
+                kv[i] = c < Dk ? to_f32(k[ko + c]) : 0.f;
+                qv[i] = c < Dk ? to_f32(q[ko + c]) : 0.f;
+                sk = fmaf(kv[i], kv[i], sk);
+                sq = fmaf(qv[i], qv[i], sq);
+                skq = fmaf(kv[i], qv[i], skq);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                skq += __shfl_xor_sync(0xffffffffu, skq, off);
+            }
+            const float rk = rsqrtf(sk + p.qk_eps);
+            const float rq = rsqrtf(sq + p.qk_eps) * qscale;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int c = lane + 32 * i;
+                if (c < dk4) {
+                    KH[tt * dk4 + c] = kv[i] * rk;
+                    QH[tt * dk4 + c] = qv[i] * rq;
+                }
+            }
+            if (lane == 0) {
+                const int64_t go = g_off(t0 + tt);
+                KQ[tt] = skq * rk * rq;
+                AL[tt] = expf(fmaxf(load_gate(p.log_decay, p.gate_dtype, go), kGenMinLogDecay));
+                BE[tt] = load_gate(p.beta, p.gate_dtype, go);
+            }
+        }
+        for (int i = tid; i < nt * Dv; i += kGenThreads) {  // v and z rows of the chunk
+            const int tt = i / Dv, r = i - tt * Dv;
+            const int64_t vo = v_off(t0 + tt);
+            VB[i] = to_f32(v[vo + r]);
+            if (gated) ZB[i] = to_f32(z[vo + r]);
+        }
+        __syncthreads();
+        // the tokens in order: each row's TPR threads own it, so no barrier between tokens
+        for (int tt = 0; tt < nt; tt++) {
+            const float4 *kh4 = reinterpret_cast<const float4 *>(KH + tt * dk4);
+            const float4 *qh4 = reinterpret_cast<const float4 *>(QH + tt * dk4);
+            float uu = 0.f, ww = 0.f;
+            if (live) {
+#pragma unroll 4
+                for (int c = part; c < nc; c += TPR) {
+                    const float4 s4 = row4[c];
+                    uu = dot4(s4, kh4[c], uu);
+                    ww = dot4(s4, qh4[c], ww);
+                }
+            }
+            for (int off = 1; off < TPR; off <<= 1) {      // the row's threads are adjacent lanes
+                uu += __shfl_xor_sync(0xffffffffu, uu, off);
+                ww += __shfl_xor_sync(0xffffffffu, ww, off);
+            }
+            if (live) {
+                const float alpha = AL[tt];
+                const float coef = BE[tt] * (VB[tt * Dv + a] - alpha * uu);
+#pragma unroll 4
+                for (int c = part; c < nc; c += TPR) {
+                    const float4 s4 = row4[c], k4 = kh4[c];
+                    row4[c] = make_float4(fmaf(alpha, s4.x, coef * k4.x), fmaf(alpha, s4.y, coef * k4.y),
+                                          fmaf(alpha, s4.z, coef * k4.z), fmaf(alpha, s4.w, coef * k4.w));
+                }
+                if (part == 0) OB[tt * Dv + a] = fmaf(alpha, ww, coef * KQ[tt]);
+            }
+        }
+        __syncthreads();
+        // the gated RMSNorm (or raw o) and the y stores, a warp per token
+        for (int tt = warp; tt < nt; tt += kGenWarps) {
+            float *yo = p.y + v_off(t0 + tt);
+            float *ob = OB + tt * Dv;
+            if (gated) {
+                const float *zb = ZB + tt * Dv;
+                float ss = 0.f;
+                for (int r = lane; r < Dv; r += 32) {
+                    const float g = ob[r] * silu(zb[r]);
+                    ob[r] = g;
+                    ss = fmaf(g, g, ss);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float rr = rsqrtf(fmaf(ss, 1.0f / static_cast<float>(Dv), p.norm_eps));
+                for (int r = lane; r < Dv; r += 32) yo[r] = ob[r] * rr * p.gn[r];
+            } else {
+                for (int r = lane; r < Dv; r += 32) yo[r] = ob[r];
+            }
+        }
+        __syncthreads();                                   // the chunk's buffers are rewritten next
+    }
+    // the final memory
+    for (int r = warp; r < Dv; r += kGenWarps) {
+        float *dst = p.state + head * mem + static_cast<int64_t>(r) * Dk;
+        for (int c = lane; c < Dk; c += 32) dst[c] = Sm[r * ld + c];
+    }
+}
+
 // One decode step (S = 1) for a head: the same arithmetic as the scan kernel's token, on the
 // memory in its dense [Dv][Dk] layout in shared memory.  The memory's copy in is issued first
 // and lands while the k, q norms are reduced; the row walks read scalars (a row of odd Dk is
@@ -314,6 +481,11 @@ __global__ void __launch_bounds__(kGenThreads, 4) gdn_general_decode_kernel(cons
     }
 }
 
+size_t general_chunk_smem_bytes(int dk, int dv, int c) {
+    return sizeof(float) * (static_cast<size_t>(dv) * gen_ld(dk, dv) +
+                            static_cast<size_t>(c) * (2 * static_cast<size_t>(gen_dk4(dk)) + 3 * static_cast<size_t>(dv) + 3));
+}
+
 size_t general_decode_smem_bytes(int dk, int dv) {
     return sizeof(float) * (4 * ((static_cast<size_t>(dv) * dk + 3) / 4) + 2 * static_cast<size_t>(gen_dk4(dk)) +
                             3 * kGenWarps);
@@ -328,6 +500,18 @@ cudaError_t launch_general_typed(const gdn_params &p, bool decode, cudaStream_t 
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
         gdn_general_decode_kernel<TA><<<static_cast<unsigned>(heads), kGenThreads, bytes, stream>>>(p);
+        return cudaGetLastError();
+    }
+    // the chunked scan with the most tokens a chunk (up to 32) that fit; a head whose memory
+    // leaves no room even for one token's buffers takes the token-by-token kernel
+    int C = 32;
+    while (C > 1 && general_chunk_smem_bytes(p.Dk, p.Dv, C) > kGeneralSmemMax) C /= 2;
+    if (general_chunk_smem_bytes(p.Dk, p.Dv, C) <= kGeneralSmemMax) {
+        const int bytes = static_cast<int>(general_chunk_smem_bytes(p.Dk, p.Dv, C));
+        cudaError_t e = cudaFuncSetAttribute(gdn_general_chunk_kernel<TA>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        gdn_general_chunk_kernel<TA><<<static_cast<unsigned>(heads), kGenThreads, bytes, stream>>>(p, C);
         return cudaGetLastError();
     }
     const int bytes = static_cast<int>(general_smem_bytes(p.Dk, p.Dv));

@@ -9,8 +9,10 @@
 //     o = alpha w + coef (k^ . q^),  y = rmsnorm(o * silu(z)) * gn   (or y = o without z).
 // One CTA per (b, hv) head keeps the head's f32 memory in shared memory for the whole sequence
 // (rows padded to whole float4s and a bank-spreading stride); 1 to 8 adjacent threads own a
-// memory row and split its float4s.  Per token the k, q rows are staged and normalised with one block
-// reduction, the rows are updated in place, and the gated RMSNorm reduces over the head's rows.
+// memory row and split its float4s.  The scan runs in chunks of up to 32 tokens (the chunk's
+// k, q norms at once, its tokens' row updates in place back to back, then the gated RMSNorm a
+// warp per token); a memory too large for the chunk buffers goes token by token, with block
+// reductions for the norms.
 // A decode step has its own kernel: the memory streams through shared memory in its dense
 // layout (16-byte copies wherever Dv Dk is a multiple of 4), with up to 4 heads per SM in
 // flight.  Plain loads and stores of the step's inputs and outputs: they may sit at any

@@ -14,7 +14,7 @@
 // warp per token); a memory too large for the chunk buffers goes token by token, with block
 // reductions for the norms.
 // A decode step has its own kernel: the memory streams through shared memory in its dense
-// layout (16-byte copies wherever Dv Dk is a multiple of 4), with up to 4 heads per SM in
+// layout (16-byte copies wherever Dv Dk is a multiple of 4), with up to 7 heads per SM in
 // flight.  Plain loads and stores of the step's inputs and outputs: they may sit at any
 // element offset (pinned host memory under GDN_FLAG_HOST_IO included).
 #include <math.h>
@@ -378,10 +378,10 @@ __global__ void __launch_bounds__(kGenThreads, 1) gdn_general_chunk_kernel(const
 // One decode step (S = 1) for a head: the same arithmetic as the scan kernel's token, on the
 // memory in its dense [Dv][Dk] layout in shared memory.  The memory's copy in is issued first
 // and lands while the k, q norms are reduced; the row walks read scalars (a row of odd Dk is
-// not float4-aligned); the memory goes back by 16-byte stores where it can.  At most 64
-// registers a thread, so 4 CTAs share an SM when their memory fits.
+// not float4-aligned); the memory goes back by 16-byte stores where it can.  At most 32
+// registers a thread, so up to 7 CTAs share an SM when their memory fits.
 template <typename TA>
-__global__ void __launch_bounds__(kGenThreads, 4) gdn_general_decode_kernel(const gdn_params p) {
+__global__ void __launch_bounds__(kGenThreads, 7) gdn_general_decode_kernel(const gdn_params p) {
     extern __shared__ __align__(16) float gsm[];
     const int Dk = p.Dk, Dv = p.Dv;
     const int TPR = gen_tpr(Dv), dk4 = gen_dk4(Dk);
